@@ -1,0 +1,214 @@
+"""fp64 definitions of the chunk-step operators (test infrastructure only).
+
+Source for every function: HeyGen, "Avatar inference at scale" (see the
+package docstring for the sections).  Arrays are NumPy float64.  Token
+tensors are laid out [B][N][H][D] (batch, token, head, channel); a token n of
+a t x h x w latent chunk sits at row-major position (t, h, w).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+# --------------------------------------------------------------------------
+# 3D rotary position embedding
+# --------------------------------------------------------------------------
+
+def rope_axis_split(D: int):
+    """Number of rotary channel pairs given to the t, h and w axes.
+
+    Reading (pages silent): D/2 pairs are shared by the three latent axes, the
+    two spatial axes get floor(P/3) pairs each and time takes the rest, in the
+    channel order [t | h | w].
+    """
+    if D % 2:
+        raise ValueError("head_dim must be even")
+    P = D // 2
+    p_h = P // 3
+    p_w = P // 3
+    p_t = P - p_h - p_w
+    return p_t, p_h, p_w
+
+
+def rope_frequencies(n_pairs: int, base: float) -> np.ndarray:
+    """Angular frequency of each pair on one axis: omega_j = base**(-j/n_pairs).
+
+    Reading (pages silent): the usual rotary spectrum applied per axis, pair j
+    of an axis that owns n_pairs pairs turning at base**(-2j/d_a), d_a = 2*n_pairs.
+    """
+    j = np.arange(n_pairs, dtype=np.float64)
+    return np.power(float(base), -j / n_pairs)
+
+
+def token_positions(grid_t: int, grid_h: int, grid_w: int, t0: int = 0):
+    """(t, h, w) of each token of a grid_t x grid_h x grid_w block, row-major,
+    time starting at t0.  Chunk tokens use t0 = 0 (chunk-local time)."""
+    n = np.arange(grid_t * grid_h * grid_w)
+    t = t0 + n // (grid_h * grid_w)
+    h = (n // grid_w) % grid_h
+    w = n % grid_w
+    return t.astype(np.float64), h.astype(np.float64), w.astype(np.float64)
+
+
+def rope3d(x: np.ndarray, grid_t: int, grid_h: int, grid_w: int, t0: int = 0,
+           base: float = 10000.0) -> np.ndarray:
+    """Rotate every adjacent channel pair (x[2i], x[2i+1]) of x [B][N][H][D] by
+    the angle pos_axis * omega_j of the axis that owns pair i.
+
+    (a, b) -> (a cos th - b sin th, a sin th + b cos th).  N must equal
+    grid_t * grid_h * grid_w.
+    """
+    B, N, H, D = x.shape
+    if N != grid_t * grid_h * grid_w:
+        raise ValueError("token count does not match the grid")
+    p_t, p_h, p_w = rope_axis_split(D)
+    t, h, w = token_positions(grid_t, grid_h, grid_w, t0)
+    theta = np.concatenate(
+        [np.outer(t, rope_frequencies(p_t, base)),
+         np.outer(h, rope_frequencies(p_h, base)),
+         np.outer(w, rope_frequencies(p_w, base))], axis=1)  # [N][D/2]
+    c = np.cos(theta)[None, :, None, :]
+    s = np.sin(theta)[None, :, None, :]
+    a = x[..., 0::2]
+    b = x[..., 1::2]
+    out = np.empty_like(x, dtype=np.float64)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = a * s + b * c
+    return out
+
+
+# --------------------------------------------------------------------------
+# attention over [reference | boundary | chunk]
+# --------------------------------------------------------------------------
+
+def softmax_rows(s: np.ndarray) -> np.ndarray:
+    """Row-wise softmax, exp(s - max) / sum (the max only for range)."""
+    m = s.max(axis=-1, keepdims=True)
+    p = np.exp(s - m)
+    return p / p.sum(axis=-1, keepdims=True)
+
+
+def attention(q: np.ndarray, segments, scale: float | None = None) -> np.ndarray:
+    """O = softmax(q K^T * scale) V per (batch, head), K and V the
+    concatenation of the given (k, v) segments along the token axis.
+
+    q [B][Nq][H][D]; each segment k, v [B][n][H][D] (n may be 0).
+    Reading (pages silent): queries are the chunk tokens only, no mask, scale
+    1/sqrt(D) unless given.
+    """
+    B, Nq, H, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    ks = [k for k, _ in segments if k.shape[1] > 0]
+    vs = [v for k, v in segments if k.shape[1] > 0]
+    K = np.concatenate(ks, axis=1)
+    V = np.concatenate(vs, axis=1)
+    out = np.empty((B, Nq, H, D), dtype=np.float64)
+    for b in range(B):
+        for hh in range(H):
+            s = (q[b, :, hh, :] @ K[b, :, hh, :].T) * scale
+            out[b, :, hh, :] = softmax_rows(s) @ V[b, :, hh, :]
+    return out
+
+
+# --------------------------------------------------------------------------
+# output projection and the flow-matching Euler update
+# --------------------------------------------------------------------------
+
+def out_proj(o: np.ndarray, w_o: np.ndarray, bias: np.ndarray | None = None) -> np.ndarray:
+    """Velocity v = O W_o^T (+ bias); O [M][hid_in], W_o [hid_out][hid_in]."""
+    v = o @ w_o.T
+    if bias is not None:
+        v = v + bias[None, :]
+    return v
+
+
+def euler_update(x: np.ndarray, v: np.ndarray, dt: float) -> np.ndarray:
+    """One explicit Euler step of the flow ODE: x + dt * v.
+
+    Reading (pages silent beyond "flow matching" and "multi-step diffusion
+    pass"): time runs from noise to data with positive steps dt.
+    """
+    return x + dt * v
+
+
+def time_grid(steps: int, shift: float = 1.0) -> np.ndarray:
+    """Step sizes dt_0..dt_{S-1} of the sampling grid, summing to 1.
+
+    Noise levels sigma_i = 1 - i/S are warped by
+    sigma' = shift*sigma / (1 + (shift - 1)*sigma) and dt_i = sigma'_i - sigma'_{i+1}.
+    shift = 1 is the uniform grid.
+    """
+    if steps < 1 or shift <= 0:
+        raise ValueError("steps >= 1 and shift > 0 required")
+    sigma = 1.0 - np.arange(steps + 1, dtype=np.float64) / steps
+    warped = shift * sigma / (1.0 + (shift - 1.0) * sigma)
+    return warped[:-1] - warped[1:]
+
+
+# --------------------------------------------------------------------------
+# one chunk step and a stream of chunks
+# --------------------------------------------------------------------------
+
+def boundary_from_chunk(k_chunk: np.ndarray, v_chunk: np.ndarray, frame_tokens: int,
+                        boundary_frames: int, grid_h: int, grid_w: int, base: float):
+    """Boundary carried into the next chunk: the last ``boundary_frames``
+    frames of the finished chunk's K and V (before RoPE, taken from its final
+    denoising step), K rotated to t = -boundary_frames .. -1 of the next
+    chunk's local time.  Returns (k_rot, v)."""
+    n_b = boundary_frames * frame_tokens
+    N = k_chunk.shape[1]
+    k_tail = k_chunk[:, N - n_b:]
+    v_tail = v_chunk[:, N - n_b:]
+    return rope3d(k_tail, boundary_frames, grid_h, grid_w, -boundary_frames, base), v_tail.copy()
+
+
+def chunk_step(q, k, v, ref_k_rot, ref_v, bnd_k_rot, bnd_v, w_o, x, dt, grid, base=10000.0,
+               scale=None, bias=None):
+    """One denoising step of one chunk.
+
+    q, k, v: the chunk's tokens [B][Nq][H][D] before RoPE; ref_k_rot / bnd_k_rot
+    are already rotated; x [B*Nq][hid].  grid = (F, grid_h, grid_w).
+    Returns (x_next, O) with O [B][Nq][H][D].
+    """
+    F, gh, gw = grid
+    q_rot = rope3d(q, F, gh, gw, 0, base)
+    k_rot = rope3d(k, F, gh, gw, 0, base)
+    o = attention(q_rot, [(ref_k_rot, ref_v), (bnd_k_rot, bnd_v), (k_rot, v)], scale)
+    B, Nq, H, D = o.shape
+    vel = out_proj(o.reshape(B * Nq, H * D), w_o, bias)
+    return euler_update(x, vel, dt), o
+
+
+def run_stream(w, ref_k, ref_v, w_o, x0_per_chunk, step_inputs_fn, dts, scale=None, bias=None,
+               chunks=None):
+    """A stream of chunks: reference K rotated once (at t = ref_t), each chunk
+    run over the grid ``dts`` against [reference | boundary | chunk], the
+    boundary rolled from chunk to chunk.
+
+    step_inputs_fn(chunk, step) -> (q, k, v) float64 [B][Nq][H][D].
+    x0_per_chunk(chunk) -> float64 [B*Nq][hid].
+    Returns the list of final x per chunk and the list of boundaries used.
+    """
+    n_chunks = w.chunks if chunks is None else chunks
+    ref_k_rot = rope3d(ref_k, w.ref_frames, w.grid_h, w.grid_w,
+                       w.ref_t - w.ref_frames + 1, w.rope_base)
+    empty = np.zeros((w.B, 0, w.H, w.D))
+    bnd = (empty, empty)
+    xs, bnds = [], []
+    for c in range(n_chunks):
+        x = x0_per_chunk(c)
+        bnds.append(bnd)
+        last = None
+        for s, dt in enumerate(dts):
+            q, k, v = step_inputs_fn(c, s)
+            x, _ = chunk_step(q, k, v, ref_k_rot, ref_v, bnd[0], bnd[1], w_o, x, dt,
+                              (w.F, w.grid_h, w.grid_w), w.rope_base, scale, bias)
+            last = (k, v)
+        xs.append(x)
+        if w.boundary_frames > 0:
+            bnd = boundary_from_chunk(last[0], last[1], w.frame_tokens, w.boundary_frames,
+                                      w.grid_h, w.grid_w, w.rope_base)
+    return xs, bnds
