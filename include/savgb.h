@@ -1,0 +1,236 @@
+/*
+ * savgb.h - C ABI of the GB300 (sm_103a) chunk-step library.
+ *
+ * One denoising step of one video chunk of a chunked, flow-matching Diffusion
+ * Transformer avatar generator, as described in HeyGen, "Avatar inference at
+ * scale":
+ *   - section "The underlying model architecture": a DiT trained with flow
+ *     matching that attends to rich reference tokens; long videos are made
+ *     chunk by chunk, the first chunk relying on the static reference only,
+ *     later chunks also on boundary data from the previous chunk;
+ *   - section "The streaming framework and pipeline loop": the reference
+ *     identity is encoded once per request, then each chunk runs a multi-step
+ *     diffusion pass conditioned on the previous chunk's boundary frames;
+ *   - section "Constant memory over duration": only the static reference
+ *     conditioning and a minimal set of carried tensors live across chunks,
+ *     so peak GPU memory does not grow with session length.
+ * The pages state the problem, not the operators.  The operator readings
+ * this library implements are stated with each call below.
+ *
+ * Conventions shared by every call
+ *   Token tensors are bfloat16, laid out [B][N][H][D] (batch, token, head,
+ *   channel), i.e. row-major [B*N][H*D].  Token n of a t x h x w latent block
+ *   sits at (t0 + n / (h*w), (n / w) % h, n % w).
+ *   Device pointers are caller-owned; the library neither frees them nor keeps
+ *   them past the call.  Every device pointer must be 16-byte aligned.
+ *   `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *   enqueue work: they return after host-side validation and launch.  Errors
+ *   raised by a kernel on the device (a bounded wait that ran out) are
+ *   recorded in a per-device error word and reported by savgb_device_check()
+ *   or chunk_stream_sync().
+ *   Every call returns a savgb_status; on failure savgb_last_error() gives a
+ *   thread-local message.  Nothing throws across this boundary.  No call falls
+ *   back to the CPU.
+ */
+#ifndef SAVGB_H
+#define SAVGB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SAVGB_OK = 0,
+  SAVGB_ERR_INVALID_ARG = -1, /* a size, count or pointer is out of range */
+  SAVGB_ERR_UNSUPPORTED = -2, /* valid but not supported (e.g. head_dim not 64/128, no sm_103 device) */
+  SAVGB_ERR_ALIGNMENT = -3,   /* a pointer is not 16-byte aligned */
+  SAVGB_ERR_OOM = -4,         /* a device allocation failed */
+  SAVGB_ERR_CUDA = -5,        /* a CUDA runtime or driver call failed */
+  SAVGB_ERR_TIMEOUT = -6,     /* a kernel's bounded wait ran out (device error word) */
+  SAVGB_ERR_STATE = -7,       /* call out of order for a stream handle */
+} savgb_status;
+
+/* Human-readable name of a status code (static string). */
+const char* savgb_status_string(int status);
+/* Message of the last failing call on this thread ("" if none). */
+const char* savgb_last_error(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int savgb_version(void);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns SAVGB_ERR_TIMEOUT (with the kernel and wait that gave up in
+ * savgb_last_error()) if a kernel's bounded wait ran out since the last
+ * check, SAVGB_ERR_CUDA if the stream reports an error, else SAVGB_OK. */
+int savgb_device_check(void* stream);
+
+/* Diagnostic with no counterpart on the pages: launches one block that waits,
+ * through the same bounded wait the library's kernels use, on a barrier that
+ * nothing arrives on, for at most limit_ns nanoseconds (0 < limit_ns <= 1e10).
+ * A following savgb_device_check() then returns SAVGB_ERR_TIMEOUT.  It checks
+ * failure reporting without faulting or hanging the GPU. */
+int savgb_watchdog_selftest(uint64_t limit_ns, void* stream);
+
+/* --------------------------------------------------------------------------
+ * rope3d_apply - 3D (t, h, w) rotary position embedding.
+ *
+ * Positions of the latent tokens in time and space (the chunked latent video
+ * of "The underlying model architecture").  Reading: the D/2 channel pairs are
+ * split [t | h | w]; each spatial axis owns floor(D/6) pairs and time the rest
+ * (D=128: 22/21/21, D=64: 12/10/10).  Pair j of an axis with P pairs turns at
+ * omega_j = base^(-j/P) radians per position; the adjacent pair (a, b) becomes
+ * (a cos th - b sin th, a sin th + b cos th), th = pos * omega_j.
+ *
+ *   in, out   bf16 [B][n_tokens][H][D]; in == out is allowed (in place).
+ *   n_tokens  must equal grid_t * grid_h * grid_w (>= 1).
+ *   D         even, 8 <= D <= 256, D % 8 == 0.
+ *   t0        time of the first frame (chunk tokens 0, boundary -T_b, ...).
+ *   base      rotary base (> 0), typically 10000.
+ * Math in fp32 from the bf16 inputs; output rounded to bf16 (nearest even).
+ * Limits: grid_h, grid_w <= 4096, grid_t <= 4096 and the three angle tables
+ * (grid_t*P_t + grid_h*P_h + grid_w*P_w entries) fit 96 KiB of shared memory.
+ * ------------------------------------------------------------------------ */
+int rope3d_apply(const void* in, void* out, int B, int64_t n_tokens, int H, int D, int grid_t,
+                 int grid_h, int grid_w, int t0, double base, void* stream);
+
+/* One key/value segment: bf16 k and v, each [B][n_tokens][H][D] with the
+ * same B, H, D as the queries.  n_tokens may be 0 (then k and v are unused). */
+typedef struct {
+  const void* k;
+  const void* v;
+  int64_t n_tokens;
+} savgb_kv_segment;
+
+/* --------------------------------------------------------------------------
+ * chunk_attention - queries of the current chunk attend over the
+ * concatenation of up to three key/value segments, in practice
+ * [static reference | previous chunk's boundary | current chunk]
+ * ("The underlying model architecture": rich reference tokens and boundary
+ * data from previous segments; "The streaming framework and pipeline loop":
+ * the chunk is conditioned on the previous chunk's boundary frames).
+ *
+ * Reading: no mask; O = softmax(Q K^T * scale) V per (batch, head).
+ *   q        bf16 [B][n_q][H][D], already rotated.
+ *   segs     n_segs (1..3) segments; their total token count must be >= 1.
+ *   scale    softmax scale; <= 0 selects 1/sqrt(D).
+ *   o        bf16 [B][n_q][H][D] output (must not alias q or any k/v).
+ *   lse      optional fp32 [B][H][n_q]: natural-log sum of exp(scale*q.k).
+ * D must be 64 or 128.  bf16 tensor-core products, fp32 accumulation and
+ * softmax; probabilities rounded to bf16 for the PV product.
+ * ------------------------------------------------------------------------ */
+int chunk_attention(const void* q, int B, int64_t n_q, int H, int D, const savgb_kv_segment* segs,
+                    int n_segs, float scale, void* o, float* lse, void* stream);
+
+/* --------------------------------------------------------------------------
+ * out_proj_euler_step - output projection of the attention, taken as the
+ * flow-matching velocity, followed by one explicit Euler step of the flow
+ * ("The underlying model architecture": a DiT trained with flow matching;
+ * "The streaming framework and pipeline loop": a multi-step diffusion pass).
+ *
+ *   v = O W_o^T (+ bias);  x <- x + dt * v
+ *   o      bf16 [M][hid_in] (the attention output, rows = B*n_q tokens).
+ *   w_o    bf16 [hid_out][hid_in] (PyTorch Linear layout).
+ *   bias   optional fp32 [hid_out].
+ *   x      fp32 [M][hid_out], updated in place.
+ *   v_out  optional fp32 [M][hid_out]: receives v (for inspection).
+ * hid_in % 8 == 0, hid_out % 16 == 0.  bf16 tensor-core product, fp32
+ * accumulation; the update is fused into the GEMM epilogue.
+ * ------------------------------------------------------------------------ */
+int out_proj_euler_step(const void* o, const void* w_o, const float* bias, float* x, int64_t M,
+                        int hid_in, int hid_out, float dt, float* v_out, void* stream);
+
+/* --------------------------------------------------------------------------
+ * flow_time_grid - step sizes of the sampling grid (host only).
+ * Reading of "multi-step diffusion pass": noise levels sigma_i = 1 - i/steps,
+ * warped by sigma' = shift*sigma / (1 + (shift-1)*sigma), dt_i = sigma'_i -
+ * sigma'_{i+1} > 0, sum 1.  shift = 1 is the uniform grid.
+ *   dt_out  host array of `steps` doubles.
+ * ------------------------------------------------------------------------ */
+int flow_time_grid(int steps, double shift, double* dt_out);
+
+/* --------------------------------------------------------------------------
+ * Chunk stream: the rolling state of one or more sessions.
+ * ("The underlying model architecture": the first chunk relies on the static
+ * reference alone, later chunks also on boundary data; "The streaming
+ * framework and pipeline loop": the reference is encoded once per request;
+ * "Constant memory over duration": only the reference conditioning and a
+ * minimal carried state survive a chunk, so memory is fixed by the chunk
+ * size, not by the session length.)
+ *
+ * The handle owns one device arena, sized at create and never grown: the
+ * rotated reference K and V, two boundary slots (in use / being captured) and
+ * the per-step scratch for rotated Q, rotated K and the attention output.
+ * Boundary reading: the pre-RoPE K and V of the last `boundary_frames`
+ * frames of a chunk, taken at its last denoising step, with K rotated to
+ * t = -boundary_frames .. -1 of the next chunk's local time.  Chunk-local time
+ * keeps every angle bounded however long the session runs.
+ * A handle is not thread-safe; separate handles are independent.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int B;               /* sessions batched in one launch (independent) */
+  int H, D;            /* heads, head_dim (64 or 128) */
+  int F;               /* latent frames per chunk */
+  int grid_h, grid_w;  /* latent tokens per frame = grid_h * grid_w */
+  int ref_frames;      /* reference frames (>= 1), at t = ref_t-ref_frames+1 .. ref_t */
+  int boundary_frames; /* frames carried to the next chunk, 0 <= boundary_frames <= F */
+  int ref_t;           /* time of the last reference frame, e.g. -1 */
+  double rope_base;    /* rotary base, e.g. 10000 */
+  float softmax_scale; /* <= 0 selects 1/sqrt(D) */
+} chunk_stream_config;
+
+typedef struct chunk_stream chunk_stream_t;
+
+/* Validates the config, allocates the arena on the current device and binds
+ * the handle to `stream` (cudaStream_t).  *out receives the handle. */
+int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stream_t** out);
+
+/* Copies the reference K (rotated once, here) and V, bf16 [B][R][H][D] with
+ * R = ref_frames*grid_h*grid_w, into the arena.  Call once before the first
+ * step; calling again replaces the reference and restarts the stream. */
+int chunk_stream_set_reference(chunk_stream_t* s, const void* k_ref, const void* v_ref);
+
+/* One denoising step of the current chunk:
+ *   rope3d(q), rope3d(k) at chunk-local positions -> chunk_attention over
+ *   [reference | boundary | chunk] -> out_proj_euler_step(x, dt).
+ *   q, k, v  bf16 [B][N][H][D], N = F*grid_h*grid_w (pre-RoPE, caller-owned).
+ *   w_o      bf16 [H*D][H*D]; bias optional fp32 [H*D].
+ *   x        fp32 [B*N][H*D], updated in place.
+ * With is_last_step != 0 the boundary for the next chunk is captured from
+ * this step's k and v. */
+int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const void* v,
+                      const void* w_o, const float* bias, float* x, float dt, int is_last_step);
+
+/* Ends the current chunk: the boundary captured at its last step becomes the
+ * boundary of the next chunk, and the chunk index advances.  Returns
+ * SAVGB_ERR_STATE if no step of the chunk had is_last_step set (with
+ * boundary_frames > 0). */
+int chunk_stream_end_chunk(chunk_stream_t* s);
+
+/* Synchronises the handle's stream and reports device-side errors. */
+int chunk_stream_sync(chunk_stream_t* s);
+
+/* Read-only view of the state: chunk index, boundary tokens in use (0 on
+ * chunk 0), bytes of the device arena, and device pointers to the boundary K
+ * (rotated) and V in use (NULL when there is no boundary). */
+int chunk_stream_info(const chunk_stream_t* s, int64_t* chunk_index, int64_t* boundary_tokens,
+                      int64_t* arena_bytes, const void** boundary_k, const void** boundary_v);
+
+/* Checkpoint of the rolling state (chunk index + boundary K/V in use) into a
+ * host buffer.  With buf == NULL only *size_out is set.  Synchronises the
+ * stream.  The reference is not part of the state (it is set again on
+ * resume). */
+int chunk_stream_export_state(chunk_stream_t* s, void* buf, size_t cap, size_t* size_out);
+/* Restores a state written by chunk_stream_export_state of a handle with the
+ * same config.  SAVGB_ERR_INVALID_ARG on a size or config mismatch. */
+int chunk_stream_import_state(chunk_stream_t* s, const void* buf, size_t size);
+
+/* Frees the arena and the handle (after synchronising its stream). */
+int chunk_stream_destroy(chunk_stream_t* s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAVGB_H */

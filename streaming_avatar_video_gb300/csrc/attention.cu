@@ -1,0 +1,492 @@
+// Chunk attention on the sm_103a tensor cores (tcgen05 + tensor memory + TMA).
+//
+// Queries of the current chunk attend over up to three key/value segments,
+// [static reference | previous chunk's boundary | current chunk] (HeyGen,
+// "Avatar inference at scale", sections "The underlying model architecture"
+// and "The streaming framework and pipeline loop").  O = softmax(s Q K^T) V
+// per (batch, head), no mask.
+//
+// Design (one CTA = two 128-row query tiles of one (batch, head)):
+//   warp 0      TMA producer: Q tiles once, then K and V tiles of the
+//               concatenated segments through a 2-stage ring each.
+//   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma.
+//   warps 2-5   softmax of query tile 0, warps 6-9 of query tile 1; thread =
+//               one query row (TMEM lane), so row max and sum need no shuffle.
+// TMEM columns: S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D,256+2D).
+// P (bf16) overwrites the first 64 columns of its S and feeds the PV product
+// straight from TMEM.  The two query tiles alternate so that the tensor core
+// works on one tile's QK^T / PV while the other tile's softmax runs.
+// The running max is updated lazily (only when it grows by more than 2^8 in
+// probability), and O is rescaled in TMEM by the softmax warps when it is.
+// Every wait is bounded; on a timeout the block records it in the device
+// error word and every role leaves its loop.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace savgb {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kBlockQ = 256;  // two 128-row tiles
+constexpr int kTileKV = 128;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct AttnMaps {
+  CUtensorMap q;
+  CUtensorMap k[3];
+  CUtensorMap v[3];
+};
+
+struct AttnParams {
+  int n_q, H, n_tiles;
+  int seg_tiles[3];
+  int seg_len[3];
+  float scale_log2;
+  __nv_bfloat16* o;
+  float* lse;
+  DeviceErrorWord* err;
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kTileBytes = 128 * D * 2;  // one 128-row tile, D/64 swizzled column blocks
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + 2 * kTileBytes;
+  static constexpr int kV = kK + 2 * kTileBytes;
+  static constexpr int kBar = kV + 2 * kTileBytes;
+  static constexpr int kNumBars = 16;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16;
+  // request at least 120 KiB so two blocks never share an SM (each holds all 512 TMEM columns)
+  static constexpr int kDynSmem = (kBytes + 1024 > 120 * 1024) ? kBytes + 1024 : 120 * 1024;
+};
+
+enum Bar {
+  kQFull = 0,
+  kKFull = 1,   // +stage
+  kKEmpty = 3,  // +stage
+  kVFull = 5,   // +stage
+  kVEmpty = 7,  // +stage
+  kSFull = 9,   // +tile
+  kPFull = 11,  // +tile
+  kODone = 13,  // +tile
+  kDrain = 15,
+};
+
+__device__ __forceinline__ void tile_of(const AttnParams& p, int j, int& seg, int& row0, int& valid) {
+  int jj = j;
+  seg = 0;
+  while (seg < 2 && jj >= p.seg_tiles[seg]) {
+    jj -= p.seg_tiles[seg];
+    ++seg;
+  }
+  row0 = jj * kTileKV;
+  const int rest = p.seg_len[seg] - row0;
+  valid = rest < kTileKV ? rest : kTileKV;
+}
+
+__device__ __forceinline__ void give_up(const AttnParams& p, volatile int* abort, unsigned code) {
+  if (atomicExch(const_cast<int*>(abort), 1) == 0) {
+    atomicOr(&p.err->flags, kErrAttnWait);
+    atomicCAS(&p.err->where, 0u, code);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = dev::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int b = blockIdx.z;
+  const int h = blockIdx.y;
+  const int q0 = blockIdx.x * kBlockQ;
+
+  if (tid == 0) {
+    dev::mbar_init(&bars[kQFull], 1);
+    for (int s = 0; s < 2; ++s) {
+      dev::mbar_init(&bars[kKFull + s], 1);
+      dev::mbar_init(&bars[kKEmpty + s], 1);
+      dev::mbar_init(&bars[kVFull + s], 1);
+      dev::mbar_init(&bars[kVEmpty + s], 1);
+      dev::mbar_init(&bars[kSFull + s], 1);
+      dev::mbar_init(&bars[kPFull + s], 128);
+      dev::mbar_init(&bars[kODone + s], 1);
+    }
+    dev::mbar_init(&bars[kDrain], 1);
+    *abort = 0;
+    dev::fence_barrier_init();
+  }
+  if (warp == 1) {
+    dev::tmem_alloc(tmem_slot, 512);
+    dev::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    dev::tma_prefetch_desc(&maps.q);
+    for (int s = 0; s < 3; ++s) {
+      if (p.seg_tiles[s] > 0) {
+        dev::tma_prefetch_desc(&maps.k[s]);
+        dev::tma_prefetch_desc(&maps.v[s]);
+      }
+    }
+  }
+  dev::tc_fence_before();
+  __syncthreads();
+  dev::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n = p.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint8_t* sQ = smem + L::kQ;
+      uint8_t* sK = smem + L::kK;
+      uint8_t* sV = smem + L::kV;
+      dev::mbar_arrive_expect_tx(&bars[kQFull], 2 * L::kTileBytes);
+      #pragma unroll
+      for (int x = 0; x < 2; ++x)
+        #pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          dev::tma_load_4d(sQ + x * L::kTileBytes + c * 16384, &maps.q, &bars[kQFull], c * 64, h,
+                           q0 + x * 128, b);
+      int issued = 0;
+      for (int j = 0; j < n; ++j) {
+        int seg, row0, valid;
+        tile_of(p, j, seg, row0, valid);
+        const int st = j & 1;
+        const uint32_t use = j >> 1;
+        if (j >= 2 && !dev::mbar_wait(&bars[kKEmpty + st], (use - 1) & 1, abort)) {
+          give_up(p, abort, 1);
+          break;
+        }
+        dev::mbar_arrive_expect_tx(&bars[kKFull + st], L::kTileBytes);
+        #pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          dev::tma_load_4d(sK + st * L::kTileBytes + c * 16384, &maps.k[seg], &bars[kKFull + st],
+                           c * 64, h, row0, b);
+        if (j >= 2 && !dev::mbar_wait(&bars[kVEmpty + st], (use - 1) & 1, abort)) {
+          give_up(p, abort, 2);
+          issued = 2 * j + 1;
+          break;
+        }
+        dev::mbar_arrive_expect_tx(&bars[kVFull + st], L::kTileBytes);
+        #pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          dev::tma_load_4d(sV + st * L::kTileBytes + c * 16384, &maps.v[seg], &bars[kVFull + st],
+                           c * 64, h, row0, b);
+        issued = 2 * (j + 1);
+      }
+      // drain: every issued copy has landed before the block may exit
+      volatile int never = 0;
+      dev::mbar_wait(&bars[kQFull], 0, &never);
+      const int nk = (issued + 1) / 2, nv = issued / 2;  // K tiles and V tiles issued
+      for (int t = (nk > 2 ? nk - 2 : 0); t < nk; ++t)
+        dev::mbar_wait(&bars[kKFull + (t & 1)], (t >> 1) & 1, &never);
+      for (int t = (nv > 2 ? nv - 2 : 0); t < nv; ++t)
+        dev::mbar_wait(&bars[kVFull + (t & 1)], (t >> 1) & 1, &never);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sQ = dev::smem_u32(smem + L::kQ);
+      const uint32_t sK = dev::smem_u32(smem + L::kK);
+      const uint32_t sV = dev::smem_u32(smem + L::kV);
+      constexpr uint32_t idesc_s = dev::idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_o = dev::idesc_bf16_f32(128, D, false, true);
+      auto issue_s = [&](int x, int st) {
+        const uint32_t d = tmem + x * 128;
+        #pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          const uint64_t a = dev::sdesc_sw128(sQ + x * L::kTileBytes + off, 16, 1024);
+          const uint64_t bd = dev::sdesc_sw128(sK + st * L::kTileBytes + off, 16, 1024);
+          dev::mma_ss(d, a, bd, idesc_s, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int x, int st, bool acc) {
+        const uint32_t d = tmem + 256 + x * D;
+        #pragma unroll
+        for (int kk = 0; kk < kTileKV / 16; ++kk) {
+          const uint64_t bd = dev::sdesc_sw128(sV + st * L::kTileBytes + kk * 2048, 16384, 1024);
+          dev::mma_ts(d, tmem + x * 128 + kk * 8, bd, idesc_o, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = dev::mbar_wait(&bars[kQFull], 0, abort) && dev::mbar_wait(&bars[kKFull], 0, abort);
+      if (!ok) give_up(p, abort, 3);
+      if (ok) {
+        dev::tc_fence_after();
+        issue_s(0, 0);
+        dev::mma_commit(&bars[kSFull + 0]);
+        issue_s(1, 0);
+        dev::mma_commit(&bars[kSFull + 1]);
+        dev::mma_commit(&bars[kKEmpty + 0]);
+        for (int j = 0; j < n; ++j) {
+          const int st = j & 1;
+          const uint32_t use = j >> 1;
+          const bool more = j + 1 < n;
+          const int st1 = (j + 1) & 1;
+          const uint32_t use1 = (j + 1) >> 1;
+          if (!dev::mbar_wait(&bars[kVFull + st], use & 1, abort) ||
+              !dev::mbar_wait(&bars[kPFull + 0], j & 1, abort)) {
+            give_up(p, abort, 4);
+            break;
+          }
+          dev::tc_fence_after();
+          issue_pv(0, st, j > 0);
+          if (more) {
+            if (!dev::mbar_wait(&bars[kKFull + st1], use1 & 1, abort)) {
+              give_up(p, abort, 5);
+              break;
+            }
+            dev::tc_fence_after();
+            issue_s(0, st1);
+            dev::mma_commit(&bars[kSFull + 0]);
+          }
+          if (!dev::mbar_wait(&bars[kPFull + 1], j & 1, abort)) {
+            give_up(p, abort, 6);
+            break;
+          }
+          dev::tc_fence_after();
+          issue_pv(1, st, j > 0);
+          dev::mma_commit(&bars[kVEmpty + st]);
+          if (more) {
+            issue_s(1, st1);
+            dev::mma_commit(&bars[kSFull + 1]);
+            dev::mma_commit(&bars[kKEmpty + st1]);
+          }
+        }
+        dev::mma_commit(&bars[kODone + 0]);
+        dev::mma_commit(&bars[kODone + 1]);
+      }
+      // drain: all issued MMAs complete before TMEM is released
+      dev::mma_commit(&bars[kDrain]);
+      volatile int never = 0;
+      dev::mbar_wait(&bars[kDrain], 0, &never);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int x = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + x * 128;
+    const uint32_t tO = tmem + lane_off + 256 + x * D;
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      int seg, row0, valid;
+      tile_of(p, j, seg, row0, valid);
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[kSFull + x], j & 1, abort));
+      if (!ok) {
+        give_up(p, abort, 7);
+        break;
+      }
+      dev::tc_fence_after();
+      uint32_t sr[128];
+      {
+        uint32_t (&lo)[64] = *reinterpret_cast<uint32_t(*)[64]>(&sr[0]);
+        uint32_t (&hi)[64] = *reinterpret_cast<uint32_t(*)[64]>(&sr[64]);
+        dev::tmem_ld64(tS, lo);
+        dev::tmem_ld64(tS + 64, hi);
+      }
+      float* s = reinterpret_cast<float*>(sr);
+      if (valid < kTileKV) {
+        #pragma unroll
+        for (int c = 0; c < kTileKV; ++c)
+          if (c >= valid) s[c] = -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      #pragma unroll
+      for (int c = 4; c < kTileKV; c += 4) {
+        mx0 = fmaxf(mx0, s[c]);
+        mx1 = fmaxf(mx1, s[c + 1]);
+        mx2 = fmaxf(mx2, s[c + 2]);
+        mx3 = fmaxf(mx3, s[c + 3]);
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float m_new = fmaxf(m, mx);
+      const bool need = m_new > m + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? dev::ex2_approx(m - m_new) : 1.f;
+        if (need) {
+          m = m_new;
+          l *= alpha;
+        }
+        if (j > 0) {
+          #pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            dev::tmem_ld32(tO + c, o);
+            #pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            dev::tmem_st32(tO + c, o);
+          }
+        }
+      }
+      const float nm = -m;
+      float l0 = 0.f, l1 = 0.f;
+      #pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+        #pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = dev::ex2_approx(fmaf(s[half * 64 + 2 * i], sl2, nm));
+          const float p1 = dev::ex2_approx(fmaf(s[half * 64 + 2 * i + 1], sl2, nm));
+          l0 += p0;
+          l1 += p1;
+          pk[i] = dev::pack_bf16x2(p0, p1);
+        }
+        dev::tmem_st32(tS + half * 32, pk);
+      }
+      l += l0 + l1;
+      dev::tc_fence_before();
+      dev::mbar_arrive(&bars[kPFull + x]);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[kODone + x], 0, abort));
+    if (ok) {
+      dev::tc_fence_after();
+      const int q = q0 + x * 128 + row;
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* dst = p.o + ((static_cast<int64_t>(b) * p.n_q + q) * p.H + h) * D;
+      #pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        dev::tmem_ld32(tO + c, o);
+        uint32_t pk[16];
+        #pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = dev::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                   __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (q < p.n_q) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+          #pragma unroll
+          for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (p.lse != nullptr && q < p.n_q)
+        p.lse[(static_cast<int64_t>(b) * p.H + h) * p.n_q + q] =
+            (m + log2f(l)) * 0.69314718055994530942f;
+    } else {
+      give_up(p, abort, 8);
+    }
+  }
+
+  dev::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    dev::tc_fence_after();
+    dev::tmem_dealloc(tmem, 512);
+  }
+}
+
+int make_token_map(CUtensorMap* m, const void* ptr, int B, int64_t N, int H, int D) {
+  const uint64_t dims[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)N, (uint64_t)B};
+  const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)N * H * D * 2};
+  const uint32_t box[4] = {64, 1, 128, 1};
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int D>
+int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, int n_segs,
+                float scale, void* o, float* lse, cudaStream_t stream) {
+  using L = Layout<D>;
+  static bool attr_done[64] = {false};
+  int dev_id = 0;
+  SAVGB_CUDA(cudaGetDevice(&dev_id));
+  if (!attr_done[dev_id & 63]) {
+    SAVGB_CUDA(cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    L::kDynSmem));
+    attr_done[dev_id & 63] = true;
+  }
+  AttnMaps maps;
+  int rc = make_token_map(&maps.q, q, B, n_q, H, D);
+  if (rc) return rc;
+  AttnParams p{};
+  p.n_q = (int)n_q;
+  p.H = H;
+  p.n_tiles = 0;
+  for (int s = 0; s < 3; ++s) {
+    const bool used = s < n_segs && segs[s].n > 0;
+    p.seg_len[s] = used ? (int)segs[s].n : 0;
+    p.seg_tiles[s] = used ? (int)((segs[s].n + kTileKV - 1) / kTileKV) : 0;
+    p.n_tiles += p.seg_tiles[s];
+    if (used) {
+      if ((rc = make_token_map(&maps.k[s], segs[s].k, B, segs[s].n, H, D))) return rc;
+      if ((rc = make_token_map(&maps.v[s], segs[s].v, B, segs[s].n, H, D))) return rc;
+    } else {
+      maps.k[s] = maps.q;
+      maps.v[s] = maps.q;
+    }
+  }
+  if (!(scale > 0.f)) scale = 1.0f / std::sqrt((float)D);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  if ((rc = error_word(&p.err))) return rc;
+  dim3 grid((unsigned)((n_q + kBlockQ - 1) / kBlockQ), (unsigned)H, (unsigned)B);
+  attn_fwd_kernel<D><<<grid, kThreads, L::kDynSmem, stream>>>(maps, p);
+  SAVGB_CUDA(cudaGetLastError());
+  return SAVGB_OK;
+}
+
+}  // namespace
+
+int validate_attention(const void* q, int B, int64_t n_q, int H, int D, const AttnSeg* segs,
+                       int n_segs, const void* o) {
+  if (!q || !o) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention: null q or o");
+  if (!aligned16(q) || !aligned16(o)) return fail(SAVGB_ERR_ALIGNMENT, "chunk_attention: q and o must be 16-byte aligned");
+  if (D != 64 && D != 128) return fail(SAVGB_ERR_UNSUPPORTED, "chunk_attention: head_dim %d (64 or 128 supported)", D);
+  if (B < 1 || B > 65535 || H < 1 || H > 65535) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention: B and H must be in [1, 65535]");
+  if (n_q < 1 || n_q > (int64_t)1 << 30) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention: n_q must be in [1, 2^30]");
+  if (n_segs < 1 || n_segs > 3 || !segs) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention: 1 to 3 segments");
+  int64_t total = 0;
+  for (int s = 0; s < n_segs; ++s) {
+    if (segs[s].n < 0 || segs[s].n > (int64_t)1 << 30) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention: segment %d size", s);
+    if (segs[s].n == 0) continue;
+    if (!segs[s].k || !segs[s].v) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention: segment %d has null k or v", s);
+    if (!aligned16(segs[s].k) || !aligned16(segs[s].v)) return fail(SAVGB_ERR_ALIGNMENT, "chunk_attention: segment %d not 16-byte aligned", s);
+    total += segs[s].n;
+  }
+  if (total < 1) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention: no key/value tokens");
+  return SAVGB_OK;
+}
+
+int launch_attention(const void* q, int B, int64_t n_q, int H, int D, const AttnSeg* segs,
+                     int n_segs, float scale, void* o, float* lse, cudaStream_t stream) {
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  if (D == 64) return launch_impl<64>(q, B, n_q, H, segs, n_segs, scale, o, lse, stream);
+  return launch_impl<128>(q, B, n_q, H, segs, n_segs, scale, o, lse, stream);
+}
+
+}  // namespace savgb
+
+extern "C" int chunk_attention(const void* q, int B, int64_t n_q, int H, int D,
+                               const savgb_kv_segment* segs, int n_segs, float scale, void* o,
+                               float* lse, void* stream) {
+  using namespace savgb;
+  clear_error();
+  AttnSeg s[3] = {};
+  if (segs && n_segs >= 1 && n_segs <= 3)
+    for (int i = 0; i < n_segs; ++i) s[i] = AttnSeg{segs[i].k, segs[i].v, segs[i].n_tokens};
+  int rc = validate_attention(q, B, n_q, H, D, segs ? s : nullptr, n_segs, o);
+  if (rc) return rc;
+  return launch_attention(q, B, n_q, H, D, s, n_segs, scale, o, lse,
+                          static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,316 @@
+// Chunk stream: the rolling state of B independent sessions.
+//
+// HeyGen, "Avatar inference at scale":
+//   - "The underlying model architecture": the first chunk relies on the
+//     static reference only; later chunks also use boundary data from the
+//     previous chunk.
+//   - "The streaming framework and pipeline loop": the reference identity is
+//     encoded once per request; each chunk runs a multi-step diffusion pass
+//     conditioned on the previous chunk's boundary frames.
+//   - "Constant memory over duration": only the reference conditioning and a
+//     minimal carried state survive a chunk; peak memory is set by the chunk
+//     size, not by the session length.
+//
+// The handle owns one device arena allocated at create and never grown:
+//   ref_k (rotated once) | ref_v | boundary k/v x 2 slots | q_rot | k_rot | o
+// A step enqueues, on the handle's stream: RoPE of q and k (one launch),
+// attention over [reference | boundary | chunk], then the W_o GEMM with the
+// Euler update fused into its epilogue.  The last step of a chunk also rotates
+// the tail frames of its k into the spare boundary slot (t = -T_b .. -1) and
+// copies the tail of v; end_chunk swaps the slots.
+#include <cuda_bf16.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <cmath>
+#include <new>
+
+#include "common.h"
+
+using namespace savgb;
+
+struct chunk_stream {
+  chunk_stream_config cfg;
+  cudaStream_t stream;
+  int device;
+  int64_t n_tok;     // tokens per chunk
+  int64_t n_ref;     // reference tokens
+  int64_t n_bnd;     // boundary tokens once a boundary exists
+  int64_t hid;
+  void* arena;
+  int64_t arena_bytes;
+  __nv_bfloat16_raw* ref_k;
+  __nv_bfloat16_raw* ref_v;
+  __nv_bfloat16_raw* bnd_k[2];
+  __nv_bfloat16_raw* bnd_v[2];
+  __nv_bfloat16_raw* q_rot;
+  __nv_bfloat16_raw* k_rot;
+  __nv_bfloat16_raw* o;
+  int cur;             // boundary slot in use
+  int64_t bnd_in_use;  // 0 on chunk 0
+  bool captured;
+  bool ref_set;
+  int64_t chunk_index;
+};
+
+namespace {
+
+constexpr uint64_t kStateMagic = 0x5341564742535431ull;  // "SAVGBST1"
+
+struct StateHeader {
+  uint64_t magic;
+  int32_t B, H, D, F, grid_h, grid_w, boundary_frames, pad;
+  int64_t chunk_index;
+  int64_t bnd_in_use;
+  int64_t payload_bytes;
+};
+
+int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+int validate_config(const chunk_stream_config* c) {
+  if (!c) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: null config");
+  if (c->B < 1 || c->H < 1 || c->F < 1 || c->grid_h < 1 || c->grid_w < 1)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: B, H, F, grid_h, grid_w must be >= 1");
+  if (c->D != 64 && c->D != 128) return fail(SAVGB_ERR_UNSUPPORTED, "chunk_stream: head_dim %d (64 or 128 supported)", c->D);
+  if (c->ref_frames < 1) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: ref_frames must be >= 1");
+  if (c->boundary_frames < 0 || c->boundary_frames > c->F)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: boundary_frames must be in [0, F]");
+  if (!(c->rope_base > 0.0) || !std::isfinite(c->rope_base))
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: rope_base must be finite and > 0");
+  const int64_t hid = (int64_t)c->H * c->D;
+  if (hid % 16) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: H*D must be a multiple of 16");
+  return SAVGB_OK;
+}
+
+RopeArgs rope_args(const chunk_stream* s, const void* in, void* out, int64_t in_bs, int64_t out_bs,
+                   int grid_t, int t0) {
+  const chunk_stream_config& c = s->cfg;
+  return RopeArgs{in, out, c.B, (int64_t)grid_t * c.grid_h * c.grid_w, c.H, c.D, grid_t,
+                  c.grid_h, c.grid_w, t0, c.rope_base, in_bs, out_bs};
+}
+
+}  // namespace
+
+extern "C" {
+
+int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stream_t** out) {
+  clear_error();
+  if (!out) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_create: null out");
+  *out = nullptr;
+  int rc = validate_config(cfg);
+  if (rc) return rc;
+  if ((rc = check_device(nullptr))) return rc;
+  chunk_stream* s = new (std::nothrow) chunk_stream();
+  if (!s) return fail(SAVGB_ERR_OOM, "chunk_stream_create: host allocation");
+  s->cfg = *cfg;
+  s->stream = static_cast<cudaStream_t>(stream);
+  cudaGetDevice(&s->device);
+  const chunk_stream_config& c = *cfg;
+  s->hid = (int64_t)c.H * c.D;
+  const int64_t fr = (int64_t)c.grid_h * c.grid_w;
+  s->n_tok = c.F * fr;
+  s->n_ref = c.ref_frames * fr;
+  s->n_bnd = c.boundary_frames * fr;
+  // validate every launch shape once, up front
+  RopeArgs probe = rope_args(s, (void*)16, (void*)16, 0, 0, c.F, 0);
+  if ((rc = validate_rope(probe))) { delete s; return rc; }
+  probe = rope_args(s, (void*)16, (void*)16, 0, 0, c.ref_frames, c.ref_t - c.ref_frames + 1);
+  if ((rc = validate_rope(probe))) { delete s; return rc; }
+  const int64_t tok_bytes = s->hid * 2 * c.B;  // one token of all sessions
+  const int64_t ref_b = round_up(s->n_ref * tok_bytes, 256);
+  const int64_t bnd_b = round_up((s->n_bnd > 0 ? s->n_bnd : 1) * tok_bytes, 256);
+  const int64_t tok_b = round_up(s->n_tok * tok_bytes, 256);
+  s->arena_bytes = 2 * ref_b + 4 * bnd_b + 3 * tok_b;
+  const char* cap = getenv("SAVGB_ARENA_LIMIT_BYTES");
+  if (cap && *cap) {
+    const long long lim = atoll(cap);
+    if (lim >= 0 && s->arena_bytes > lim) {
+      const long long need = (long long)s->arena_bytes;
+      delete s;
+      return fail(SAVGB_ERR_OOM, "chunk_stream_create: arena of %lld bytes exceeds SAVGB_ARENA_LIMIT_BYTES=%lld", need, lim);
+    }
+  }
+  cudaError_t e = cudaMalloc(&s->arena, (size_t)s->arena_bytes);
+  if (e != cudaSuccess) {
+    delete s;
+    return cuda_fail(e, "chunk_stream_create: cudaMalloc(arena)");
+  }
+  uint8_t* p = static_cast<uint8_t*>(s->arena);
+  auto take = [&](int64_t bytes) { auto* r = reinterpret_cast<__nv_bfloat16_raw*>(p); p += bytes; return r; };
+  s->ref_k = take(ref_b);
+  s->ref_v = take(ref_b);
+  for (int i = 0; i < 2; ++i) { s->bnd_k[i] = take(bnd_b); s->bnd_v[i] = take(bnd_b); }
+  s->q_rot = take(tok_b);
+  s->k_rot = take(tok_b);
+  s->o = take(tok_b);
+  s->cur = 0;
+  s->bnd_in_use = 0;
+  s->captured = false;
+  s->ref_set = false;
+  s->chunk_index = 0;
+  *out = s;
+  return SAVGB_OK;
+}
+
+int chunk_stream_set_reference(chunk_stream_t* s, const void* k_ref, const void* v_ref) {
+  clear_error();
+  if (!s || !k_ref || !v_ref) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_set_reference: null argument");
+  if (!aligned16(k_ref) || !aligned16(v_ref)) return fail(SAVGB_ERR_ALIGNMENT, "chunk_stream_set_reference: pointers must be 16-byte aligned");
+  const chunk_stream_config& c = s->cfg;
+  const int64_t per_b = s->n_ref * s->hid;
+  RopeArgs a = rope_args(s, k_ref, s->ref_k, per_b, per_b, c.ref_frames, c.ref_t - c.ref_frames + 1);
+  int rc = launch_rope(a, s->stream);
+  if (rc) return rc;
+  SAVGB_CUDA(cudaMemcpyAsync(s->ref_v, v_ref, (size_t)(per_b * c.B * 2), cudaMemcpyDeviceToDevice, s->stream));
+  s->ref_set = true;
+  s->cur = 0;
+  s->bnd_in_use = 0;
+  s->captured = false;
+  s->chunk_index = 0;
+  return SAVGB_OK;
+}
+
+int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const void* v,
+                      const void* w_o, const float* bias, float* x, float dt, int is_last_step) {
+  clear_error();
+  if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_step: null handle");
+  if (!s->ref_set) return fail(SAVGB_ERR_STATE, "chunk_stream_step: set_reference has not been called");
+  if (!q || !k || !v || !w_o || !x) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_step: null argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(w_o) || !aligned16(x) ||
+      (bias && !aligned16(bias)))
+    return fail(SAVGB_ERR_ALIGNMENT, "chunk_stream_step: pointers must be 16-byte aligned");
+  if (!std::isfinite(dt)) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_step: dt must be finite");
+  const chunk_stream_config& c = s->cfg;
+  const int64_t per_b = s->n_tok * s->hid;
+  RopeArgs aq = rope_args(s, q, s->q_rot, per_b, per_b, c.F, 0);
+  RopeArgs ak = rope_args(s, k, s->k_rot, per_b, per_b, c.F, 0);
+  int rc = launch_rope_pair(aq, ak, s->stream);
+  if (rc) return rc;
+  AttnSeg segs[3] = {
+      {s->ref_k, s->ref_v, s->n_ref},
+      {s->bnd_k[s->cur], s->bnd_v[s->cur], s->bnd_in_use},
+      {s->k_rot, v, s->n_tok},
+  };
+  rc = launch_attention(s->q_rot, c.B, s->n_tok, c.H, c.D, segs, 3, c.softmax_scale, s->o, nullptr,
+                        s->stream);
+  if (rc) return rc;
+  rc = launch_out_proj_euler(s->o, w_o, bias, x, c.B * s->n_tok, (int)s->hid, (int)s->hid, dt,
+                             nullptr, s->stream);
+  if (rc) return rc;
+  if (is_last_step && s->n_bnd > 0) {
+    const int nxt = s->cur ^ 1;
+    const int64_t tail = (s->n_tok - s->n_bnd) * s->hid;
+    const int64_t bnd_per_b = s->n_bnd * s->hid;
+    RopeArgs ab = rope_args(s, static_cast<const __nv_bfloat16_raw*>(k) + tail, s->bnd_k[nxt],
+                            per_b, bnd_per_b, c.boundary_frames, -c.boundary_frames);
+    if ((rc = launch_rope(ab, s->stream))) return rc;
+    SAVGB_CUDA(cudaMemcpy2DAsync(s->bnd_v[nxt], (size_t)bnd_per_b * 2,
+                                 static_cast<const __nv_bfloat16_raw*>(v) + tail, (size_t)per_b * 2,
+                                 (size_t)bnd_per_b * 2, (size_t)c.B, cudaMemcpyDeviceToDevice,
+                                 s->stream));
+    s->captured = true;
+  } else if (is_last_step) {
+    s->captured = true;
+  }
+  return SAVGB_OK;
+}
+
+int chunk_stream_end_chunk(chunk_stream_t* s) {
+  clear_error();
+  if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_end_chunk: null handle");
+  if (!s->captured)
+    return fail(SAVGB_ERR_STATE, "chunk_stream_end_chunk: no step of this chunk had is_last_step set");
+  if (s->n_bnd > 0) {
+    s->cur ^= 1;
+    s->bnd_in_use = s->n_bnd;
+  }
+  s->captured = false;
+  s->chunk_index += 1;
+  return SAVGB_OK;
+}
+
+int chunk_stream_sync(chunk_stream_t* s) {
+  clear_error();
+  if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_sync: null handle");
+  return savgb_device_check(s->stream);
+}
+
+int chunk_stream_info(const chunk_stream_t* s, int64_t* chunk_index, int64_t* boundary_tokens,
+                      int64_t* arena_bytes, const void** boundary_k, const void** boundary_v) {
+  clear_error();
+  if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_info: null handle");
+  if (chunk_index) *chunk_index = s->chunk_index;
+  if (boundary_tokens) *boundary_tokens = s->bnd_in_use;
+  if (arena_bytes) *arena_bytes = s->arena_bytes;
+  if (boundary_k) *boundary_k = s->bnd_in_use ? s->bnd_k[s->cur] : nullptr;
+  if (boundary_v) *boundary_v = s->bnd_in_use ? s->bnd_v[s->cur] : nullptr;
+  return SAVGB_OK;
+}
+
+int chunk_stream_export_state(chunk_stream_t* s, void* buf, size_t cap, size_t* size_out) {
+  clear_error();
+  if (!s || !size_out) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_export_state: null argument");
+  const int64_t payload = 2 * s->bnd_in_use * s->hid * 2 * s->cfg.B;
+  const size_t total = sizeof(StateHeader) + (size_t)payload;
+  *size_out = total;
+  if (!buf) return SAVGB_OK;
+  if (cap < total) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_export_state: buffer of %zu bytes < %zu", cap, total);
+  StateHeader h{};
+  h.magic = kStateMagic;
+  const chunk_stream_config& c = s->cfg;
+  h.B = c.B; h.H = c.H; h.D = c.D; h.F = c.F; h.grid_h = c.grid_h; h.grid_w = c.grid_w;
+  h.boundary_frames = c.boundary_frames;
+  h.chunk_index = s->chunk_index;
+  h.bnd_in_use = s->bnd_in_use;
+  h.payload_bytes = payload;
+  memcpy(buf, &h, sizeof(h));
+  if (payload > 0) {
+    uint8_t* dst = static_cast<uint8_t*>(buf) + sizeof(h);
+    const size_t half = (size_t)payload / 2;
+    SAVGB_CUDA(cudaMemcpyAsync(dst, s->bnd_k[s->cur], half, cudaMemcpyDeviceToHost, s->stream));
+    SAVGB_CUDA(cudaMemcpyAsync(dst + half, s->bnd_v[s->cur], half, cudaMemcpyDeviceToHost, s->stream));
+  }
+  SAVGB_CUDA(cudaStreamSynchronize(s->stream));
+  return SAVGB_OK;
+}
+
+int chunk_stream_import_state(chunk_stream_t* s, const void* buf, size_t size) {
+  clear_error();
+  if (!s || !buf) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_import_state: null argument");
+  if (size < sizeof(StateHeader)) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_import_state: truncated state");
+  StateHeader h;
+  memcpy(&h, buf, sizeof(h));
+  const chunk_stream_config& c = s->cfg;
+  if (h.magic != kStateMagic || h.B != c.B || h.H != c.H || h.D != c.D || h.F != c.F ||
+      h.grid_h != c.grid_h || h.grid_w != c.grid_w || h.boundary_frames != c.boundary_frames)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_import_state: state of another configuration");
+  if ((h.bnd_in_use != 0 && h.bnd_in_use != s->n_bnd) ||
+      h.payload_bytes != 2 * h.bnd_in_use * s->hid * 2 * c.B ||
+      size != sizeof(StateHeader) + (size_t)h.payload_bytes || h.chunk_index < 0)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_import_state: inconsistent sizes");
+  if (!s->ref_set) return fail(SAVGB_ERR_STATE, "chunk_stream_import_state: set_reference first");
+  if (h.payload_bytes > 0) {
+    const uint8_t* src = static_cast<const uint8_t*>(buf) + sizeof(h);
+    const size_t half = (size_t)h.payload_bytes / 2;
+    SAVGB_CUDA(cudaMemcpyAsync(s->bnd_k[s->cur], src, half, cudaMemcpyHostToDevice, s->stream));
+    SAVGB_CUDA(cudaMemcpyAsync(s->bnd_v[s->cur], src + half, half, cudaMemcpyHostToDevice, s->stream));
+    SAVGB_CUDA(cudaStreamSynchronize(s->stream));
+  }
+  s->bnd_in_use = h.bnd_in_use;
+  s->chunk_index = h.chunk_index;
+  s->captured = false;
+  return SAVGB_OK;
+}
+
+int chunk_stream_destroy(chunk_stream_t* s) {
+  clear_error();
+  if (!s) return SAVGB_OK;
+  cudaError_t e1 = cudaStreamSynchronize(s->stream);
+  cudaError_t e2 = cudaFree(s->arena);
+  delete s;
+  if (e1 != cudaSuccess) return cuda_fail(e1, "chunk_stream_destroy: cudaStreamSynchronize");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "chunk_stream_destroy: cudaFree");
+  return SAVGB_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// Host-side helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "savgb.h"
+
+namespace savgb {
+
+// Records a thread-local message for savgb_last_error() and returns `code`.
+int fail(int code, const char* fmt, ...);
+// Clears the thread-local message (called at the start of every entry point).
+void clear_error();
+// Maps a CUDA runtime error to SAVGB_ERR_CUDA / SAVGB_ERR_OOM with a message.
+int cuda_fail(cudaError_t e, const char* what);
+
+#define SAVGB_CUDA(call)                                   \
+  do {                                                     \
+    cudaError_t e_ = (call);                               \
+    if (e_ != cudaSuccess) return ::savgb::cuda_fail(e_, #call); \
+  } while (0)
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device error word: bit flags set by kernels whose bounded waits ran out,
+// plus the code of the wait that gave up first.  Lives in a file-scope
+// __device__ variable (no allocation); this returns its device address on the
+// current device.
+struct DeviceErrorWord {
+  unsigned int flags;
+  unsigned int where;
+};
+enum : unsigned int {
+  kErrAttnWait = 1u << 0,
+  kErrGemmWait = 1u << 1,
+  kErrSelfTestWait = 1u << 2,
+};
+int error_word(DeviceErrorWord** out);
+
+// Current device must be an sm_103 part (GB300); returns SAVGB_ERR_UNSUPPORTED
+// otherwise.  Caches the SM count.
+int check_device(int* sm_count);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle);
+
+// Internal launchers (all validate nothing: the entry points do that).
+struct RopeArgs {
+  const void* in;
+  void* out;
+  int B;
+  int64_t n_tokens;
+  int H, D;
+  int grid_t, grid_h, grid_w, t0;
+  double base;
+  int64_t in_batch_stride;   // elements between batches of `in`
+  int64_t out_batch_stride;  // elements between batches of `out`
+};
+int validate_rope(const RopeArgs& a);
+int launch_rope(const RopeArgs& a, cudaStream_t stream);
+// Rotates two tensors of one shape and grid (a chunk's q and k) in one launch.
+int launch_rope_pair(const RopeArgs& a, const RopeArgs& b, cudaStream_t stream);
+
+struct AttnSeg {
+  const void* k;
+  const void* v;
+  int64_t n;
+};
+int validate_attention(const void* q, int B, int64_t n_q, int H, int D, const AttnSeg* segs,
+                       int n_segs, const void* o);
+int launch_attention(const void* q, int B, int64_t n_q, int H, int D, const AttnSeg* segs,
+                     int n_segs, float scale, void* o, float* lse, cudaStream_t stream);
+
+int validate_out_proj(const void* o, const void* w, const float* bias, const float* x, int64_t M,
+                      int hid_in, int hid_out, const float* v_out);
+int launch_out_proj_euler(const void* o, const void* w, const float* bias, float* x, int64_t M,
+                          int hid_in, int hid_out, float dt, float* v_out, cudaStream_t stream);
+
+}  // namespace savgb

@@ -1,0 +1,218 @@
+// 3D (t, h, w) rotary position embedding of bf16 token tensors.
+//
+// Positions of the chunked latent video (HeyGen, "Avatar inference at scale",
+// section "The underlying model architecture").  The D/2 channel pairs are
+// split [t | h | w] (spatial axes floor(D/6) pairs each, time the rest); pair
+// j of an axis with P pairs turns at base^(-j/P) radians per position.
+//
+// HBM-bound: each element is read once and written once.  Each block first
+// builds the cos/sin tables of the three axes in shared memory (fp32, from
+// sincosf), then streams 16-byte vectors (8 channels = 4 pairs of one token
+// and head) with four independent vectors in flight per thread.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "common.h"
+
+namespace savgb {
+namespace {
+
+constexpr int kRopeThreads = 512;
+constexpr int kRopeUnroll = 4;
+constexpr int kRopeMaxTableBytes = 96 * 1024;
+
+struct RopeTensor {
+  const uint4* in;
+  uint4* out;
+  int64_t in_bs;   // 16-byte vectors between batches
+  int64_t out_bs;
+};
+
+struct RopeKernelArgs {
+  RopeTensor t[2];
+  int n_tensors;
+  int B, n_tokens, vec_per_tok, vec_per_head;  // vec_per_head = D/8
+  int gh, gw, gt, t0;
+  int p_t, p_h, p_w;
+  float log2_base;
+  int total;  // B * n_tokens * vec_per_tok
+};
+
+__device__ __forceinline__ void rotate_pair(uint32_t& packed, float2 cs) {
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&packed);
+  const float a = __low2float(v);
+  const float b = __high2float(v);
+  const float ra = a * cs.x - b * cs.y;
+  const float rb = a * cs.y + b * cs.x;
+  __nv_bfloat162 r = __floats2bfloat162_rn(ra, rb);
+  packed = *reinterpret_cast<uint32_t*>(&r);
+}
+
+__global__ void __launch_bounds__(kRopeThreads) rope3d_kernel(const RopeKernelArgs a) {
+  extern __shared__ float2 tab[];
+  float2* tab_t = tab;
+  float2* tab_h = tab_t + a.gt * a.p_t;
+  float2* tab_w = tab_h + a.gh * a.p_h;
+  const int n_t = a.gt * a.p_t, n_h = a.gh * a.p_h, n_w = a.gw * a.p_w;
+  for (int i = threadIdx.x; i < n_t + n_h + n_w; i += blockDim.x) {
+    int pos, j, P;
+    if (i < n_t) {
+      pos = a.t0 + i / a.p_t; j = i % a.p_t; P = a.p_t;
+    } else if (i < n_t + n_h) {
+      const int k = i - n_t; pos = k / a.p_h; j = k % a.p_h; P = a.p_h;
+    } else {
+      const int k = i - n_t - n_h; pos = k / a.p_w; j = k % a.p_w; P = a.p_w;
+    }
+    const float omega = exp2f(-static_cast<float>(j) / static_cast<float>(P) * a.log2_base);
+    float s, c;
+    sincosf(static_cast<float>(pos) * omega, &s, &c);
+    tab[i] = make_float2(c, s);
+  }
+  __syncthreads();
+
+  const int hw = a.gh * a.gw;
+  const int stride = gridDim.x * blockDim.x;
+  for (int ti = 0; ti < a.n_tensors; ++ti) {
+    const uint4* __restrict__ in = ti == 0 ? a.t[0].in : a.t[1].in;
+    uint4* __restrict__ out = ti == 0 ? a.t[0].out : a.t[1].out;
+    const int64_t in_bs = ti == 0 ? a.t[0].in_bs : a.t[1].in_bs;
+    const int64_t out_bs = ti == 0 ? a.t[0].out_bs : a.t[1].out_bs;
+    for (int base = blockIdx.x * blockDim.x + threadIdx.x; base < a.total;
+         base += stride * kRopeUnroll) {
+      uint4 v[kRopeUnroll];
+      #pragma unroll
+      for (int u = 0; u < kRopeUnroll; ++u) {
+        const int idx = base + u * stride;
+        if (idx < a.total) {
+          const int tok = idx / a.vec_per_tok;
+          const int rem = idx - tok * a.vec_per_tok;
+          const int b = tok / a.n_tokens;
+          const int n = tok - b * a.n_tokens;
+          v[u] = __ldcs(in + (int64_t)b * in_bs + (int64_t)n * a.vec_per_tok + rem);
+        }
+      }
+      #pragma unroll
+      for (int u = 0; u < kRopeUnroll; ++u) {
+        const int idx = base + u * stride;
+        if (idx < a.total) {
+          const int tok = idx / a.vec_per_tok;
+          const int rem = idx - tok * a.vec_per_tok;
+          const int b = tok / a.n_tokens;
+          const int n = tok - b * a.n_tokens;
+          const int tt = n / hw;
+          const int r2 = n - tt * hw;
+          const int hh = r2 / a.gw;
+          const int ww = r2 - hh * a.gw;
+          const int p0 = (rem % a.vec_per_head) * 4;
+          uint32_t w0 = v[u].x, w1 = v[u].y, w2 = v[u].z, w3 = v[u].w;
+          const float2* tr = tab_t + tt * a.p_t;
+          const float2* hr = tab_h + hh * a.p_h - a.p_t;
+          const float2* wr = tab_w + ww * a.p_w - a.p_t - a.p_h;
+          const int ph_end = a.p_t + a.p_h;
+          #define SAVGB_ROT(W, Q) { const int p_ = p0 + (Q); \
+            const float2 cs_ = p_ < a.p_t ? tr[p_] : (p_ < ph_end ? hr[p_] : wr[p_]); \
+            rotate_pair(W, cs_); }
+          SAVGB_ROT(w0, 0) SAVGB_ROT(w1, 1) SAVGB_ROT(w2, 2) SAVGB_ROT(w3, 3)
+          #undef SAVGB_ROT
+          __stcs(out + (int64_t)b * out_bs + (int64_t)n * a.vec_per_tok + rem,
+                 make_uint4(w0, w1, w2, w3));
+        }
+      }
+    }
+  }
+}
+
+void axis_split(int D, int* pt, int* ph, int* pw) {
+  const int P = D / 2;
+  *ph = P / 3;
+  *pw = P / 3;
+  *pt = P - 2 * (P / 3);
+}
+
+size_t table_bytes(const RopeArgs& a) {
+  int pt, ph, pw;
+  axis_split(a.D, &pt, &ph, &pw);
+  return sizeof(float2) * ((size_t)a.grid_t * pt + (size_t)a.grid_h * ph + (size_t)a.grid_w * pw);
+}
+
+}  // namespace
+
+int validate_rope(const RopeArgs& a) {
+  if (!a.in || !a.out) return fail(SAVGB_ERR_INVALID_ARG, "rope3d: null pointer");
+  if (!aligned16(a.in) || !aligned16(a.out)) return fail(SAVGB_ERR_ALIGNMENT, "rope3d: pointers must be 16-byte aligned");
+  if (a.B < 1 || a.H < 1 || a.n_tokens < 1) return fail(SAVGB_ERR_INVALID_ARG, "rope3d: B, H, n_tokens must be >= 1");
+  if (a.D < 8 || a.D > 256 || a.D % 8) return fail(SAVGB_ERR_INVALID_ARG, "rope3d: D must be a multiple of 8 in [8, 256]");
+  if (a.grid_t < 1 || a.grid_h < 1 || a.grid_w < 1 || a.grid_t > 4096 || a.grid_h > 4096 ||
+      a.grid_w > 4096)
+    return fail(SAVGB_ERR_INVALID_ARG, "rope3d: grid sizes must be in [1, 4096]");
+  if ((int64_t)a.grid_t * a.grid_h * a.grid_w != a.n_tokens)
+    return fail(SAVGB_ERR_INVALID_ARG, "rope3d: n_tokens (%lld) != grid_t*grid_h*grid_w (%lld)",
+                (long long)a.n_tokens, (long long)a.grid_t * a.grid_h * a.grid_w);
+  if (!(a.base > 0.0) || !std::isfinite(a.base)) return fail(SAVGB_ERR_INVALID_ARG, "rope3d: base must be finite and > 0");
+  if (a.t0 < -(1 << 20) || a.t0 > (1 << 20)) return fail(SAVGB_ERR_INVALID_ARG, "rope3d: |t0| > 2^20");
+  if ((double)a.B * a.n_tokens * a.H * (a.D / 8) >= 2147483647.0)
+    return fail(SAVGB_ERR_INVALID_ARG, "rope3d: more than 2^31 16-byte vectors");
+  if (table_bytes(a) > (size_t)kRopeMaxTableBytes)
+    return fail(SAVGB_ERR_INVALID_ARG, "rope3d: angle tables need %zu bytes (> %d)", table_bytes(a), kRopeMaxTableBytes);
+  return SAVGB_OK;
+}
+
+static int launch_rope_multi(const RopeArgs* args, int n, cudaStream_t stream) {
+  int sms = 0;
+  int rc = check_device(&sms);
+  if (rc) return rc;
+  const RopeArgs& a = args[0];
+  RopeKernelArgs k{};
+  k.n_tensors = n;
+  for (int i = 0; i < n; ++i) {
+    k.t[i].in = static_cast<const uint4*>(args[i].in);
+    k.t[i].out = static_cast<uint4*>(args[i].out);
+    k.t[i].in_bs = args[i].in_batch_stride / 8;
+    k.t[i].out_bs = args[i].out_batch_stride / 8;
+  }
+  k.B = a.B;
+  k.n_tokens = (int)a.n_tokens;
+  k.vec_per_tok = a.H * a.D / 8;
+  k.vec_per_head = a.D / 8;
+  k.gt = a.grid_t; k.gh = a.grid_h; k.gw = a.grid_w; k.t0 = a.t0;
+  axis_split(a.D, &k.p_t, &k.p_h, &k.p_w);
+  k.log2_base = (float)std::log2(a.base);
+  k.total = (int)((int64_t)a.B * a.n_tokens * k.vec_per_tok);
+  const size_t smem = table_bytes(a);
+  static bool attr_done[64] = {false};
+  int dev_id = 0;
+  SAVGB_CUDA(cudaGetDevice(&dev_id));
+  if (!attr_done[dev_id & 63]) {
+    SAVGB_CUDA(cudaFuncSetAttribute(rope3d_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kRopeMaxTableBytes));
+    attr_done[dev_id & 63] = true;
+  }
+  const int need = (k.total + kRopeThreads * kRopeUnroll - 1) / (kRopeThreads * kRopeUnroll);
+  const int grid = need < 2 * sms ? (need > 0 ? need : 1) : 2 * sms;
+  rope3d_kernel<<<grid, kRopeThreads, smem, stream>>>(k);
+  SAVGB_CUDA(cudaGetLastError());
+  return SAVGB_OK;
+}
+
+int launch_rope(const RopeArgs& a, cudaStream_t stream) { return launch_rope_multi(&a, 1, stream); }
+
+// Rotates two tensors of the same shape and grid (the chunk's q and k) in one launch.
+int launch_rope_pair(const RopeArgs& a, const RopeArgs& b, cudaStream_t stream) {
+  RopeArgs both[2] = {a, b};
+  return launch_rope_multi(both, 2, stream);
+}
+
+}  // namespace savgb
+
+extern "C" int rope3d_apply(const void* in, void* out, int B, int64_t n_tokens, int H, int D,
+                            int grid_t, int grid_h, int grid_w, int t0, double base,
+                            void* stream) {
+  using namespace savgb;
+  clear_error();
+  RopeArgs a{in, out, B, n_tokens, H, D, grid_t, grid_h, grid_w, t0, base,
+             n_tokens * H * D, n_tokens * H * D};
+  int rc = validate_rope(a);
+  if (rc) return rc;
+  return launch_rope(a, static_cast<cudaStream_t>(stream));
+}

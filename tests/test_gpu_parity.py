@@ -1,0 +1,334 @@
+"""GPU parity of each C-ABI call against the fp64 oracle (bf16 inputs, fp32
+accumulation: max-abs 2e-2, mean-abs 2e-3 on every floating-point output).
+
+Sizes the oracle finishes in seconds span several tiles and a ragged tail;
+the full base-DiT and SR chunk shapes are checked on sampled query rows,
+computed by the oracle one by one against the full key/value set."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from streaming_avatar_video_gb300 import inputs as I
+from tests._util import assert_close, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def S():
+    import __graft_entry__ as g
+    g.build()
+    from streaming_avatar_video_gb300 import savgb
+    torch.cuda.set_device(0)
+    return savgb
+
+
+def bf16(shape, seed, kind=1, std=1.0, chunk=0, step=0):
+    return I.normal_bf16(shape, std, seed, kind, chunk, step)
+
+
+def rows_of(t, rows):
+    return t[:, rows]
+
+
+# ------------------------------------------------------------------- RoPE
+
+@pytest.mark.parametrize("B,gt,gh,gw,H,D,t0", [
+    (1, 2, 4, 4, 2, 64, 0),      # tiny chunk
+    (1, 1, 4, 4, 2, 64, -1),     # reference frame at t = -1
+    (2, 3, 5, 7, 3, 128, -2),    # ragged grid, B = 2, negative start
+    (1, 4, 16, 16, 8, 64, 0),    # small chunk
+    (1, 8, 30, 52, 24, 128, 0),  # base-DiT chunk, every element
+])
+def test_rope3d_parity(S, B, gt, gh, gw, H, D, t0):
+    N = gt * gh * gw
+    x = bf16((B, N, H, D), 11 + D + gt)
+    out = torch.empty((B, N, H, D), dtype=torch.bfloat16, device="cuda")
+    S.rope3d_apply(x.cuda(), out, gt, gh, gw, t0)
+    torch.cuda.synchronize()
+    want = O.rope3d(f64(x), gt, gh, gw, t0, 10000.0)
+    assert_close(f64(out), want, what="rope3d")
+
+
+def test_rope3d_in_place_and_sr_grid(S):
+    B, gt, gh, gw, H, D = 1, 2, 60, 104, 4, 128
+    x = bf16((B, gt * gh * gw, H, D), 5)
+    d = x.cuda()
+    S.rope3d_apply(d, d, gt, gh, gw, -2)
+    torch.cuda.synchronize()
+    assert_close(f64(d), O.rope3d(f64(x), gt, gh, gw, -2, 10000.0), what="rope3d in place")
+
+
+def test_rope3d_identity_at_origin(S):
+    """All positions zero (a 1x1x1 grid at t0 = 0): output == input bit for bit."""
+    x = bf16((3, 1, 5, 128), 9).cuda()
+    out = torch.empty_like(x)
+    S.rope3d_apply(x, out, 1, 1, 1, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(out, x)
+
+
+# -------------------------------------------------------------- attention
+
+def attn_case(S, B, H, D, n_q, seg_lens, seed, scale=0.0, rows=None, lse=False, q_scale=1.0):
+    q = bf16((B, n_q, H, D), seed, I.KIND_Q, std=q_scale)
+    segs = [(bf16((B, n, H, D), seed, I.KIND_K, chunk=i), bf16((B, n, H, D), seed, I.KIND_V, chunk=i))
+            for i, n in enumerate(seg_lens)]
+    dq = q.cuda()
+    dsegs = [(k.cuda(), v.cuda()) for k, v in segs]
+    lse_t = torch.empty((B, H, n_q), dtype=torch.float32, device="cuda") if lse else None
+    o = S.chunk_attention(dq, dsegs, scale=scale, lse=lse_t)
+    torch.cuda.synchronize()
+    S.savgb_device_check()
+    sc = scale if scale > 0 else 1.0 / math.sqrt(D)
+    qq = f64(q) if rows is None else f64(q)[:, rows]
+    want = O.attention(qq, [(f64(k), f64(v)) for k, v in segs], sc)
+    got = f64(o) if rows is None else f64(o)[:, rows]
+    assert_close(got, want, what=f"attention B{B} H{H} D{D} nq{n_q} segs{seg_lens}")
+    if lse:
+        kk = np.concatenate([f64(k) for k, _ in segs], axis=1)
+        s = np.einsum("bnhd,bmhd->bhnm", qq, kk) * sc
+        m = s.max(-1, keepdims=True)
+        want_lse = (m[..., 0] + np.log(np.exp(s - m).sum(-1)))
+        got_lse = f64(lse_t) if rows is None else f64(lse_t)[:, :, rows]
+        assert_close(got_lse, want_lse, max_abs=1e-3, mean_abs=1e-4, what="lse")
+    return o
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_attention_tiny_and_ragged(S, D):
+    attn_case(S, 1, 2, D, 32, [16, 0, 32], 1)                 # tiny chunk 0
+    attn_case(S, 1, 3, D, 300, [100, 37, 300], 2, lse=True)   # ragged q and every segment tail
+    attn_case(S, 2, 2, D, 129, [1, 255, 129], 3)              # B = 2: no cross-batch bleed
+
+
+def test_attention_small_config(S):
+    w = I.WORKLOADS["small"]
+    attn_case(S, 1, w.H, w.D, w.n_q, [w.n_ref, w.n_b, w.n_q], 4, lse=True)
+
+
+def test_attention_single_key_returns_v(S):
+    """One key/value token in total: O = V exactly (p = 1)."""
+    B, H, D, n_q = 1, 2, 128, 200
+    q = bf16((B, n_q, H, D), 7).cuda()
+    k = bf16((B, 1, H, D), 8).cuda()
+    v = bf16((B, 1, H, D), 9).cuda()
+    o = S.chunk_attention(q, [(k, v)])
+    torch.cuda.synchronize()
+    assert torch.equal(o, v.expand(B, n_q, H, D))
+
+
+def test_attention_large_scores_stable(S):
+    """Scores x50: the running max keeps every exponent in range."""
+    attn_case(S, 1, 2, 128, 256, [64, 0, 384], 12, scale=50.0 / math.sqrt(128))
+
+
+def test_attention_lazy_rescale_path(S):
+    """Queries scaled x8 make later tiles raise the row max by far more than
+    the lazy-rescale threshold, so O is rescaled in tensor memory."""
+    attn_case(S, 1, 2, 128, 256, [512, 0, 768], 13, q_scale=8.0)
+
+
+@pytest.mark.parametrize("name", ["base", "sr"])
+def test_attention_full_size_sampled_rows(S, name):
+    w = I.WORKLOADS[name]
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([rng.choice(w.n_q, 40, replace=False),
+                                     [0, 127, 128, 255, w.n_q - 129, w.n_q - 65, w.n_q - 1]]))
+    attn_case(S, w.B, w.H, w.D, w.n_q, [w.n_ref, w.n_b, w.n_q], 21, rows=rows)
+
+
+# ------------------------------------------------------- W_o + Euler update
+
+@pytest.mark.parametrize("M,hid_in,hid_out,bias", [
+    (32, 128, 128, False),      # tiny
+    (1024, 512, 512, True),     # small
+    (300, 384, 400, True),      # ragged M, hid_out not a multiple of 128
+    (1000, 3072, 3072, False),  # base width, ragged M
+])
+def test_out_proj_euler_parity(S, M, hid_in, hid_out, bias):
+    o = bf16((M, hid_in), 31, I.KIND_Q)
+    w = bf16((hid_out, hid_in), 32, I.KIND_WO, std=1.0 / math.sqrt(hid_in))
+    x0 = torch.from_numpy(I.normal_f32((M, hid_out), 1.0, 33, I.KIND_X))
+    b = torch.from_numpy(I.normal_f32((hid_out,), 0.1, 34, I.KIND_BIAS)) if bias else None
+    x = x0.cuda()
+    v = torch.empty((M, hid_out), dtype=torch.float32, device="cuda")
+    dt = 0.0113636
+    S.out_proj_euler_step(o.cuda(), w.cuda(), x, dt, bias=None if b is None else b.cuda(), v_out=v)
+    torch.cuda.synchronize()
+    S.savgb_device_check()
+    want_v = O.out_proj(f64(o), f64(w), None if b is None else f64(b))
+    assert_close(f64(v), want_v, what="velocity")
+    assert_close(f64(x), O.euler_update(f64(x0), want_v, dt), max_abs=1e-4, mean_abs=1e-5, what="x")
+
+
+def test_out_proj_euler_full_base(S):
+    w = I.WORKLOADS["base"]
+    M, hid = w.B * w.n_q, w.hid
+    o = bf16((M, hid), 41, I.KIND_Q, std=0.05)
+    wo = I.out_proj_weight(w, 41)
+    x0 = I.state_x(w, 41)
+    x = x0.cuda()
+    dt = S.flow_time_grid(30, 3.0)[0]
+    S.out_proj_euler_step(o.cuda(), wo.cuda(), x, dt)
+    torch.cuda.synchronize()
+    rows = np.r_[0:64, 6000:6064, M - 64:M]
+    want = O.euler_update(f64(x0)[rows], O.out_proj(f64(o)[rows], f64(wo)), dt)
+    assert_close(f64(x)[rows], want, max_abs=1e-5, mean_abs=1e-6, what="x base rows")
+
+
+# ----------------------------------------------------------- chunk stream
+
+def run_stream_gpu(S, w, seed, chunks, steps=None, bias=None):
+    steps = w.steps if steps is None else steps
+    dts = S.flow_time_grid(steps, w.shift)
+    rk, rv = I.reference_kv(w, seed)
+    wo = I.out_proj_weight(w, seed).cuda()
+    cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                       w.rope_base)
+    cs.set_reference(rk.cuda(), rv.cuda())
+    xs, bnds = [], []
+    for c in range(chunks):
+        bnds.append(cs.boundary())
+        x = torch.from_numpy(I.normal_f32((w.B * w.n_q, w.hid), 1.0, seed, I.KIND_X, c)).cuda()
+        for s, dt in enumerate(dts):
+            st = I.step_inputs(w, seed, c, s)
+            cs.step(st.q.cuda(), st.k.cuda(), st.v.cuda(), wo, x, dt, s == len(dts) - 1, bias=bias)
+        cs.end_chunk()
+        cs.sync()
+        xs.append(x.cpu())
+    return cs, xs, bnds
+
+
+def run_stream_oracle(w, seed, chunks, steps=None):
+    steps = w.steps if steps is None else steps
+    rk, rv = I.reference_kv(w, seed)
+    wo = I.out_proj_weight(w, seed)
+
+    def step_in(c, s):
+        st = I.step_inputs(w, seed, c, s)
+        return f64(st.q), f64(st.k), f64(st.v)
+
+    return O.run_stream(w, f64(rk), f64(rv), f64(wo),
+                        lambda c: I.normal_f32((w.B * w.n_q, w.hid), 1.0, seed, I.KIND_X, c).astype(np.float64),
+                        step_in, O.time_grid(steps, w.shift), chunks=chunks)
+
+
+def test_stream_tiny(S):
+    w = I.WORKLOADS["tiny"]
+    cs, xs, _ = run_stream_gpu(S, w, 0, 1)
+    want, _ = run_stream_oracle(w, 0, 1)
+    assert_close(f64(xs[0]), want[0], what="tiny x")
+    cs.close()
+
+
+def test_stream_small_pair(S):
+    """Two chunks x 4 steps; chunk 1 attends over the boundary rolled from chunk 0."""
+    w = I.WORKLOADS["small"]
+    cs, xs, bnds = run_stream_gpu(S, w, 0, 2)
+    want, wbnds = run_stream_oracle(w, 0, 2)
+    for c in range(2):
+        assert_close(f64(xs[c]), want[c], what=f"small chunk {c} x")
+    assert bnds[0] is None
+    bk, bv = bnds[1]
+    assert_close(f64(bk), wbnds[1][0], what="boundary k (rotated)")
+    assert np.array_equal(f64(bv), wbnds[1][1]), "boundary v is a copy"
+    inf = cs.info()
+    assert inf["chunk_index"] == 2 and inf["boundary_tokens"] == w.n_b
+    cs.close()
+
+
+def test_stream_export_import_resume(S):
+    """Checkpoint after chunk 1, resume in a fresh handle: chunk 2 equals the
+    uninterrupted run."""
+    w = I.Workload("resume", B=2, H=2, D=128, F=3, grid_h=8, grid_w=8, ref_frames=1, boundary_frames=2,
+                   steps=2, shift=3.0)
+    seed = 3
+    cs, xs, _ = run_stream_gpu(S, w, seed, 3)
+    # rerun two chunks, export, import into a new handle, run chunk 2
+    cs2, _, _ = run_stream_gpu(S, w, seed, 2)
+    state = cs2.export_state()
+    cs2.close()
+    rk, rv = I.reference_kv(w, seed)
+    cs3 = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                        w.rope_base)
+    cs3.set_reference(rk.cuda(), rv.cuda())
+    cs3.import_state(state)
+    assert cs3.info()["chunk_index"] == 2
+    wo = I.out_proj_weight(w, seed).cuda()
+    x = torch.from_numpy(I.normal_f32((w.B * w.n_q, w.hid), 1.0, seed, I.KIND_X, 2)).cuda()
+    dts = S.flow_time_grid(w.steps, w.shift)
+    for s, dt in enumerate(dts):
+        st = I.step_inputs(w, seed, 2, s)
+        cs3.step(st.q.cuda(), st.k.cuda(), st.v.cuda(), wo, x, dt, s == len(dts) - 1)
+    cs3.end_chunk()
+    cs3.sync()
+    assert torch.equal(x.cpu(), xs[2])
+    cs3.close()
+    cs.close()
+
+
+def test_stream_memory_is_flat(S):
+    """Device memory in use does not grow with the number of chunks."""
+    w = I.Workload("flat", B=1, H=4, D=128, F=4, grid_h=8, grid_w=12, ref_frames=1, boundary_frames=2,
+                   steps=2, shift=1.0)
+    rk, rv = I.reference_kv(w, 1)
+    wo = I.out_proj_weight(w, 1).cuda()
+    st = I.step_inputs(w, 1, 0, 0)
+    q, k, v = st.q.cuda(), st.k.cuda(), st.v.cuda()
+    x = torch.zeros((w.n_q, w.hid), dtype=torch.float32, device="cuda")
+    cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, 1, 2)
+    cs.set_reference(rk.cuda(), rv.cuda())
+    free = []
+    for c in range(24):
+        for s in range(2):
+            cs.step(q, k, v, wo, x, 0.5, s == 1)
+        cs.end_chunk()
+        cs.sync()
+        free.append(torch.cuda.mem_get_info()[0])
+    assert max(free[1:]) == min(free[1:]), "device memory changed across chunks"
+    assert cs.info()["chunk_index"] == 24
+    cs.close()
+
+
+def test_stream_state_errors(S):
+    w = I.WORKLOADS["tiny"]
+    cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, 1, 1)
+    st = I.step_inputs(w, 0, 0, 0)
+    wo = I.out_proj_weight(w, 0).cuda()
+    x = torch.zeros((w.n_q, w.hid), dtype=torch.float32, device="cuda")
+    with pytest.raises(S.SavgbError) as e:
+        cs.step(st.q.cuda(), st.k.cuda(), st.v.cuda(), wo, x, 0.5, False)
+    assert e.value.status == -7  # no reference yet
+    rk, rv = I.reference_kv(w, 0)
+    cs.set_reference(rk.cuda(), rv.cuda())
+    cs.step(st.q.cuda(), st.k.cuda(), st.v.cuda(), wo, x, 0.5, False)
+    with pytest.raises(S.SavgbError) as e:
+        cs.end_chunk()  # no last step: no boundary captured
+    assert e.value.status == -7
+    cs.close()
+
+
+def test_stream_arena_limit(S, monkeypatch):
+    monkeypatch.setenv("SAVGB_ARENA_LIMIT_BYTES", "1024")
+    with pytest.raises(S.SavgbError) as e:
+        S.ChunkStream(1, 2, 64, 2, 4, 4)
+    assert e.value.status == -4
+
+
+# ------------------------------------------------------------- watchdog
+
+def test_watchdog_timeout_is_reported(S):
+    """A wait on a barrier that nothing arrives on gives up after its limit;
+    the host reads SAVGB_ERR_TIMEOUT and the context stays usable."""
+    S.savgb_device_check()
+    S.savgb_watchdog_selftest(50_000_000)  # 50 ms
+    with pytest.raises(S.SavgbError) as e:
+        S.savgb_device_check()
+    assert e.value.status == -6 and "watchdog" in str(e.value)
+    S.savgb_device_check()  # cleared
+    x = torch.ones(4, device="cuda")
+    assert float((x * 2).sum()) == 8.0

@@ -1,0 +1,101 @@
+"""CPU-side checks of the built library: it loads, exports every symbol that
+include/savgb.h declares, and its host-only logic (time grid, argument
+validation before any launch) behaves."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def S():
+    import __graft_entry__ as g
+    g.build()
+    from streaming_avatar_video_gb300 import savgb
+    return savgb
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "savgb.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(S):
+    names = declared_symbols()
+    assert "chunk_attention" in names and "rope3d_apply" in names and "chunk_stream_step" in names
+    lib = ctypes.CDLL(S.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"libsavgb.so does not export {n}"
+    assert sorted(S.EXPORTS) == names, "binding and header disagree"
+
+
+def test_status_strings(S):
+    L = S.lib()
+    for code, name in S.STATUS.items():
+        assert L.savgb_status_string(code).decode() == name
+    assert S.savgb_version() >= 100
+
+
+@pytest.mark.parametrize("steps,shift", [(1, 1.0), (4, 1.0), (8, 1.0), (30, 3.0), (30, 5.0), (7, 0.5)])
+def test_time_grid_matches_oracle(S, steps, shift):
+    got = np.array(S.flow_time_grid(steps, shift))
+    assert np.allclose(got, O.time_grid(steps, shift), rtol=1e-14, atol=1e-16)
+    assert abs(got.sum() - 1.0) < 1e-13
+
+
+def test_time_grid_rejects_bad_args(S):
+    with pytest.raises(S.SavgbError) as e:
+        S.flow_time_grid(0, 1.0)
+    assert e.value.status == -1
+    buf = (ctypes.c_double * 4)()
+    assert S.lib().flow_time_grid(4, -1.0, buf) == -1
+    assert S.lib().flow_time_grid(4, float("nan"), buf) == -1
+    assert b"shift" in S.lib().savgb_last_error()
+
+
+def test_entry_points_validate_before_launch(S):
+    """Invalid sizes and pointers are refused on the host, with no device call."""
+    L = S.lib()
+    c_vp = ctypes.c_void_p
+    # rope: null, misaligned, grid mismatch, odd D
+    assert L.rope3d_apply(None, None, 1, 8, 1, 64, 2, 2, 2, 0, 1e4, None) == -1
+    assert L.rope3d_apply(c_vp(17), c_vp(32), 1, 8, 1, 64, 2, 2, 2, 0, 1e4, None) == -3
+    assert L.rope3d_apply(c_vp(16), c_vp(32), 1, 9, 1, 64, 2, 2, 2, 0, 1e4, None) == -1
+    assert L.rope3d_apply(c_vp(16), c_vp(32), 1, 8, 1, 60, 2, 2, 2, 0, 1e4, None) == -1
+    assert L.rope3d_apply(c_vp(16), c_vp(32), 1, 8, 1, 64, 2, 2, 2, 0, -1.0, None) == -1
+    # attention: bad head_dim, no segments, zero tokens, misaligned
+    segs = (S.KVSegment * 3)()
+    segs[0] = S.KVSegment(16, 32, 4)
+    assert L.chunk_attention(c_vp(16), 1, 8, 2, 96, segs, 1, 0.0, c_vp(16), None, None) == -2
+    assert L.chunk_attention(c_vp(16), 1, 8, 2, 64, segs, 0, 0.0, c_vp(16), None, None) == -1
+    segs[0] = S.KVSegment(16, 32, 0)
+    assert L.chunk_attention(c_vp(16), 1, 8, 2, 64, segs, 1, 0.0, c_vp(16), None, None) == -1
+    segs[0] = S.KVSegment(24, 32, 4)
+    assert L.chunk_attention(c_vp(16), 1, 8, 2, 64, segs, 1, 0.0, c_vp(16), None, None) == -3
+    # projection: bad sizes
+    assert L.out_proj_euler_step(c_vp(16), c_vp(16), None, c_vp(16), 4, 12, 16, 0.1, None, None) == -1
+    assert L.out_proj_euler_step(c_vp(16), c_vp(16), None, c_vp(16), 4, 16, 24, 0.1, None, None) == -1
+    assert L.out_proj_euler_step(c_vp(16), c_vp(16), None, c_vp(16), 0, 16, 16, 0.1, None, None) == -1
+    # stream: bad config
+    cfg = S.ChunkStreamConfig(1, 2, 96, 2, 4, 4, 1, 0, -1, 1e4, 0.0)
+    h = ctypes.c_void_p()
+    assert L.chunk_stream_create(ctypes.byref(cfg), None, ctypes.byref(h)) == -2
+    cfg = S.ChunkStreamConfig(1, 2, 64, 2, 4, 4, 1, 3, -1, 1e4, 0.0)  # boundary_frames > F
+    assert L.chunk_stream_create(ctypes.byref(cfg), None, ctypes.byref(h)) == -1
+    assert L.chunk_stream_end_chunk(None) == -1
+    assert L.chunk_stream_destroy(None) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    from streaming_avatar_video_gb300 import savgb
+    monkeypatch.setattr(savgb, "_lib", None)
+    monkeypatch.setattr(savgb, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        savgb.lib()
