@@ -1,0 +1,455 @@
+"""Benchmark of the chunk denoising step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config base|sr|long|small]
+                    [--impl ours|reference]
+
+One step is one pass of the whole hot path through the library's public API
+(chunk_stream_step): 3D RoPE of the chunk's q and k, attention of the chunk's
+queries over [reference | boundary | chunk], and the W_o GEMM with the Euler
+update fused into its epilogue; the last step of every chunk also rolls the
+boundary.  Inputs are seeded synthetic tensors shaped like the workload, two
+input sets alternate between steps (each larger than the 129 MB L2), resident
+in HBM before timing.  Each rank runs an independent replica (sessions are
+independent; no collective on the data path), so scaling is weak.
+
+Printed: one JSON line on rank 0.  value = dense attention TFLOP per step /
+device time per step (whole job); e2e = the same with, every step, the host ->
+device copy of the step's q, k, v from pinned memory and the device -> host
+read of the updated state x inside the timed region.  The reference arm
+(--impl reference) times the fp64 CPU oracle on a bounded sample of the same
+workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from streaming_avatar_video_gb300 import inputs as I  # noqa: E402
+
+METRIC = "chunk-attention TFLOP/s (% of bf16 tensor peak); latent frames/s per denoise step"
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
+def describe(w: I.Workload) -> str:
+    return (f"{w.name}: B{w.B} H{w.H} D{w.D} chunk {w.F}x{w.grid_h}x{w.grid_w}={w.n_q} q tokens, "
+            f"{w.n_ref} ref + {w.n_b} boundary + {w.n_q} chunk kv tokens, "
+            f"{w.steps} Euler steps/chunk (shift {w.shift:g})")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
+    import __graft_entry__ as g
+    g.build()
+    from streaming_avatar_video_gb300 import savgb as S
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    seed = 1 + rank
+    dts = S.flow_time_grid(w.steps, w.shift)
+
+    # two input sets (each > L2) alternate between steps; generated on the host, resident in HBM
+    sets = []
+    for c in range(2):
+        st = I.step_inputs(w, seed, c, 0)
+        sets.append((st.q, st.k, st.v))
+    dsets = [tuple(t.to(dev) for t in s) for s in sets]
+    rk, rv = I.reference_kv(w, seed)
+    wo = I.out_proj_weight(w, seed).to(dev)
+    x = I.state_x(w, seed).to(dev)
+
+    cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                       w.rope_base)
+    cs.set_reference(rk.to(dev), rv.to(dev))
+    # prime: one chunk end so that every timed step attends over the boundary too
+    q, k, v = dsets[0]
+    cs.step(q, k, v, wo, x, dts[0], True)
+    cs.end_chunk()
+
+    state = {"i": 0, "launches": 0}
+
+    def one_step(events=None):
+        i = state["i"]
+        s = i % w.steps
+        q, k, v = dsets[i & 1]
+        last = s == w.steps - 1
+        if events is not None:
+            cs.set_step_events(events)
+        cs.step(q, k, v, wo, x, dts[s], last)
+        state["launches"] += 3 + (1 if last and w.boundary_frames > 0 else 0)
+        if last:
+            cs.end_chunk()
+        state["i"] = i + 1
+
+    for _ in range(args.warmup):
+        one_step()
+    cs.sync()
+
+    # timed region: K steps, per-step events around each stage
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    state["launches"] = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for k_ in range(args.steps):
+            one_step(ev[k_])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    launches = state["launches"]
+    cs.sync()
+    ms_local = start.elapsed_time(end)
+    ms_total = max_over_ranks(world, ms_local)
+    ms_step = ms_total / args.steps
+    rope_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    wo_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    clocks = clk.summary()
+
+    attn_flops = w.attn_flops(True)
+    value = world * attn_flops / (ms_step * 1e-3) / 1e12
+    frames_per_s = world * w.B * w.F / (ms_step * 1e-3)
+    attn_tflops = attn_flops / (attn_ms * 1e-3) / 1e12
+    pk, pk_kind = peaks()
+    peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    rope_bytes = 2 * 2 * 2 * w.B * w.n_q * w.hid  # q and k, read + write, 2 bytes each
+    wo_flops = w.wo_flops()
+
+    # end-to-end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world)
+    cs.close()
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v/ref, W_o ~ N(0,1/hid), x ~ N(0,1))",
+        "config": {
+            "workload": describe(w),
+            "parallelism": f"replicas x{world} (independent sessions)",
+            "global_batch": world * w.B,
+            "l2": "inputs larger than L2: two alternating input sets of "
+                  f"{3 * w.B * w.n_q * w.hid * 2 / 1e6:.0f} MB",
+        },
+        "latent_frames_per_s": round(frames_per_s, 1),
+        "pct_of_bf16_peak": {"nominal_2250": round(100 * attn_tflops / NOMINAL_BF16_TFLOPS, 1),
+                             f"{pk_kind}_sustained": round(100 * attn_tflops / peak, 1)},
+        "kernels_ms": {"rope3d_qk": round(rope_ms, 4), "chunk_attention": round(attn_ms, 4),
+                       "out_proj_euler": round(wo_ms, 4)},
+        "kernel_rates": {
+            "chunk_attention_tflops": round(attn_tflops, 1),
+            "out_proj_euler_tflops": round(wo_flops / (wo_ms * 1e-3) / 1e12, 1),
+            "rope3d_gbs": round(rope_bytes / (rope_ms * 1e-3) / 1e9, 1),
+        },
+        "roofline": {
+            "kernel": "chunk_attention (attn_fwd_kernel<128>)",
+            "bound": "tensor",
+            "achieved": round(attn_tflops, 1),
+            "peak": peak,
+            "peak_kind": f"{pk_kind} bf16 sustained (cuBLAS, timed inside a long loop)",
+            "unit": "TFLOP/s",
+            "frac": round(attn_tflops / peak, 4),
+            "traffic": None,
+            "algorithmic": f"4*B*H*Nq*Nkv*D = {attn_flops / 1e12:.4f} TFLOP per launch",
+        },
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": None,
+    }
+    return result
+
+
+def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world):
+    """Same metric through ChunkStream.step with host buffers: every step copies
+    q, k, v from pinned host memory and reads x back into pinned memory."""
+    hsets = [tuple(t.pin_memory() for t in s) for s in sets]
+    dq, dk, dv = (torch.empty_like(t, device=dev) for t in sets[0])
+    hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    n = max(3, min(args.steps, 60))
+    i0 = [0]
+
+    def step():
+        i = i0[0]
+        s = i % w.steps
+        hq, hk, hv = hsets[i & 1]
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        last = s == w.steps - 1
+        cs.step(dq, dk, dv, wo, x, dts[s], last)
+        if last:
+            cs.end_chunk()
+        hx.copy_(x, non_blocking=True)
+        i0[0] = i + 1
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(world, a.elapsed_time(b)) / n
+    h2d = sum(t.numel() * t.element_size() for t in sets[0])
+    d2h = x.numel() * x.element_size()
+    return {"value": round(world * w.attn_flops(True) / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "ChunkStream.step (C ABI chunk_stream_step) with pinned host q/k/v in, x out"}
+
+
+# ------------------------------------------------------------- oracle arm
+
+class OracleSample:
+    """The fp64 CPU oracle on a bounded sample of one step of ``w``.
+
+    Untimed set-up: the step's inputs and the rotated reference, boundary and
+    chunk keys (the keys every query row needs).  Timed: RoPE of ``frames``
+    latent frames of q and k, then attention over the full key/value set,
+    W_o and the Euler update for ``rows`` random query rows of every session
+    and head.  Both parts scale linearly (RoPE in frames, the rest in rows),
+    so the per-step time is extrapolated from the sample."""
+
+    def __init__(self, w: I.Workload, seed: int = 1):
+        import oracle as O
+        self.O, self.w = O, w
+        st = I.step_inputs(w, seed, 0, 0)
+        rk, rv = I.reference_kv(w, seed)
+        bk, bv = I.boundary_kv(w, seed)
+        self.wo = I.out_proj_weight(w, seed).double().numpy()
+        self.x = I.state_x(w, seed).numpy().astype(np.float64)
+        self.q, self.k, self.v = (t.double().numpy() for t in (st.q, st.k, st.v))
+        self.segs = [
+            (O.rope3d(rk.double().numpy(), w.ref_frames, w.grid_h, w.grid_w, w.ref_t, w.rope_base),
+             rv.double().numpy()),
+            (O.rope3d(bk.double().numpy(), w.boundary_frames, w.grid_h, w.grid_w, -w.boundary_frames,
+                      w.rope_base) if w.n_b else np.zeros((w.B, 0, w.H, w.D)), bv.double().numpy()),
+            (O.rope3d(self.k, w.F, w.grid_h, w.grid_w, 0, w.rope_base), self.v),
+        ]
+        self.q_rot = O.rope3d(self.q, w.F, w.grid_h, w.grid_w, 0, w.rope_base)
+        self.dt = O.time_grid(w.steps, w.shift)[0]
+        self.rng = np.random.default_rng(seed)
+
+    def run(self, rows: int, frames: int):
+        O, w = self.O, self.w
+        rows = min(rows, w.n_q)
+        frames = min(frames, w.F)
+        sel = np.sort(self.rng.choice(w.n_q, size=rows, replace=False))
+        nf = frames * w.frame_tokens
+        t0 = time.perf_counter()
+        O.rope3d(self.q[:, :nf], frames, w.grid_h, w.grid_w, 0, w.rope_base)
+        O.rope3d(self.k[:, :nf], frames, w.grid_h, w.grid_w, 0, w.rope_base)
+        t1 = time.perf_counter()
+        o = O.attention(self.q_rot[:, sel], self.segs)
+        flat_rows = (np.arange(w.B)[:, None] * w.n_q + sel[None, :]).reshape(-1)
+        vel = O.out_proj(o.reshape(-1, w.hid), self.wo)
+        O.euler_update(self.x[flat_rows], vel, self.dt)
+        t2 = time.perf_counter()
+        per_step = (t1 - t0) * (w.F / frames) + (t2 - t1) * (w.n_q / rows)
+        desc = (f"oracle on {rows} of {w.n_q} query rows x {w.B} sessions x {w.H} heads over all "
+                f"{w.n_kv} kv tokens, + RoPE of {frames} of {w.F} frames of q and k; per-step time "
+                f"extrapolated linearly (rows, frames)")
+        return t2 - t0, per_step, desc
+
+    def calibrated(self, budget_s: float):
+        """Rows and frames whose sample takes about ``budget_s`` seconds."""
+        secs, _, _ = self.run(16, 1)
+        rows = int(max(8, min(self.w.n_q, 16 * budget_s / max(secs, 1e-3))))
+        frames = 1 if budget_s < 5 else self.w.F
+        return rows, frames
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w: I.Workload, budget_s: float):
+    smp = OracleSample(w)
+    rows, frames = smp.calibrated(budget_s)
+    secs, per_step, desc = smp.run(rows, frames)
+    return {"value": round(w.attn_flops(True) / per_step / 1e12, 6), "unit": "TFLOP/s",
+            "cores": cpu_cores(), "kind": "oracle", "sample": desc,
+            "sample_seconds": round(secs, 2), "extrapolated_s_per_step": round(per_step, 2),
+            "threads": "numpy BLAS default (all affinity cores)"}
+
+
+def run_reference(args, w: I.Workload, world: int, rank: int):
+    if rank != 0:
+        return None
+    smp = OracleSample(w)
+    budget = min(20.0, max(0.05, 100.0 / (args.steps + args.warmup)))
+    rows, frames = smp.calibrated(budget)
+    per = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        _, per_step, desc = smp.run(rows, frames)
+        if i >= args.warmup:
+            per.append(per_step)
+    ms = 1e3 * statistics.mean(per)
+    value = w.attn_flops(True) / (ms * 1e-3) / 1e12
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": describe(w)},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="base", choices=["base", "sr", "long", "small", "tiny"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the oracle's timed sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = I.WORKLOADS[args.config]
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, w, world, rank)
+        if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res = run_ours(args, w, world, rank, local)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -208,6 +208,14 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
  * boundary_frames > 0). */
 int chunk_stream_end_chunk(chunk_stream_t* s);
 
+/* Optional timing of the next step: `events` holds 4 cudaEvent_t that the
+ * next chunk_stream_step records on the handle's stream at its start, after
+ * the RoPE launch, after the attention launch and after the W_o/Euler launch.
+ * They apply to one step only; NULL clears them.  (A library facility with
+ * no counterpart on the pages: it lets a caller attribute step time to the
+ * kernels as they run inside a loop.) */
+int chunk_stream_set_step_events(chunk_stream_t* s, void* const* events);
+
 /* Synchronises the handle's stream and reports device-side errors. */
 int chunk_stream_sync(chunk_stream_t* s);
 

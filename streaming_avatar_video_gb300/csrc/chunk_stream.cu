@@ -51,6 +51,8 @@ struct chunk_stream {
   bool captured;
   bool ref_set;
   int64_t chunk_index;
+  cudaEvent_t step_events[4];  // recorded by the next step, then cleared
+  bool have_events;
 };
 
 namespace {
@@ -182,10 +184,14 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
   if (!std::isfinite(dt)) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_step: dt must be finite");
   const chunk_stream_config& c = s->cfg;
   const int64_t per_b = s->n_tok * s->hid;
+  const bool ev = s->have_events;
+  s->have_events = false;
+  if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[0], s->stream));
   RopeArgs aq = rope_args(s, q, s->q_rot, per_b, per_b, c.F, 0);
   RopeArgs ak = rope_args(s, k, s->k_rot, per_b, per_b, c.F, 0);
   int rc = launch_rope_pair(aq, ak, s->stream);
   if (rc) return rc;
+  if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[1], s->stream));
   AttnSeg segs[3] = {
       {s->ref_k, s->ref_v, s->n_ref},
       {s->bnd_k[s->cur], s->bnd_v[s->cur], s->bnd_in_use},
@@ -194,9 +200,11 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
   rc = launch_attention(s->q_rot, c.B, s->n_tok, c.H, c.D, segs, 3, c.softmax_scale, s->o, nullptr,
                         s->stream);
   if (rc) return rc;
+  if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[2], s->stream));
   rc = launch_out_proj_euler(s->o, w_o, bias, x, c.B * s->n_tok, (int)s->hid, (int)s->hid, dt,
                              nullptr, s->stream);
   if (rc) return rc;
+  if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[3], s->stream));
   if (is_last_step && s->n_bnd > 0) {
     const int nxt = s->cur ^ 1;
     const int64_t tail = (s->n_tok - s->n_bnd) * s->hid;
@@ -226,6 +234,21 @@ int chunk_stream_end_chunk(chunk_stream_t* s) {
   }
   s->captured = false;
   s->chunk_index += 1;
+  return SAVGB_OK;
+}
+
+int chunk_stream_set_step_events(chunk_stream_t* s, void* const* events) {
+  clear_error();
+  if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_set_step_events: null handle");
+  if (!events) {
+    s->have_events = false;
+    return SAVGB_OK;
+  }
+  for (int i = 0; i < 4; ++i) {
+    if (!events[i]) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_set_step_events: null event %d", i);
+    s->step_events[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  s->have_events = true;
   return SAVGB_OK;
 }
 

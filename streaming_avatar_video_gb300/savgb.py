@@ -29,7 +29,7 @@ EXPORTS = (
     "savgb_status_string", "savgb_last_error", "savgb_version", "savgb_device_check",
     "savgb_watchdog_selftest", "rope3d_apply", "chunk_attention", "out_proj_euler_step",
     "flow_time_grid", "chunk_stream_create", "chunk_stream_set_reference", "chunk_stream_step",
-    "chunk_stream_end_chunk", "chunk_stream_sync", "chunk_stream_info", "chunk_stream_export_state",
+    "chunk_stream_end_chunk", "chunk_stream_set_step_events", "chunk_stream_sync", "chunk_stream_info", "chunk_stream_export_state",
     "chunk_stream_import_state", "chunk_stream_destroy",
 )
 
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
         "chunk_stream_set_reference": (c_int, [c_vp, c_vp, c_vp]),
         "chunk_stream_step": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f, c_int]),
         "chunk_stream_end_chunk": (c_int, [c_vp]),
+        "chunk_stream_set_step_events": (c_int, [c_vp, ctypes.POINTER(c_vp)]),
         "chunk_stream_sync": (c_int, [c_vp]),
         "chunk_stream_info": (c_int, [c_vp, ctypes.POINTER(c_i64), ctypes.POINTER(c_i64), ctypes.POINTER(c_i64),
                                       ctypes.POINTER(c_vp), ctypes.POINTER(c_vp)]),
@@ -259,6 +260,21 @@ class ChunkStream:
 
     def end_chunk(self) -> None:
         _check(lib().chunk_stream_end_chunk(self.handle))
+
+    def set_step_events(self, events) -> None:
+        """events: 4 torch.cuda.Event (created with enable_timing) recorded by
+        the next step at its start, after RoPE, after attention and after
+        the W_o/Euler GEMM; None clears them."""
+        if events is None:
+            _check(lib().chunk_stream_set_step_events(self.handle, None))
+            return
+        if len(events) != 4:
+            raise ValueError("4 events")
+        for e in events:
+            if not e.cuda_event:  # torch creates the CUDA event on its first record
+                e.record()
+        arr = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
+        _check(lib().chunk_stream_set_step_events(self.handle, arr))
 
     def sync(self) -> None:
         _check(lib().chunk_stream_sync(self.handle))
