@@ -237,6 +237,37 @@ int chunk_stream_import_state(chunk_stream_t* s, const void* buf, size_t size);
 /* Frees the arena and the handle (after synchronising its stream). */
 int chunk_stream_destroy(chunk_stream_t* s);
 
+/* --------------------------------------------------------------------------
+ * chunk_step_noalloc - one chunk denoising step that allocates no device
+ * memory.  The pages have no counterpart to this call: it serves callers that
+ * cannot call cudaMalloc, such as a plugin inside a serving runtime that owns
+ * every device allocation and offers plugins no allocator, or a real-time loop
+ * that may not allocate (or synchronise the device through an allocation) once
+ * the session runs.  Such callers cannot create a chunk_stream handle.
+ *
+ * Computes what chunk_stream_step computes: RoPE of q and k at chunk-local
+ * positions, attention over [context segments | chunk], and the W_o GEMM with
+ * the Euler update x <- x + dt * (O W_o^T + bias).  The caller keeps the
+ * rolling state itself: `context` holds 0 to 2 already-rotated segments (the
+ * reference, then the boundary, as rope3d_apply produces them), each bf16
+ * [B][n][H][D].  q, k, v: bf16 [B][N][H][D], N = F*grid_h*grid_w; w_o bf16
+ * [H*D][H*D]; bias optional fp32 [H*D]; x fp32 [B*N][H*D], updated in place.
+ *
+ * The step's intermediates (rotated q, rotated k, attention output: 3 x
+ * B*N*H*D bf16, each rounded up to 256 bytes) live in one file-scope device
+ * array of SAVGB_NOALLOC_SCRATCH_BYTES, which every device that loads the
+ * library holds until the process exits.  Larger steps are rejected with
+ * SAVGB_ERR_INVALID_ARG.  The array's address is looked up on the first call
+ * made on each device; make that call before any stream capture.  All calls
+ * share the array, so calls that overlap on the GPU race; nothing in it needs
+ * clearing between calls.
+ * ------------------------------------------------------------------------ */
+#define SAVGB_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int chunk_step_noalloc(const void* q, const void* k, const void* v, const savgb_kv_segment* context,
+                       int n_context, const void* w_o, const float* bias, float* x, float dt, int B,
+                       int H, int D, int F, int grid_h, int grid_w, double rope_base,
+                       float softmax_scale, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

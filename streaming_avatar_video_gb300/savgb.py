@@ -30,7 +30,7 @@ EXPORTS = (
     "savgb_watchdog_selftest", "rope3d_apply", "chunk_attention", "out_proj_euler_step",
     "flow_time_grid", "chunk_stream_create", "chunk_stream_set_reference", "chunk_stream_step",
     "chunk_stream_end_chunk", "chunk_stream_set_step_events", "chunk_stream_sync", "chunk_stream_info", "chunk_stream_export_state",
-    "chunk_stream_import_state", "chunk_stream_destroy",
+    "chunk_stream_import_state", "chunk_stream_destroy", "chunk_step_noalloc",
 )
 
 
@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
         "chunk_stream_export_state": (c_int, [c_vp, c_vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]),
         "chunk_stream_import_state": (c_int, [c_vp, c_vp, ctypes.c_size_t]),
         "chunk_stream_destroy": (c_int, [c_vp]),
+        "chunk_step_noalloc": (c_int, [c_vp, c_vp, c_vp, ctypes.POINTER(KVSegment), c_int, c_vp, c_vp, c_vp, c_f,
+                                       c_int, c_int, c_int, c_int, c_int, c_int, c_d, c_f, c_vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -323,3 +325,40 @@ class ChunkStream:
             self.close()
         except Exception:
             pass
+
+
+# ------------------------------------------------------ allocation-free step
+
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def chunk_step_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                       context: Sequence[Tuple[torch.Tensor, torch.Tensor]], w_o: torch.Tensor,
+                       x: torch.Tensor, dt: float, grid: Tuple[int, int, int], bias: Optional[torch.Tensor] = None,
+                       rope_base: float = 10000.0, softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
+    """One chunk step whose intermediates live in the library's fixed device
+    scratch array (no allocation by the library).  For callers that cannot
+    allocate device memory while a session runs; the caller passes the
+    already-rotated reference / boundary segments in ``context``.
+    grid = (F, grid_h, grid_w)."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, 4)
+    B, N, H, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have one shape")
+    if len(context) > 2:
+        raise ValueError("0 to 2 context segments")
+    segs = (KVSegment * 2)()
+    for i, (ck, cv) in enumerate(context):
+        _need(ck, f"context[{i}].k", torch.bfloat16, 4)
+        _need(cv, f"context[{i}].v", torch.bfloat16, 4)
+        segs[i] = KVSegment(ck.data_ptr(), cv.data_ptr(), ck.shape[1])
+    _need(w_o, "w_o", torch.bfloat16, 2)
+    _need(x, "x", torch.float32)
+    if bias is not None:
+        _need(bias, "bias", torch.float32, 1)
+    F, gh, gw = grid
+    _check(lib().chunk_step_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), segs, len(context), w_o.data_ptr(),
+                                    _ptr(bias), x.data_ptr(), float(dt), B, H, D, F, gh, gw, float(rope_base),
+                                    float(softmax_scale), _stream(stream)))
+    return x
