@@ -10,11 +10,17 @@
 //   warp 0      TMA producer: Q tiles once, then K and V tiles of the
 //               concatenated segments through a 2-stage ring each.
 //   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma.
-//   warps 2-5   softmax of query tile 0, warps 6-9 of query tile 1; thread =
+//   warps 2-3   idle (they complete the first warpgroup).
+//   warps 4-7   softmax of query tile 0, warps 8-11 of query tile 1; thread =
 //               one query row (TMEM lane), so row max and sum need no shuffle.
+// Registers: the block launches with 168 per thread; the first warpgroup
+// gives back down to 88 and the two softmax warpgroups take 208 each
+// (setmaxnreg), so a thread holds a whole 128-column score row without spills.
 // TMEM columns: S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D,256+2D).
 // P (bf16) overwrites the first 64 columns of its S and feeds the PV product
-// straight from TMEM.  The two query tiles alternate so that the tensor core
+// straight from TMEM; each half of a row's probabilities is published as
+// soon as it is written, so PV over the first 64 keys overlaps the
+// exponentials of the last 64.  The two query tiles alternate so that the tensor core
 // works on one tile's QK^T / PV while the other tile's softmax runs.
 // The running max is updated lazily (only when it grows by more than 2^8 in
 // probability), and O is rescaled in TMEM by the softmax warps when it is.
@@ -30,10 +36,23 @@
 namespace savgb {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kRegsLow = 88;     // producer / MMA warpgroup after setmaxnreg.dec
+constexpr int kRegsHigh = 208;  // softmax warpgroups after setmaxnreg.inc
+// the split must fit the block's launch pool: kThreads * launch registers
+constexpr int kRegPoolNeeded = 128 * kRegsLow + 256 * kRegsHigh;
 constexpr int kBlockQ = 256;  // two 128-row tiles
 constexpr int kTileKV = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// K / V ring depths: 128-row tiles of 32 KiB (D=128) or 16 KiB (D=64)
+#ifndef SAVGB_ATTN_KS128
+#define SAVGB_ATTN_KS128 3
+#endif
+#ifndef SAVGB_ATTN_VS128
+#define SAVGB_ATTN_VS128 2
+#endif
+constexpr int kStagesK128 = SAVGB_ATTN_KS128, kStagesV128 = SAVGB_ATTN_VS128;
+constexpr int kStagesK64 = 4, kStagesV64 = 4;
 
 struct AttnMaps {
   CUtensorMap q;
@@ -51,30 +70,31 @@ struct AttnParams {
   DeviceErrorWord* err;
 };
 
-template <int D>
+template <int D, int KS, int VS>
 struct Layout {
   static constexpr int kTileBytes = 128 * D * 2;  // one 128-row tile, D/64 swizzled column blocks
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + 2 * kTileBytes;
-  static constexpr int kV = kK + 2 * kTileBytes;
-  static constexpr int kBar = kV + 2 * kTileBytes;
-  static constexpr int kNumBars = 16;
+  static constexpr int kV = kK + KS * kTileBytes;
+  static constexpr int kBar = kV + VS * kTileBytes;
+  // barriers: Q full, K full/empty per stage, V full/empty per stage,
+  // S full / P full / O done per query tile, MMA drain
+  static constexpr int kQFull = 0;
+  static constexpr int kKFull = 1;
+  static constexpr int kKEmpty = kKFull + KS;
+  static constexpr int kVFull = kKEmpty + KS;
+  static constexpr int kVEmpty = kVFull + VS;
+  static constexpr int kSFull = kVEmpty + VS;
+  static constexpr int kPLo = kSFull + 2;  // first 64 probabilities of a row written
+  static constexpr int kPHi = kPLo + 2;    // last 64 written
+  static constexpr int kODone = kPHi + 2;
+  static constexpr int kDrain = kODone + 2;
+  static constexpr int kNumBars = kDrain + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   // request at least 120 KiB so two blocks never share an SM (each holds all 512 TMEM columns)
   static constexpr int kDynSmem = (kBytes + 1024 > 120 * 1024) ? kBytes + 1024 : 120 * 1024;
-};
-
-enum Bar {
-  kQFull = 0,
-  kKFull = 1,   // +stage
-  kKEmpty = 3,  // +stage
-  kVFull = 5,   // +stage
-  kVEmpty = 7,  // +stage
-  kSFull = 9,   // +tile
-  kPFull = 11,  // +tile
-  kODone = 13,  // +tile
-  kDrain = 15,
+  static_assert(kBytes + 1024 <= 227 * 1024, "shared memory budget");
 };
 
 __device__ __forceinline__ void tile_of(const AttnParams& p, int j, int& seg, int& row0, int& valid) {
@@ -96,10 +116,10 @@ __device__ __forceinline__ void give_up(const AttnParams& p, volatile int* abort
   }
 }
 
-template <int D>
+template <int D, int KS, int VS>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p) {
-  using L = Layout<D>;
+  using L = Layout<D, KS, VS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = dev::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -115,17 +135,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = blockIdx.x * kBlockQ;
 
   if (tid == 0) {
-    dev::mbar_init(&bars[kQFull], 1);
-    for (int s = 0; s < 2; ++s) {
-      dev::mbar_init(&bars[kKFull + s], 1);
-      dev::mbar_init(&bars[kKEmpty + s], 1);
-      dev::mbar_init(&bars[kVFull + s], 1);
-      dev::mbar_init(&bars[kVEmpty + s], 1);
-      dev::mbar_init(&bars[kSFull + s], 1);
-      dev::mbar_init(&bars[kPFull + s], 128);
-      dev::mbar_init(&bars[kODone + s], 1);
+    dev::mbar_init(&bars[L::kQFull], 1);
+    for (int s = 0; s < KS; ++s) {
+      dev::mbar_init(&bars[L::kKFull + s], 1);
+      dev::mbar_init(&bars[L::kKEmpty + s], 1);
     }
-    dev::mbar_init(&bars[kDrain], 1);
+    for (int s = 0; s < VS; ++s) {
+      dev::mbar_init(&bars[L::kVFull + s], 1);
+      dev::mbar_init(&bars[L::kVEmpty + s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      dev::mbar_init(&bars[L::kSFull + x], 1);
+      dev::mbar_init(&bars[L::kPLo + x], 4);  // one elected lane per softmax warp
+      dev::mbar_init(&bars[L::kPHi + x], 4);
+      dev::mbar_init(&bars[L::kODone + x], 1);
+    }
+    dev::mbar_init(&bars[L::kDrain], 1);
     *abort = 0;
     dev::fence_barrier_init();
   }
@@ -148,136 +173,149 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int n = p.n_tiles;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint8_t* sQ = smem + L::kQ;
-      uint8_t* sK = smem + L::kK;
-      uint8_t* sV = smem + L::kV;
-      dev::mbar_arrive_expect_tx(&bars[kQFull], 2 * L::kTileBytes);
-      #pragma unroll
-      for (int x = 0; x < 2; ++x)
+  if (warp < 4) {
+    dev::setmaxnreg_dec<kRegsLow>();
+    if ((warp == 0 || warp == 2) && lane == 0) {
+      // ------------------------------------------- producers: K (warp 0), V (warp 2)
+      const bool is_k = warp == 0;
+      const int stages = is_k ? KS : VS;
+      uint8_t* ring = smem + (is_k ? L::kK : L::kV);
+      uint64_t* full = &bars[is_k ? L::kKFull : L::kVFull];
+      uint64_t* empty = &bars[is_k ? L::kKEmpty : L::kVEmpty];
+      const CUtensorMap* seg_map[3] = {is_k ? &maps.k[0] : &maps.v[0], is_k ? &maps.k[1] : &maps.v[1],
+                                       is_k ? &maps.k[2] : &maps.v[2]};
+      if (is_k) {
+        uint8_t* sQ = smem + L::kQ;
+        dev::mbar_arrive_expect_tx(&bars[L::kQFull], 2 * L::kTileBytes);
         #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          dev::tma_load_4d(sQ + x * L::kTileBytes + c * 16384, &maps.q, &bars[kQFull], c * 64, h,
-                           q0 + x * 128, b);
+        for (int x = 0; x < 2; ++x)
+          #pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            dev::tma_load_4d(sQ + x * L::kTileBytes + c * 16384, &maps.q, &bars[L::kQFull], c * 64, h,
+                             q0 + x * 128, b);
+      }
       int issued = 0;
       for (int j = 0; j < n; ++j) {
         int seg, row0, valid;
         tile_of(p, j, seg, row0, valid);
-        const int st = j & 1;
-        const uint32_t use = j >> 1;
-        if (j >= 2 && !dev::mbar_wait(&bars[kKEmpty + st], (use - 1) & 1, abort)) {
-          give_up(p, abort, 1);
+        const int st = j % stages;
+        const uint32_t use = j / stages;
+        if (j >= stages && !dev::mbar_wait(&empty[st], (use - 1) & 1, abort)) {
+          give_up(p, abort, is_k ? 1 : 2);
           break;
         }
-        dev::mbar_arrive_expect_tx(&bars[kKFull + st], L::kTileBytes);
+        dev::mbar_arrive_expect_tx(&full[st], L::kTileBytes);
         #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          dev::tma_load_4d(sK + st * L::kTileBytes + c * 16384, &maps.k[seg], &bars[kKFull + st],
-                           c * 64, h, row0, b);
-        if (j >= 2 && !dev::mbar_wait(&bars[kVEmpty + st], (use - 1) & 1, abort)) {
-          give_up(p, abort, 2);
-          issued = 2 * j + 1;
-          break;
-        }
-        dev::mbar_arrive_expect_tx(&bars[kVFull + st], L::kTileBytes);
-        #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          dev::tma_load_4d(sV + st * L::kTileBytes + c * 16384, &maps.v[seg], &bars[kVFull + st],
-                           c * 64, h, row0, b);
-        issued = 2 * (j + 1);
+          dev::tma_load_4d(ring + st * L::kTileBytes + c * 16384, seg_map[seg], &full[st], c * 64, h,
+                           row0, b);
+        issued = j + 1;
       }
       // drain: every issued copy has landed before the block may exit
       volatile int never = 0;
-      dev::mbar_wait(&bars[kQFull], 0, &never);
-      const int nk = (issued + 1) / 2, nv = issued / 2;  // K tiles and V tiles issued
-      for (int t = (nk > 2 ? nk - 2 : 0); t < nk; ++t)
-        dev::mbar_wait(&bars[kKFull + (t & 1)], (t >> 1) & 1, &never);
-      for (int t = (nv > 2 ? nv - 2 : 0); t < nv; ++t)
-        dev::mbar_wait(&bars[kVFull + (t & 1)], (t >> 1) & 1, &never);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+      if (is_k) dev::mbar_wait(&bars[L::kQFull], 0, &never);
+      for (int t = (issued > stages ? issued - stages : 0); t < issued; ++t)
+        dev::mbar_wait(&full[t % stages], (t / stages) & 1, &never);
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       const uint32_t sQ = dev::smem_u32(smem + L::kQ);
       const uint32_t sK = dev::smem_u32(smem + L::kK);
       const uint32_t sV = dev::smem_u32(smem + L::kV);
       constexpr uint32_t idesc_s = dev::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_o = dev::idesc_bf16_f32(128, D, false, true);
+      // descriptors of the region starts; an operand at byte offset `off`
+      // inside a region is its descriptor + off/16 (the address field never
+      // carries: shared-memory addresses stay below 2^18)
+      const uint64_t dQ = dev::sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dK = dev::sdesc_sw128(sK, 16, 1024);
+      const uint64_t dV = dev::sdesc_sw128(sV, 16384, 1024);
       auto issue_s = [&](int x, int st) {
         const uint32_t d = tmem + x * 128;
+        const uint64_t a0 = dQ + static_cast<uint32_t>(x * (L::kTileBytes >> 4));
+        const uint64_t b0 = dK + static_cast<uint32_t>(st * (L::kTileBytes >> 4));
         #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint64_t a = dev::sdesc_sw128(sQ + x * L::kTileBytes + off, 16, 1024);
-          const uint64_t bd = dev::sdesc_sw128(sK + st * L::kTileBytes + off, 16, 1024);
-          dev::mma_ss(d, a, bd, idesc_s, kk > 0);
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          dev::mma_ss(d, a0 + off, b0 + off, idesc_s, kk > 0);
         }
       };
-      auto issue_pv = [&](int x, int st, bool acc) {
+      // PV over key rows [16*k0, 16*k1) of the tile
+      auto issue_pv = [&](int x, int st, bool acc, int k0, int k1) {
         const uint32_t d = tmem + 256 + x * D;
+        const uint64_t b0 = dV + static_cast<uint32_t>(st * (L::kTileBytes >> 4));
         #pragma unroll
-        for (int kk = 0; kk < kTileKV / 16; ++kk) {
-          const uint64_t bd = dev::sdesc_sw128(sV + st * L::kTileBytes + kk * 2048, 16384, 1024);
-          dev::mma_ts(d, tmem + x * 128 + kk * 8, bd, idesc_o, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = k0; kk < k1; ++kk)
+          dev::mma_ts(d, tmem + x * 128 + kk * 8, b0 + static_cast<uint32_t>(kk * (2048 >> 4)), idesc_o,
+                      (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = dev::mbar_wait(&bars[kQFull], 0, abort) && dev::mbar_wait(&bars[kKFull], 0, abort);
+      bool ok = dev::mbar_wait(&bars[L::kQFull], 0, abort) && dev::mbar_wait(&bars[L::kKFull], 0, abort);
       if (!ok) give_up(p, abort, 3);
       if (ok) {
         dev::tc_fence_after();
         issue_s(0, 0);
-        dev::mma_commit(&bars[kSFull + 0]);
+        dev::mma_commit(&bars[L::kSFull + 0]);
         issue_s(1, 0);
-        dev::mma_commit(&bars[kSFull + 1]);
-        dev::mma_commit(&bars[kKEmpty + 0]);
+        dev::mma_commit(&bars[L::kSFull + 1]);
+        dev::mma_commit(&bars[L::kKEmpty + 0]);
         for (int j = 0; j < n; ++j) {
-          const int st = j & 1;
-          const uint32_t use = j >> 1;
+          const int vst = j % VS;
+          const uint32_t vuse = j / VS;
           const bool more = j + 1 < n;
-          const int st1 = (j + 1) & 1;
-          const uint32_t use1 = (j + 1) >> 1;
-          if (!dev::mbar_wait(&bars[kVFull + st], use & 1, abort) ||
-              !dev::mbar_wait(&bars[kPFull + 0], j & 1, abort)) {
+          const int kst1 = (j + 1) % KS;
+          const uint32_t kuse1 = (j + 1) / KS;
+          if (!dev::mbar_wait(&bars[L::kVFull + vst], vuse & 1, abort) ||
+              !dev::mbar_wait(&bars[L::kPLo + 0], j & 1, abort)) {
             give_up(p, abort, 4);
             break;
           }
           dev::tc_fence_after();
-          issue_pv(0, st, j > 0);
+          issue_pv(0, vst, j > 0, 0, 4);
+          if (!dev::mbar_wait(&bars[L::kPHi + 0], j & 1, abort)) {
+            give_up(p, abort, 4);
+            break;
+          }
+          dev::tc_fence_after();
+          issue_pv(0, vst, j > 0, 4, 8);
           if (more) {
-            if (!dev::mbar_wait(&bars[kKFull + st1], use1 & 1, abort)) {
+            if (!dev::mbar_wait(&bars[L::kKFull + kst1], kuse1 & 1, abort)) {
               give_up(p, abort, 5);
               break;
             }
             dev::tc_fence_after();
-            issue_s(0, st1);
-            dev::mma_commit(&bars[kSFull + 0]);
+            issue_s(0, kst1);
+            dev::mma_commit(&bars[L::kSFull + 0]);
           }
-          if (!dev::mbar_wait(&bars[kPFull + 1], j & 1, abort)) {
+          if (!dev::mbar_wait(&bars[L::kPLo + 1], j & 1, abort)) {
             give_up(p, abort, 6);
             break;
           }
           dev::tc_fence_after();
-          issue_pv(1, st, j > 0);
-          dev::mma_commit(&bars[kVEmpty + st]);
+          issue_pv(1, vst, j > 0, 0, 4);
+          if (!dev::mbar_wait(&bars[L::kPHi + 1], j & 1, abort)) {
+            give_up(p, abort, 6);
+            break;
+          }
+          dev::tc_fence_after();
+          issue_pv(1, vst, j > 0, 4, 8);
+          dev::mma_commit(&bars[L::kVEmpty + vst]);
           if (more) {
-            issue_s(1, st1);
-            dev::mma_commit(&bars[kSFull + 1]);
-            dev::mma_commit(&bars[kKEmpty + st1]);
+            issue_s(1, kst1);
+            dev::mma_commit(&bars[L::kSFull + 1]);
+            dev::mma_commit(&bars[L::kKEmpty + kst1]);
           }
         }
-        dev::mma_commit(&bars[kODone + 0]);
-        dev::mma_commit(&bars[kODone + 1]);
+        dev::mma_commit(&bars[L::kODone + 0]);
+        dev::mma_commit(&bars[L::kODone + 1]);
       }
       // drain: all issued MMAs complete before TMEM is released
-      dev::mma_commit(&bars[kDrain]);
+      dev::mma_commit(&bars[L::kDrain]);
       volatile int never = 0;
-      dev::mbar_wait(&bars[kDrain], 0, &never);
+      dev::mbar_wait(&bars[L::kDrain], 0, &never);
     }
   } else {
+    dev::setmaxnreg_inc<kRegsHigh>();
     // ------------------------------------------------------------ softmax
-    const int x = (warp - 2) >> 2;
+    const int x = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -290,7 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < n; ++j) {
       int seg, row0, valid;
       tile_of(p, j, seg, row0, valid);
-      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[kSFull + x], j & 1, abort));
+      // one lane polls the barrier; the warp follows it
+      bool got = true;
+      if (lane == 0) got = dev::mbar_wait(&bars[L::kSFull + x], j & 1, abort);
+      ok = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
       if (!ok) {
         give_up(p, abort, 7);
         break;
@@ -309,15 +350,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kTileKV; ++c)
           if (c >= valid) s[c] = -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      // row max: a shallow tree of 3-input maxes (128 -> 43 -> 15 -> 5 -> 2 -> 1)
+      float t1[43];
       #pragma unroll
-      for (int c = 4; c < kTileKV; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
-      }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      for (int i = 0; i < 42; ++i) t1[i] = dev::fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+      t1[42] = fmaxf(s[126], s[127]);
+      float t2[15];
+      #pragma unroll
+      for (int i = 0; i < 14; ++i) t2[i] = dev::fmax3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
+      t2[14] = t1[42];
+      float t3[5];
+      #pragma unroll
+      for (int i = 0; i < 5; ++i) t3[i] = dev::fmax3(t2[3 * i], t2[3 * i + 1], t2[3 * i + 2]);
+      const float mx0 = dev::fmax3(t3[0], t3[1], t3[2]);
+      const float mx1 = fmaxf(t3[3], t3[4]);
+      const float mx = fmaxf(mx0, mx1) * sl2;
       const float m_new = fmaxf(m, mx);
       const bool need = m_new > m + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
@@ -344,19 +391,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[32];
         #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = dev::ex2_approx(fmaf(s[half * 64 + 2 * i], sl2, nm));
-          const float p1 = dev::ex2_approx(fmaf(s[half * 64 + 2 * i + 1], sl2, nm));
-          l0 += p0;
-          l1 += p1;
+          float y0, y1;
+          dev::ffma2(y0, y1, s[half * 64 + 2 * i], s[half * 64 + 2 * i + 1], sl2, nm);
+          const float p0 = dev::ex2_approx(y0);
+          const float p1 = dev::ex2_approx(y1);
+          dev::fadd2(l0, l1, p0, p1);
           pk[i] = dev::pack_bf16x2(p0, p1);
         }
         dev::tmem_st32(tS + half * 32, pk);
+        // publish this half: the PV product over its 64 keys may start
+        dev::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(&bars[(half == 0 ? L::kPLo : L::kPHi) + x]);
       }
       l += l0 + l1;
-      dev::tc_fence_before();
-      dev::mbar_arrive(&bars[kPFull + x]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[kODone + x], 0, abort));
+    if (ok) ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kODone + x], 0, abort));
     if (ok) {
       dev::tc_fence_after();
       const int q = q0 + x * 128 + row;
@@ -402,17 +452,27 @@ int make_token_map(CUtensorMap* m, const void* ptr, int B, int64_t N, int H, int
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int D>
+template <int D, int KS, int VS>
 int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, int n_segs,
                 float scale, void* o, float* lse, cudaStream_t stream) {
-  using L = Layout<D>;
+  using L = Layout<D, KS, VS>;
   static bool attr_done[64] = {false};
   int dev_id = 0;
   SAVGB_CUDA(cudaGetDevice(&dev_id));
   if (!attr_done[dev_id & 63]) {
-    SAVGB_CUDA(cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    SAVGB_CUDA(cudaFuncSetAttribute(attn_fwd_kernel<D, KS, VS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     L::kDynSmem));
     attr_done[dev_id & 63] = true;
+  }
+  static int regs_checked[64] = {0};
+  if (!regs_checked[dev_id & 63]) {
+    cudaFuncAttributes fa;
+    SAVGB_CUDA(cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, KS, VS>));
+    if (fa.numRegs * kThreads < kRegPoolNeeded)
+      return fail(SAVGB_ERR_UNSUPPORTED,
+                  "chunk_attention: kernel built with %d registers/thread; its register split needs %d",
+                  fa.numRegs, (kRegPoolNeeded + kThreads - 1) / kThreads);
+    regs_checked[dev_id & 63] = 1;
   }
   AttnMaps maps;
   int rc = make_token_map(&maps.q, q, B, n_q, H, D);
@@ -440,7 +500,7 @@ int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, i
   p.lse = lse;
   if ((rc = error_word(&p.err))) return rc;
   dim3 grid((unsigned)((n_q + kBlockQ - 1) / kBlockQ), (unsigned)H, (unsigned)B);
-  attn_fwd_kernel<D><<<grid, kThreads, L::kDynSmem, stream>>>(maps, p);
+  attn_fwd_kernel<D, KS, VS><<<grid, kThreads, L::kDynSmem, stream>>>(maps, p);
   SAVGB_CUDA(cudaGetLastError());
   return SAVGB_OK;
 }
@@ -471,8 +531,8 @@ int launch_attention(const void* q, int B, int64_t n_q, int H, int D, const Attn
                      int n_segs, float scale, void* o, float* lse, cudaStream_t stream) {
   int rc = check_device(nullptr);
   if (rc) return rc;
-  if (D == 64) return launch_impl<64>(q, B, n_q, H, segs, n_segs, scale, o, lse, stream);
-  return launch_impl<128>(q, B, n_q, H, segs, n_segs, scale, o, lse, stream);
+  if (D == 64) return launch_impl<64, kStagesK64, kStagesV64>(q, B, n_q, H, segs, n_segs, scale, o, lse, stream);
+  return launch_impl<128, kStagesK128, kStagesV128>(q, B, n_q, H, segs, n_segs, scale, o, lse, stream);
 }
 
 }  // namespace savgb

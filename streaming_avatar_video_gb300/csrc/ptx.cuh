@@ -216,12 +216,46 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 #undef SAVGB_R8
 #undef SAVGB_W8
 
+// Per-warpgroup register budget (all four warps of a warpgroup execute it).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ numerics
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Packed fp32 pairs (sm_100+): one instruction for two lanes of work.
+// (y0, y1) = (x0 * a + c0, x1 * a + c1)
+__device__ __forceinline__ void ffma2(float& y0, float& y1, float x0, float x1, float a, float c) {
+  asm("{\n\t.reg .b64 xs, as, cs, ys;\n\t"
+      "mov.b64 xs, {%2, %3};\n\tmov.b64 as, {%4, %4};\n\tmov.b64 cs, {%5, %5};\n\t"
+      "fma.rn.ftz.f32x2 ys, xs, as, cs;\n\tmov.b64 {%0, %1}, ys;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(a), "f"(c));
+}
+// (a0, a1) += (x0, x1)
+__device__ __forceinline__ void fadd2(float& a0, float& a1, float x0, float x1) {
+  asm("{\n\t.reg .b64 as, xs;\n\t"
+      "mov.b64 as, {%0, %1};\n\tmov.b64 xs, {%2, %3};\n\t"
+      "add.rn.ftz.f32x2 as, as, xs;\n\tmov.b64 {%0, %1}, as;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1));
+}
+// max of three
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` in the low half.
