@@ -40,6 +40,21 @@ if ROOT not in sys.path:
 from streaming_avatar_video_gb300 import inputs as I  # noqa: E402
 
 METRIC = "chunk-attention TFLOP/s (% of bf16 tensor peak); latent frames/s per denoise step"
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one attention
+# launch, from one ncu capture per workload, keyed by the sha256 of the kernel
+# source the capture was taken on; any later change of the source reports null.
+ATTN_TRAFFIC = {
+    # profiles/chunk_attention_base.md: 292.735 MB read + 67.092 MB written
+    "dacd1c68419cf4d48a6914ea861c498fc466286f53c10aa3d261cc0e8311dc67": {"base": 359827456},
+}
+
+
+def attn_traffic(workload: str):
+    import hashlib
+    path = os.path.join(ROOT, "streaming_avatar_video_gb300", "csrc", "attention.cu")
+    sha = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    return ATTN_TRAFFIC.get(sha, {}).get(workload)
 NOMINAL_BF16_TFLOPS = 2250.0
 
 
@@ -113,14 +128,19 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def dist_setup():
+def dist_setup(backend: str = "nccl"):
+    """Reads RANK / LOCAL_RANK / WORLD_SIZE (torchrun) and joins the process
+    group when there is more than one rank.  Returns (world, rank, local)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
     return world, rank, local
 
 
@@ -131,12 +151,20 @@ def barrier(world):
 
 
 def max_over_ranks(world, v: float) -> float:
+    """The largest of every rank's value (the slowest rank's time)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank: float, ms_max: float) -> float:
+    """Units per second of the whole job: every rank processes the same
+    number of units (weak scaling), the job ends with the slowest rank."""
+    return world * units_per_rank / (ms_max * 1e-3)
 
 
 # ------------------------------------------------------------------ our arm
@@ -213,8 +241,8 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
     clocks = clk.summary()
 
     attn_flops = w.attn_flops(True)
-    value = world * attn_flops / (ms_step * 1e-3) / 1e12
-    frames_per_s = world * w.B * w.F / (ms_step * 1e-3)
+    value = whole_job_rate(world, attn_flops, ms_step) / 1e12
+    frames_per_s = whole_job_rate(world, w.B * w.F, ms_step)
     attn_tflops = attn_flops / (attn_ms * 1e-3) / 1e12
     pk, pk_kind = peaks()
     peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
@@ -265,8 +293,10 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
             "peak_kind": f"{pk_kind} bf16 sustained (cuBLAS, timed inside a long loop)",
             "unit": "TFLOP/s",
             "frac": round(attn_tflops / peak, 4),
-            "traffic": None,
+            "traffic": attn_traffic(w.name),
+            "traffic_unit": "bytes per launch (ncu)",
             "algorithmic": f"4*B*H*Nq*Nkv*D = {attn_flops / 1e12:.4f} TFLOP per launch",
+            "min_bytes": 2 * w.B * w.hid * (2 * w.n_q + 2 * w.n_kv),
         },
         "gpu_launches": launches,
         "clocks": clocks,
@@ -312,7 +342,7 @@ def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world):
     ms = max_over_ranks(world, a.elapsed_time(b)) / n
     h2d = sum(t.numel() * t.element_size() for t in sets[0])
     d2h = x.numel() * x.element_size()
-    return {"value": round(world * w.attn_flops(True) / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    return {"value": round(whole_job_rate(world, w.attn_flops(True), ms) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "api": "ChunkStream.step (C ABI chunk_stream_step) with pinned host q/k/v in, x out"}
 
