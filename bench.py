@@ -347,6 +347,89 @@ def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world):
             "api": "ChunkStream.step (C ABI chunk_stream_step) with pinned host q/k/v in, x out"}
 
 
+def run_long(args, w: I.Workload, world: int, rank: int, local: int):
+    """Long streaming session: w.B sessions batched, args.chunks consecutive
+    chunks of w.steps denoising steps each, the boundary rolled every chunk.
+    Reports the attention throughput over the whole run, sustained latent
+    frames/s, nearest-rank p50/p99 of the per-chunk latency, and whether the
+    device's free memory stayed constant from chunk to chunk."""
+    import __graft_entry__ as g
+    g.build()
+    from streaming_avatar_video_gb300 import savgb as S
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    seed = 1 + rank
+    dts = S.flow_time_grid(w.steps, w.shift)
+    sets = []
+    for c in range(2):  # two resident input sets alternate between steps
+        st = I.step_inputs(w, seed, c, 0)
+        sets.append(tuple(t.to(dev) for t in (st.q, st.k, st.v)))
+    rk, rv = I.reference_kv(w, seed)
+    wo = I.out_proj_weight(w, seed).to(dev)
+    x = I.state_x(w, seed).to(dev)
+    cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                       w.rope_base)
+    cs.set_reference(rk.to(dev), rv.to(dev))
+    launches = [0]
+
+    def chunk(i0):
+        for s in range(w.steps):
+            q, k, v = sets[(i0 + s) & 1]
+            cs.step(q, k, v, wo, x, dts[s], s == w.steps - 1)
+            launches[0] += 3
+        launches[0] += 1 if w.boundary_frames else 0
+        cs.end_chunk()
+
+    for c in range(max(1, args.warmup // w.steps + 1)):  # warm-up chunks
+        chunk(0)
+    cs.sync()
+    n = args.chunks
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    free = []
+    launches[0] = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev[0].record(stream)
+        for c in range(n):
+            chunk(c * w.steps)
+            ev[c + 1].record(stream)
+            if c % 8 == 7:
+                free.append(torch.cuda.mem_get_info(dev)[0])  # synchronising query, outside the events
+        torch.cuda.synchronize()
+    barrier(world)
+    cs.sync()
+    per_chunk = sorted(ev[c].elapsed_time(ev[c + 1]) for c in range(n))
+    total_ms = max_over_ranks(world, ev[0].elapsed_time(ev[n]))
+    nearest = lambda q: per_chunk[max(0, math.ceil(q * len(per_chunk)) - 1)]
+    info = cs.info()
+    cs.close()
+    attn = w.attn_flops(True) * w.steps * n
+    return {
+        "metric": METRIC,
+        "value": round(whole_job_rate(world, attn, total_ms) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world, "steps": n * w.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / (n * w.steps), 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v/ref, W_o ~ N(0,1/hid), x ~ N(0,1))",
+        "config": {"workload": describe(w) + f", {n} consecutive chunks", "parallelism": f"replicas x{world}",
+                   "global_batch": world * w.B,
+                   "l2": "inputs larger than L2: two alternating input sets of "
+                         f"{3 * w.B * w.n_q * w.hid * 2 / 1e6:.0f} MB"},
+        "sustained_latent_frames_per_s": round(whole_job_rate(world, w.B * w.F * n, total_ms), 2),
+        "chunk_latency_ms": {"p50": round(nearest(0.50), 3), "p99": round(nearest(0.99), 3),
+                             "min": round(per_chunk[0], 3), "max": round(per_chunk[-1], 3)},
+        "memory": {"arena_bytes": info["arena_bytes"], "free_bytes_samples": len(free),
+                   "free_bytes_constant": len(set(free)) <= 1},
+        "gpu_launches": launches[0],
+        "clocks": clk.summary(),
+        "e2e": None, "cpu_baseline": None, "roofline": None,
+    }
+
+
 # ------------------------------------------------------------- oracle arm
 
 class OracleSample:
@@ -461,6 +544,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the oracle's timed sample")
+    ap.add_argument("--chunks", type=int, default=64, help="chunks of the long-session run (--config long)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -469,6 +553,11 @@ def main():
     if args.impl == "reference":
         res = run_reference(args, w, world, rank)
         if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if args.config == "long":
+        res = run_long(args, w, world, rank, local)
+        if rank == 0:
             print(json.dumps(res), flush=True)
         return
     res = run_ours(args, w, world, rank, local)
