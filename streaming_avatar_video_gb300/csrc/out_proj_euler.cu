@@ -8,14 +8,16 @@
 // trained with flow matching; section "The streaming framework and pipeline
 // loop": a multi-step diffusion pass per chunk).
 //
-// One CTA computes a 128 x BN tile of v with tcgen05.mma (bf16 operands in
-// 128-byte-swizzled shared memory fed by TMA through a 4-stage ring, fp32
-// accumulator in TMEM).  The epilogue reads the accumulator from TMEM and
-// applies the Euler update to x (fp32, read-modify-write) directly, so v
-// never goes through global memory.
-//   warp 0     TMA producer
-//   warp 1     TMEM allocation; lane 0 issues the MMAs
-//   warps 2-5  epilogue, one accumulator row (TMEM lane) per thread
+// One CTA computes a 256 x BN tile of v: two 128-row tcgen05.mma halves share
+// every B (W_o) tile, so each byte fed from L2 does twice the work of a
+// 128-row tile.  bf16 operands sit in 128-byte-swizzled shared memory fed by
+// TMA through a 3-stage ring; the fp32 accumulators live in TMEM.  The
+// epilogue reads them back, turns each 32 x 32 chunk around in shared memory
+// and applies the Euler update to x (fp32, read-modify-write) with coalesced
+// 128-byte row segments, so v never goes through global memory.
+//   warp 0      TMA producer
+//   warp 1      TMEM allocation; lane 0 issues the MMAs
+//   warps 4-11  epilogue (warps 2-3 idle)
 #include <cuda_bf16.h>
 
 #include "common.h"
@@ -24,10 +26,10 @@
 namespace savgb {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kBM = 128;
+constexpr int kThreads = 384;
+constexpr int kBM = 256;  // two 128-row MMA halves share every B tile
 constexpr int kBK = 64;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 
 struct WoParams {
   int M, N, K;
@@ -40,13 +42,16 @@ struct WoParams {
 
 template <int BN>
 struct WoLayout {
-  static constexpr int kABytes = kBM * kBK * 2;  // 16 KiB
-  static constexpr int kBBytes = BN * kBK * 2;   // 16 or 32 KiB
+  static constexpr int kAHalf = 128 * kBK * 2;  // 16 KiB
+  static constexpr int kABytes = 2 * kAHalf;
+  static constexpr int kBBytes = BN * kBK * 2;  // 16 or 32 KiB
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBar = kStages * kStageBytes;
   static constexpr int kMisc = kBar + (2 * kStages + 2) * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kDynSmem = kBytes + 1024;
+  static_assert(kDynSmem <= 227 * 1024, "shared memory budget");
+  static_assert(8 * 4096 <= kBar, "epilogue staging must fit in the ring");
 };
 
 __device__ __forceinline__ void give_up(const WoParams& p, volatile int* abort, unsigned code) {
@@ -89,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     dev::fence_barrier_init();
   }
   if (warp == 1) {
-    dev::tmem_alloc(tmem_slot, BN);
+    dev::tmem_alloc(tmem_slot, 2 * BN);
     dev::tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -112,10 +117,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         uint8_t* sa = smem + st * L::kStageBytes;
-        uint8_t* sb = sa + L::kABytes;
         dev::mbar_arrive_expect_tx(&full[st], L::kStageBytes);
         dev::tma_load_2d(sa, &map_a, &full[st], kb * kBK, m0);
-        dev::tma_load_2d(sb, &map_b, &full[st], kb * kBK, n0);
+        dev::tma_load_2d(sa + L::kAHalf, &map_a, &full[st], kb * kBK, m0 + 128);
+        dev::tma_load_2d(sa + L::kABytes, &map_b, &full[st], kb * kBK, n0);
         issued = kb + 1;
       }
       volatile int never = 0;
@@ -124,7 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = dev::idesc_bf16_f32(kBM, BN, false, false);
+      constexpr uint32_t idesc = dev::idesc_bf16_f32(128, BN, false, false);
+      const uint64_t d0 = dev::sdesc_sw128(dev::smem_u32(smem), 16, 1024);
       bool ok = true;
       for (int kb = 0; kb < kb_count; ++kb) {
         const int st = kb % kStages;
@@ -134,13 +140,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         dev::tc_fence_after();
-        const uint32_t sa = dev::smem_u32(smem + st * L::kStageBytes);
-        const uint32_t sb = sa + L::kABytes;
+        const uint64_t ds = d0 + static_cast<uint32_t>((st * L::kStageBytes) >> 4);
         #pragma unroll
         for (int k = 0; k < kBK / 16; ++k) {
-          const uint64_t ad = dev::sdesc_sw128(sa + k * 32, 16, 1024);
-          const uint64_t bd = dev::sdesc_sw128(sb + k * 32, 16, 1024);
-          dev::mma_ss(tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          const uint32_t koff = (k * 32) >> 4;
+          const uint64_t bd = ds + ((L::kABytes >> 4) + koff);
+          dev::mma_ss(tmem, ds + koff, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          dev::mma_ss(tmem + BN, ds + ((L::kAHalf >> 4) + koff), bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
         }
         dev::mma_commit(&empty[st]);
       }
@@ -149,42 +155,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int never = 0;
       dev::mbar_wait(drain, 0, &never);
     }
-  } else {
+  } else if (warp >= 4) {
+    // epilogue: warps 4-7 take rows 0-127 (accumulator columns [0, BN)),
+    // warps 8-11 rows 128-255 ([BN, 2 BN)).  Each 32-row x 32-column chunk is
+    // loaded from TMEM (one row per lane), turned around in shared memory and
+    // applied to x with 8 lanes per 128-byte row segment (coalesced).
+    const int half = (warp - 4) >> 2;
     const int quad = warp & 3;
-    const int row = quad * 32 + lane;
-    const int m = m0 + row;
-    const bool ok = __all_sync(0xffffffffu, dev::mbar_wait(acc_full, 0, abort));
+    const int row_base = m0 + half * 128 + quad * 32;
+    // while the MMAs run, pull this warp's 32 rows of x (BN columns) into L2
+    {
+      const int m = row_base + lane;
+      const int ncols = min(BN, p.N - n0);
+      if (m < p.M && ncols > 0) dev::prefetch_l2(p.x + static_cast<int64_t>(m) * p.N + n0, ncols * 4);
+    }
+    bool ok = true;
+    if (lane == 0) ok = dev::mbar_wait(acc_full, 0, abort);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     if (ok) {
       dev::tc_fence_after();
-      const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+      // the operand ring is idle once every MMA has completed: 4 KiB per warp
+      float4* stage = reinterpret_cast<float4*>(smem + (warp - 4) * 4096);
+      const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * BN;
       const float dt = p.dt;
+      const int seg = lane & 7;
       #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t acc[32];
         dev::tmem_ld32(t_row + c, acc);
-        const int nb = n0 + c;
-        if (m < p.M) {
-          float* xr = p.x + static_cast<int64_t>(m) * p.N + nb;
-          float* vr = p.v_out ? p.v_out + static_cast<int64_t>(m) * p.N + nb : nullptr;
-          #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            if (nb + i < p.N) {  // N % 16 == 0: a group of 4 is all in or all out
-              float4 v = make_float4(__uint_as_float(acc[i]), __uint_as_float(acc[i + 1]),
-                                     __uint_as_float(acc[i + 2]), __uint_as_float(acc[i + 3]));
-              if (p.bias) {
-                const float4 bb = *reinterpret_cast<const float4*>(p.bias + nb + i);
-                v.x += bb.x; v.y += bb.y; v.z += bb.z; v.w += bb.w;
-              }
-              float4 xv = *reinterpret_cast<float4*>(xr + i);
-              xv.x = fmaf(dt, v.x, xv.x);
-              xv.y = fmaf(dt, v.y, xv.y);
-              xv.z = fmaf(dt, v.z, xv.z);
-              xv.w = fmaf(dt, v.w, xv.w);
-              *reinterpret_cast<float4*>(xr + i) = xv;
-              if (vr) *reinterpret_cast<float4*>(vr + i) = v;
-            }
+        #pragma unroll
+        for (int j = 0; j < 8; ++j)
+          stage[lane * 8 + ((j + lane) & 7)] =
+              make_float4(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]),
+                          __uint_as_float(acc[4 * j + 2]), __uint_as_float(acc[4 * j + 3]));
+        __syncwarp();
+        const int n = n0 + c + 4 * seg;
+        float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.bias && n < p.N) bb = *reinterpret_cast<const float4*>(p.bias + n);
+        // all eight loads of x first (the stores below could alias them as far
+        // as the compiler knows), then the updates
+        float4 xv[8];
+        float4 v[8];
+        #pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int r = 4 * k + (lane >> 3);
+          const int m = row_base + r;
+          v[k] = stage[r * 8 + ((seg + r) & 7)];
+          if (m < p.M && n < p.N)  // N % 16 == 0: a group of 4 columns is all in or all out
+            xv[k] = *reinterpret_cast<const float4*>(p.x + static_cast<int64_t>(m) * p.N + n);
+        }
+        #pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int m = row_base + 4 * k + (lane >> 3);
+          if (m < p.M && n < p.N) {
+            float4 u = v[k];
+            u.x += bb.x; u.y += bb.y; u.z += bb.z; u.w += bb.w;
+            float4 y = xv[k];
+            y.x = fmaf(dt, u.x, y.x);
+            y.y = fmaf(dt, u.y, y.y);
+            y.z = fmaf(dt, u.z, y.z);
+            y.w = fmaf(dt, u.w, y.w);
+            *reinterpret_cast<float4*>(p.x + static_cast<int64_t>(m) * p.N + n) = y;
+            if (p.v_out) *reinterpret_cast<float4*>(p.v_out + static_cast<int64_t>(m) * p.N + n) = u;
           }
         }
+        __syncwarp();
       }
     } else {
       give_up(p, abort, 3);
@@ -195,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     dev::tc_fence_after();
-    dev::tmem_dealloc(tmem, BN);
+    dev::tmem_dealloc(tmem, 2 * BN);
   }
 }
 
@@ -214,7 +249,7 @@ int launch_bn(const void* o, const void* w, const float* bias, float* x, int64_t
   CUtensorMap ma, mb;
   const uint64_t da[2] = {(uint64_t)K, (uint64_t)M};
   const uint64_t sa[1] = {(uint64_t)K * 2};
-  const uint32_t ba[2] = {kBK, kBM};
+  const uint32_t ba[2] = {kBK, 128};
   int rc = encode_tiled(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o, da, sa, ba, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
   const uint64_t db[2] = {(uint64_t)K, (uint64_t)N};
