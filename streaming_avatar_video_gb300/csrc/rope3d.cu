@@ -7,8 +7,9 @@
 //
 // HBM-bound: each element is read once and written once.  Each block first
 // builds the cos/sin tables of the three axes in shared memory (fp32, from
-// sincosf), then streams 16-byte vectors (8 channels = 4 pairs of one token
-// and head) with four independent vectors in flight per thread.
+// sincosf); then a warp takes one token at a time, decodes its (t, h, w)
+// once and streams its 16-byte vectors (8 channels = 4 pairs of one head),
+// eight per lane in flight.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -18,8 +19,9 @@
 namespace savgb {
 namespace {
 
-constexpr int kRopeThreads = 512;
-constexpr int kRopeUnroll = 4;
+constexpr int kRopeThreads = 256;  // 8 warps; a warp rotates one token at a time
+constexpr int kRopeWarps = kRopeThreads / 32;
+constexpr int kRopeBatch = 8;      // 16-byte vectors of a token in flight per lane
 constexpr int kRopeMaxTableBytes = 96 * 1024;
 
 struct RopeTensor {
@@ -31,12 +33,10 @@ struct RopeTensor {
 
 struct RopeKernelArgs {
   RopeTensor t[2];
-  int n_tensors;
-  int B, n_tokens, vec_per_tok, vec_per_head;  // vec_per_head = D/8
+  int n_tokens, vec_per_tok, vec_per_head;  // vec_per_head = D/8
   int gh, gw, gt, t0;
   int p_t, p_h, p_w;
   float log2_base;
-  int total;  // B * n_tokens * vec_per_tok
 };
 
 __device__ __forceinline__ void rotate_pair(uint32_t& packed, float2 cs) {
@@ -49,6 +49,10 @@ __device__ __forceinline__ void rotate_pair(uint32_t& packed, float2 cs) {
   packed = *reinterpret_cast<uint32_t*>(&r);
 }
 
+// grid: (token groups, B, tensors).  Each block builds the cos/sin tables of
+// the three axes in shared memory, then each warp takes whole tokens: the
+// token's (t, h, w) is decoded once and its H*D/8 vectors are streamed with
+// kRopeBatch loads in flight per lane.
 __global__ void __launch_bounds__(kRopeThreads) rope3d_kernel(const RopeKernelArgs a) {
   extern __shared__ float2 tab[];
   float2* tab_t = tab;
@@ -71,52 +75,43 @@ __global__ void __launch_bounds__(kRopeThreads) rope3d_kernel(const RopeKernelAr
   }
   __syncthreads();
 
+  const int ti = blockIdx.z;
+  const int b = blockIdx.y;
+  const uint4* __restrict__ in = (ti == 0 ? a.t[0].in : a.t[1].in) + b * (ti == 0 ? a.t[0].in_bs : a.t[1].in_bs);
+  uint4* __restrict__ out = (ti == 0 ? a.t[0].out : a.t[1].out) + b * (ti == 0 ? a.t[0].out_bs : a.t[1].out_bs);
+  const int lane = threadIdx.x & 31;
   const int hw = a.gh * a.gw;
-  const int stride = gridDim.x * blockDim.x;
-  for (int ti = 0; ti < a.n_tensors; ++ti) {
-    const uint4* __restrict__ in = ti == 0 ? a.t[0].in : a.t[1].in;
-    uint4* __restrict__ out = ti == 0 ? a.t[0].out : a.t[1].out;
-    const int64_t in_bs = ti == 0 ? a.t[0].in_bs : a.t[1].in_bs;
-    const int64_t out_bs = ti == 0 ? a.t[0].out_bs : a.t[1].out_bs;
-    for (int base = blockIdx.x * blockDim.x + threadIdx.x; base < a.total;
-         base += stride * kRopeUnroll) {
-      uint4 v[kRopeUnroll];
+  const int vpt = a.vec_per_tok;
+  const int ph_end = a.p_t + a.p_h;
+  for (int n = blockIdx.x * kRopeWarps + (threadIdx.x >> 5); n < a.n_tokens; n += gridDim.x * kRopeWarps) {
+    const int tt = n / hw;
+    const int r2 = n - tt * hw;
+    const int hh = r2 / a.gw;
+    const int ww = r2 - hh * a.gw;
+    const float2* tr = tab_t + tt * a.p_t;
+    const float2* hr = tab_h + hh * a.p_h - a.p_t;
+    const float2* wr = tab_w + ww * a.p_w - ph_end;
+    const uint4* src = in + static_cast<int64_t>(n) * vpt;
+    uint4* dst = out + static_cast<int64_t>(n) * vpt;
+    for (int j0 = 0; j0 < vpt; j0 += 32 * kRopeBatch) {
+      uint4 v[kRopeBatch];
       #pragma unroll
-      for (int u = 0; u < kRopeUnroll; ++u) {
-        const int idx = base + u * stride;
-        if (idx < a.total) {
-          const int tok = idx / a.vec_per_tok;
-          const int rem = idx - tok * a.vec_per_tok;
-          const int b = tok / a.n_tokens;
-          const int n = tok - b * a.n_tokens;
-          v[u] = __ldcs(in + (int64_t)b * in_bs + (int64_t)n * a.vec_per_tok + rem);
-        }
+      for (int u = 0; u < kRopeBatch; ++u) {
+        const int j = j0 + lane + 32 * u;
+        if (j < vpt) v[u] = __ldcs(src + j);
       }
       #pragma unroll
-      for (int u = 0; u < kRopeUnroll; ++u) {
-        const int idx = base + u * stride;
-        if (idx < a.total) {
-          const int tok = idx / a.vec_per_tok;
-          const int rem = idx - tok * a.vec_per_tok;
-          const int b = tok / a.n_tokens;
-          const int n = tok - b * a.n_tokens;
-          const int tt = n / hw;
-          const int r2 = n - tt * hw;
-          const int hh = r2 / a.gw;
-          const int ww = r2 - hh * a.gw;
-          const int p0 = (rem % a.vec_per_head) * 4;
+      for (int u = 0; u < kRopeBatch; ++u) {
+        const int j = j0 + lane + 32 * u;
+        if (j < vpt) {
+          const int p0 = (j % a.vec_per_head) * 4;
           uint32_t w0 = v[u].x, w1 = v[u].y, w2 = v[u].z, w3 = v[u].w;
-          const float2* tr = tab_t + tt * a.p_t;
-          const float2* hr = tab_h + hh * a.p_h - a.p_t;
-          const float2* wr = tab_w + ww * a.p_w - a.p_t - a.p_h;
-          const int ph_end = a.p_t + a.p_h;
           #define SAVGB_ROT(W, Q) { const int p_ = p0 + (Q); \
             const float2 cs_ = p_ < a.p_t ? tr[p_] : (p_ < ph_end ? hr[p_] : wr[p_]); \
             rotate_pair(W, cs_); }
           SAVGB_ROT(w0, 0) SAVGB_ROT(w1, 1) SAVGB_ROT(w2, 2) SAVGB_ROT(w3, 3)
           #undef SAVGB_ROT
-          __stcs(out + (int64_t)b * out_bs + (int64_t)n * a.vec_per_tok + rem,
-                 make_uint4(w0, w1, w2, w3));
+          __stcs(dst + j, make_uint4(w0, w1, w2, w3));
         }
       }
     }
@@ -141,7 +136,7 @@ size_t table_bytes(const RopeArgs& a) {
 int validate_rope(const RopeArgs& a) {
   if (!a.in || !a.out) return fail(SAVGB_ERR_INVALID_ARG, "rope3d: null pointer");
   if (!aligned16(a.in) || !aligned16(a.out)) return fail(SAVGB_ERR_ALIGNMENT, "rope3d: pointers must be 16-byte aligned");
-  if (a.B < 1 || a.H < 1 || a.n_tokens < 1) return fail(SAVGB_ERR_INVALID_ARG, "rope3d: B, H, n_tokens must be >= 1");
+  if (a.B < 1 || a.B > 65535 || a.H < 1 || a.n_tokens < 1) return fail(SAVGB_ERR_INVALID_ARG, "rope3d: B must be in [1, 65535], H and n_tokens >= 1");
   if (a.D < 8 || a.D > 256 || a.D % 8) return fail(SAVGB_ERR_INVALID_ARG, "rope3d: D must be a multiple of 8 in [8, 256]");
   if (a.grid_t < 1 || a.grid_h < 1 || a.grid_w < 1 || a.grid_t > 4096 || a.grid_h > 4096 ||
       a.grid_w > 4096)
@@ -164,21 +159,18 @@ static int launch_rope_multi(const RopeArgs* args, int n, cudaStream_t stream) {
   if (rc) return rc;
   const RopeArgs& a = args[0];
   RopeKernelArgs k{};
-  k.n_tensors = n;
   for (int i = 0; i < n; ++i) {
     k.t[i].in = static_cast<const uint4*>(args[i].in);
     k.t[i].out = static_cast<uint4*>(args[i].out);
     k.t[i].in_bs = args[i].in_batch_stride / 8;
     k.t[i].out_bs = args[i].out_batch_stride / 8;
   }
-  k.B = a.B;
   k.n_tokens = (int)a.n_tokens;
   k.vec_per_tok = a.H * a.D / 8;
   k.vec_per_head = a.D / 8;
   k.gt = a.grid_t; k.gh = a.grid_h; k.gw = a.grid_w; k.t0 = a.t0;
   axis_split(a.D, &k.p_t, &k.p_h, &k.p_w);
   k.log2_base = (float)std::log2(a.base);
-  k.total = (int)((int64_t)a.B * a.n_tokens * k.vec_per_tok);
   const size_t smem = table_bytes(a);
   static bool attr_done[64] = {false};
   int dev_id = 0;
@@ -188,8 +180,14 @@ static int launch_rope_multi(const RopeArgs* args, int n, cudaStream_t stream) {
                                     kRopeMaxTableBytes));
     attr_done[dev_id & 63] = true;
   }
-  const int need = (k.total + kRopeThreads * kRopeUnroll - 1) / (kRopeThreads * kRopeUnroll);
-  const int grid = need < 2 * sms ? (need > 0 ? need : 1) : 2 * sms;
+  // one wave: as many blocks as fit on the device at once, over all (batch, tensor) pairs
+  int occ = 0;
+  SAVGB_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rope3d_kernel, kRopeThreads, smem));
+  if (occ < 1) occ = 1;
+  const int groups = (k.n_tokens + kRopeWarps - 1) / kRopeWarps;
+  int per = occ * sms / (a.B * n);
+  if (per < 1) per = 1;
+  dim3 grid((unsigned)(groups < per ? groups : per), (unsigned)a.B, (unsigned)n);
   rope3d_kernel<<<grid, kRopeThreads, smem, stream>>>(k);
   SAVGB_CUDA(cudaGetLastError());
   return SAVGB_OK;
