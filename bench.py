@@ -1,6 +1,6 @@
 """Benchmark of the chunk denoising step on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config base|sr|long|small]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config base|sr|sr1|long|small]
                     [--impl ours|reference]
 
 One step is one pass of the whole hot path through the library's public API
@@ -539,7 +539,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=600)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="base", choices=["base", "sr", "long", "small", "tiny"])
+    ap.add_argument("--config", default="base", choices=["base", "sr", "sr1", "long", "small", "tiny"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

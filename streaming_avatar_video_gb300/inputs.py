@@ -95,6 +95,9 @@ WORKLOADS = {
     # SR-shaped chunk: 24 heads of 128, 8x60x104 chunk, 2-frame boundary, 8 uniform steps
     "sr": Workload("sr", B=1, H=24, D=128, F=8, grid_h=60, grid_w=104, ref_frames=1,
                    boundary_frames=2, steps=8, shift=1.0),
+    # SR-shaped chunk refined in a single step (dt = 1)
+    "sr1": Workload("sr1", B=1, H=24, D=128, F=8, grid_h=60, grid_w=104, ref_frames=1,
+                    boundary_frames=2, steps=1, shift=1.0),
     # long session: 4 sessions batched, 64 base-shaped chunks each
     "long": Workload("long", B=4, H=24, D=128, F=8, grid_h=30, grid_w=52, ref_frames=1,
                      boundary_frames=2, steps=30, shift=3.0, chunks=64),

@@ -332,3 +332,41 @@ def test_watchdog_timeout_is_reported(S):
     S.savgb_device_check()  # cleared
     x = torch.ones(4, device="cuda")
     assert float((x * 2).sum()) == 8.0
+
+
+@pytest.mark.parametrize("name", ["base", "sr1"])
+def test_stream_step_full_size_sampled_rows(S, name):
+    """Two one-step chunks of a full-size workload through chunk_stream_step:
+    chunk 1 attends over the boundary rolled from chunk 0.  Sampled rows of
+    chunk 1's x against the oracle (every key, every head)."""
+    w = I.WORKLOADS[name]
+    seed = 5
+    rk, rv = I.reference_kv(w, seed)
+    wo = I.out_proj_weight(w, seed)
+    dt = 1.0 if w.steps == 1 else S.flow_time_grid(w.steps, w.shift)[0]
+    cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                       w.rope_base)
+    cs.set_reference(rk.cuda(), rv.cuda())
+    st0 = I.step_inputs(w, seed, 0, 0)
+    x_scratch = torch.zeros((w.B * w.n_q, w.hid), dtype=torch.float32, device="cuda")
+    cs.step(st0.q.cuda(), st0.k.cuda(), st0.v.cuda(), wo.cuda(), x_scratch, dt, True)
+    cs.end_chunk()
+    del x_scratch
+    st1 = I.step_inputs(w, seed, 1, 0)
+    x0 = torch.from_numpy(I.normal_f32((w.B * w.n_q, w.hid), 1.0, seed, I.KIND_X, 1))
+    x = x0.cuda()
+    cs.step(st1.q.cuda(), st1.k.cuda(), st1.v.cuda(), wo.cuda(), x, dt, False)
+    cs.sync()
+    got = x.cpu()
+    cs.close()
+    # oracle on sampled rows: rotations of the full chunk, attention for the sampled queries only
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([rng.choice(w.n_q, 24, replace=False), [0, 255, 256, w.n_q - 1]]))
+    rk_rot = O.rope3d(f64(rk), w.ref_frames, w.grid_h, w.grid_w, w.ref_t, w.rope_base)
+    bk_rot, bv = O.boundary_from_chunk(f64(st0.k), f64(st0.v), w.frame_tokens, w.boundary_frames, w.grid_h,
+                                       w.grid_w, w.rope_base)
+    q_rot = O.rope3d(f64(st1.q), w.F, w.grid_h, w.grid_w, 0, w.rope_base)[:, rows]
+    k_rot = O.rope3d(f64(st1.k), w.F, w.grid_h, w.grid_w, 0, w.rope_base)
+    o = O.attention(q_rot, [(rk_rot, f64(rv)), (bk_rot, bv), (k_rot, f64(st1.v))])
+    want = O.euler_update(f64(x0)[rows], O.out_proj(o.reshape(len(rows), w.hid), f64(wo)), dt)
+    assert_close(f64(got)[rows], want, what=f"{name} step x (sampled rows)")
