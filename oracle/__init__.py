@@ -16,6 +16,10 @@ What it computes follows HeyGen, "Avatar inference at scale":
   is encoded once per request; the audio-to-video stage runs a multi-step
   diffusion pass per chunk, conditioned on the previous chunk's boundary
   frames.
+* section "Boundary continuity and chunk consistency": interpolation (I)
+  chunks between consecutive N chunks, generated after both, anchored on the
+  previous chunk's last frame and the next chunk's first frame, anchor
+  predictions discarded.
 * section "Constant memory over duration": only the static reference
   conditioning and a minimal set of carried tensors survive from chunk to
   chunk.
@@ -43,4 +47,7 @@ from .step import (  # noqa: F401
     boundary_from_chunk,
     chunk_step,
     run_stream,
+    anchors_from_chunk,
+    ichunk_step,
+    run_stream_ni,
 )

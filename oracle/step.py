@@ -212,3 +212,90 @@ def run_stream(w, ref_k, ref_v, w_o, x0_per_chunk, step_inputs_fn, dts, scale=No
             bnd = boundary_from_chunk(last[0], last[1], w.frame_tokens, w.boundary_frames,
                                       w.grid_h, w.grid_w, w.rope_base)
     return xs, bnds
+
+
+# --------------------------------------------------------------------------
+# interpolation (I) chunks between consecutive N chunks
+# --------------------------------------------------------------------------
+
+def anchors_from_chunk(k_chunk: np.ndarray, v_chunk: np.ndarray, frame_tokens: int):
+    """The two frames of a finished N chunk that serve as anchors (before
+    RoPE, taken from its final denoising step): (first frame k, v) and (last
+    frame k, v).
+
+    Reading of "Boundary continuity and chunk consistency": an I chunk uses
+    the last frame of the previous N chunk and an early frame of the next one;
+    the early frame taken here is the first."""
+    N = k_chunk.shape[1]
+    first = (k_chunk[:, :frame_tokens].copy(), v_chunk[:, :frame_tokens].copy())
+    last = (k_chunk[:, N - frame_tokens:].copy(), v_chunk[:, N - frame_tokens:].copy())
+    return first, last
+
+
+def ichunk_step(q, k, v, ref_k_rot, ref_v, anchor_prev, anchor_next, w_o, x, dt, grid, base=10000.0,
+                scale=None, bias=None):
+    """One denoising step of an interpolation chunk of F latent frames whose
+    first and last frames are anchors.
+
+    Reading of "Boundary continuity and chunk consistency": the I chunk is
+    generated only after the N chunks on both sides are finished; the anchor
+    frames carry the motion on either side and their own predictions are
+    discarded, so the queries are the F-2 interior frames only.
+      q, k, v      interior tokens [B][(F-2)*h*w][H][D] before RoPE (t = 1..F-2)
+      anchor_prev  (k, v) of the previous N chunk's last frame, before RoPE (t = 0)
+      anchor_next  (k, v) of the next N chunk's first frame, before RoPE (t = F-1)
+    Keys and values: [reference | anchors | interior].  grid = (F, h, w).
+    Returns (x_next, O) for the interior rows."""
+    F, gh, gw = grid
+    q_rot = rope3d(q, F - 2, gh, gw, 1, base)
+    k_rot = rope3d(k, F - 2, gh, gw, 1, base)
+    a_prev = rope3d(anchor_prev[0], 1, gh, gw, 0, base)
+    a_next = rope3d(anchor_next[0], 1, gh, gw, F - 1, base)
+    anchors_k = np.concatenate([a_prev, a_next], axis=1)
+    anchors_v = np.concatenate([anchor_prev[1], anchor_next[1]], axis=1)
+    o = attention(q_rot, [(ref_k_rot, ref_v), (anchors_k, anchors_v), (k_rot, v)], scale)
+    B, Nq, H, D = o.shape
+    vel = out_proj(o.reshape(B * Nq, H * D), w_o, bias)
+    return euler_update(x, vel, dt), o
+
+
+def run_stream_ni(w, ref_k, ref_v, w_o, x0_n, x0_i, n_inputs, i_inputs, dts, idts, n_chunks,
+                  scale=None, bias=None):
+    """N and I chunks in the order N0, N1, I0, N2, I1, ..., N_{n-1}, I_{n-2}.
+
+    n_inputs(c, s) -> (q, k, v) of N chunk c at step s; i_inputs(c, s) -> the
+    interior (q, k, v) of I chunk c; x0_n(c), x0_i(c) -> initial states.
+    Returns (x of every N chunk, x of every I chunk, anchors used by every I
+    chunk as (prev, next))."""
+    ref_k_rot = rope3d(ref_k, w.ref_frames, w.grid_h, w.grid_w, w.ref_t - w.ref_frames + 1, w.rope_base)
+    empty = np.zeros((w.B, 0, w.H, w.D))
+    bnd = (empty, empty)
+    xs_n, xs_i, used = [], [], []
+    anchors = {}  # N chunk index -> (first frame, last frame) of its final step
+
+    def run_i(c):
+        x = x0_i(c)
+        a_prev, a_next = anchors[c][1], anchors[c + 1][0]
+        for s, dt in enumerate(idts):
+            q, k, v = i_inputs(c, s)
+            x, _ = ichunk_step(q, k, v, ref_k_rot, ref_v, a_prev, a_next, w_o, x, dt,
+                               (w.F, w.grid_h, w.grid_w), w.rope_base, scale, bias)
+        xs_i.append(x)
+        used.append((a_prev, a_next))
+
+    for c in range(n_chunks):
+        x = x0_n(c)
+        last = None
+        for s, dt in enumerate(dts):
+            q, k, v = n_inputs(c, s)
+            x, _ = chunk_step(q, k, v, ref_k_rot, ref_v, bnd[0], bnd[1], w_o, x, dt,
+                              (w.F, w.grid_h, w.grid_w), w.rope_base, scale, bias)
+            last = (k, v)
+        xs_n.append(x)
+        anchors[c] = anchors_from_chunk(last[0], last[1], w.frame_tokens)
+        if w.boundary_frames > 0:
+            bnd = boundary_from_chunk(last[0], last[1], w.frame_tokens, w.boundary_frames,
+                                      w.grid_h, w.grid_w, w.rope_base)
+        if c >= 1:
+            run_i(c - 1)
+    return xs_n, xs_i, used

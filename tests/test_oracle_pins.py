@@ -412,3 +412,103 @@ def test_planted_time_grid_off_by_one():
         warped = shift * sigma / (1.0 + (shift - 1.0) * sigma)
         return warped[:-1] - warped[1:]
     _expect_pin_failure(pin_time_grid, bad)
+
+
+# ------------------------------------------------- interpolation chunks ----
+
+def _i_case(seed=11, F=4, gh=2, gw=3, H=2, D=64):
+    rng = np.random.default_rng(seed)
+    ft = gh * gw
+    n_int = (F - 2) * ft
+    q, k, v = (rng.standard_normal((1, n_int, H, D)) for _ in range(3))
+    ap = (rng.standard_normal((1, ft, H, D)), rng.standard_normal((1, ft, H, D)))
+    an = (rng.standard_normal((1, ft, H, D)), rng.standard_normal((1, ft, H, D)))
+    rk, rv = rng.standard_normal((1, ft, H, D)), rng.standard_normal((1, ft, H, D))
+    w = rng.standard_normal((H * D, H * D)) / math.sqrt(H * D)
+    x = rng.standard_normal((n_int, H * D))
+    return dict(q=q, k=k, v=v, ap=ap, an=an, rk=rk, rv=rv, w=w, x=x, F=F, gh=gh, gw=gw, H=H, D=D)
+
+
+def pin_ichunk_brute(ichunk=O.ichunk_step):
+    """Literal loops: interior frames at t = 1..F-2, anchors at t = 0 and F-1."""
+    c = _i_case()
+    base, dt, F, gh, gw, D = 10000.0, 0.5, c["F"], c["gh"], c["gw"], c["D"]
+    rk_rot = O.rope3d(c["rk"], 1, gh, gw, -1, base)
+    x1, o = ichunk(c["q"], c["k"], c["v"], rk_rot, c["rv"], c["ap"], c["an"], c["w"], c["x"], dt, (F, gh, gw), base)
+    qr = _brute.rope_block(c["q"], F - 2, gh, gw, 1, base)[0]
+    keys = (_brute.rope_block(c["rk"], 1, gh, gw, -1, base)[0]
+            + _brute.rope_block(c["ap"][0], 1, gh, gw, 0, base)[0]
+            + _brute.rope_block(c["k"], F - 2, gh, gw, 1, base)[0]
+            + _brute.rope_block(c["an"][0], 1, gh, gw, F - 1, base)[0])
+    lst = lambda a: [[list(h) for h in tok] for tok in a[0]]
+    vals = lst(c["rv"]) + lst(c["ap"][1]) + lst(c["v"]) + lst(c["an"][1])
+    ob = _brute.attend(qr, keys, vals, 1.0 / math.sqrt(D))
+    assert np.allclose(o[0], np.array(ob), atol=1e-12)
+    flat = [[e for head in tok for e in head] for tok in ob]
+    assert np.allclose(x1, c["x"] + dt * np.array(_brute.linear(flat, c["w"].tolist())), atol=1e-12)
+
+
+def test_ichunk_equals_brute_force():
+    pin_ichunk_brute()
+
+
+def test_ichunk_relative_time():
+    """Shifting the whole I chunk's time by one frame (anchors at -1 and F-2,
+    interior from 0) changes nothing: its attention equals an N-style step
+    whose two context frames sit at those times."""
+    c = _i_case(seed=3)
+    F, gh, gw = c["F"], c["gh"], c["gw"]
+    empty = np.zeros((1, 0, c["H"], c["D"]))
+    x1, o = O.ichunk_step(c["q"], c["k"], c["v"], empty, empty, c["ap"], c["an"], c["w"], c["x"], 0.5, (F, gh, gw))
+    q_rot = O.rope3d(c["q"], F - 2, gh, gw, 0)
+    k_rot = O.rope3d(c["k"], F - 2, gh, gw, 0)
+    a0 = O.rope3d(c["ap"][0], 1, gh, gw, -1)
+    a1 = O.rope3d(c["an"][0], 1, gh, gw, F - 2)
+    o2 = O.attention(q_rot, [(a0, c["ap"][1]), (k_rot, c["v"]), (a1, c["an"][1])])
+    assert np.allclose(o, o2, atol=1e-12)
+
+
+def test_stream_ni_schedule_and_anchors():
+    """I_k runs after N_{k+1}; its anchors are N_k's last frame and N_{k+1}'s
+    first frame, both from their final steps."""
+    from streaming_avatar_video_gb300.inputs import Workload
+    w = Workload("ni", B=1, H=2, D=64, F=4, grid_h=2, grid_w=2, ref_frames=1, boundary_frames=1,
+                 steps=2, shift=1.0)
+    rng = np.random.default_rng(9)
+    shp = (1, w.n_q, w.H, w.D)
+    ishp = (1, (w.F - 2) * w.frame_tokens, w.H, w.D)
+    n_in = {(c, s): tuple(rng.standard_normal(shp) for _ in range(3)) for c in range(3) for s in range(2)}
+    i_in = {(c, s): tuple(rng.standard_normal(ishp) for _ in range(3)) for c in range(2) for s in range(2)}
+    rk, rv = rng.standard_normal((1, w.n_ref, w.H, w.D)), rng.standard_normal((1, w.n_ref, w.H, w.D))
+    wo = rng.standard_normal((w.hid, w.hid)) / 8
+    xs_n, xs_i, used = O.run_stream_ni(
+        w, rk, rv, wo, lambda c: np.zeros((w.n_q, w.hid)), lambda c: np.zeros((ishp[1], w.hid)),
+        lambda c, s: n_in[(c, s)], lambda c, s: i_in[(c, s)], O.time_grid(2), O.time_grid(2), 3)
+    assert len(xs_n) == 3 and len(xs_i) == 2
+    ft = w.frame_tokens
+    for k in range(2):
+        a_prev, a_next = used[k]
+        assert np.array_equal(a_prev[0], n_in[(k, 1)][1][:, w.n_q - ft:])
+        assert np.array_equal(a_prev[1], n_in[(k, 1)][2][:, w.n_q - ft:])
+        assert np.array_equal(a_next[0], n_in[(k + 1, 1)][1][:, :ft])
+        assert np.array_equal(a_next[1], n_in[(k + 1, 1)][2][:, :ft])
+    # the N chunks are unaffected by the I chunks: same as the plain stream
+    xs_plain, _ = O.run_stream(w, rk, rv, wo, lambda c: np.zeros((w.n_q, w.hid)), lambda c, s: n_in[(c, s)],
+                               O.time_grid(2), chunks=3)
+    for c in range(3):
+        assert np.allclose(xs_n[c], xs_plain[c], atol=0)
+
+
+def test_planted_ichunk_anchor_times():
+    # both anchors rotated to t = 0: the literal-loop pin must fail
+    _expect_pin_failure(pin_ichunk_brute, _bad_ichunk)
+
+
+def _bad_ichunk(q, k, v, rk, rv, ap, an, w_o, x, dt, grid, base=10000.0, scale=None, bias=None):
+    F, gh, gw = grid
+    q_rot = O.rope3d(q, F - 2, gh, gw, 1, base)
+    k_rot = O.rope3d(k, F - 2, gh, gw, 1, base)
+    a = np.concatenate([O.rope3d(ap[0], 1, gh, gw, 0, base), O.rope3d(an[0], 1, gh, gw, 0, base)], axis=1)
+    o = O.attention(q_rot, [(rk, rv), (a, np.concatenate([ap[1], an[1]], axis=1)), (k_rot, v)])
+    B, Nq, H, D = o.shape
+    return O.euler_update(x, O.out_proj(o.reshape(B * Nq, H * D), w_o), dt), o
