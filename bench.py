@@ -430,6 +430,72 @@ def run_long(args, w: I.Workload, world: int, rank: int, local: int):
     }
 
 
+def run_interp(args, w: I.Workload, world: int, rank: int, local: int):
+    """Interpolation-chunk steps of a base-shaped stream: N0 and N1 are run
+    first, then K timed steps of the pending I chunk (its F-2 interior frames
+    attend over [reference | two anchor frames | interior])."""
+    import __graft_entry__ as g
+    g.build()
+    from streaming_avatar_video_gb300 import savgb as S
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    seed = 1 + rank
+    dts = S.flow_time_grid(w.steps, w.shift)
+    st = I.step_inputs(w, seed, 0, 0)
+    q, k, v = (t.to(dev) for t in (st.q, st.k, st.v))
+    rk, rv = I.reference_kv(w, seed)
+    wo = I.out_proj_weight(w, seed).to(dev)
+    x = I.state_x(w, seed).to(dev)
+    cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                       w.rope_base, interp_chunks=True)
+    cs.set_reference(rk.to(dev), rv.to(dev))
+    for c in range(2):  # N0, N1 (one step each is enough to fill the anchors)
+        cs.step(q, k, v, wo, x, dts[0], True)
+        cs.end_chunk()
+    isets = []
+    for c in range(2):
+        si = I.istep_inputs(w, seed, c, 0)
+        isets.append(tuple(t.to(dev) for t in (si.q, si.k, si.v)))
+    n_int = (w.F - 2) * w.frame_tokens
+    xi = torch.zeros((w.B * n_int, w.hid), dtype=torch.float32, device=dev)
+    for i in range(args.warmup):
+        cs.istep(*isets[i & 1], wo, xi, dts[i % w.steps])
+    cs.sync()
+    barrier(world)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        a.record(stream)
+        for i in range(args.steps):
+            cs.istep(*isets[i & 1], wo, xi, dts[i % w.steps])
+        b.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    cs.sync()
+    cs.close()
+    ms = max_over_ranks(world, a.elapsed_time(b)) / args.steps
+    n_kv = w.n_ref + 2 * w.frame_tokens + n_int
+    flops = 4.0 * w.B * w.H * n_int * n_kv * w.D
+    return {
+        "metric": METRIC,
+        "value": round(whole_job_rate(world, flops, ms) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v/ref, W_o ~ N(0,1/hid))",
+        "config": {"workload": f"interpolation chunk of {describe(w)}: {n_int} interior queries over "
+                               f"{w.n_ref} ref + {2 * w.frame_tokens} anchor + {n_int} interior kv tokens",
+                   "parallelism": f"replicas x{world}", "global_batch": world * w.B,
+                   "l2": "two alternating input sets larger than L2"},
+        "latent_frames_per_s": round(whole_job_rate(world, w.B * (w.F - 2), ms), 1),
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "e2e": None, "cpu_baseline": None, "roofline": None,
+    }
+
+
 # ------------------------------------------------------------- oracle arm
 
 class OracleSample:
@@ -539,7 +605,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=600)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="base", choices=["base", "sr", "sr1", "long", "small", "tiny"])
+    ap.add_argument("--config", default="base", choices=["base", "sr", "sr1", "long", "ibase", "small", "tiny"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -548,15 +614,15 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = I.WORKLOADS[args.config]
+    w = I.WORKLOADS["base" if args.config == "ibase" else args.config]
     world, rank, local = dist_setup()
     if args.impl == "reference":
         res = run_reference(args, w, world, rank)
         if rank == 0 and res is not None:
             print(json.dumps(res), flush=True)
         return
-    if args.config == "long":
-        res = run_long(args, w, world, rank, local)
+    if args.config in ("long", "ibase"):
+        res = (run_long if args.config == "long" else run_interp)(args, w, world, rank, local)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return

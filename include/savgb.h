@@ -178,6 +178,7 @@ typedef struct {
   int ref_t;           /* time of the last reference frame, e.g. -1 */
   double rope_base;    /* rotary base, e.g. 10000 */
   float softmax_scale; /* <= 0 selects 1/sqrt(D) */
+  int interp_chunks;   /* nonzero: keep the anchors of interpolation chunks (needs F >= 3) */
 } chunk_stream_config;
 
 typedef struct chunk_stream chunk_stream_t;
@@ -202,6 +203,33 @@ int chunk_stream_set_reference(chunk_stream_t* s, const void* k_ref, const void*
 int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const void* v,
                       const void* w_o, const float* bias, float* x, float dt, int is_last_step);
 
+/* --------------------------------------------------------------------------
+ * Interpolation (I) chunks ("Boundary continuity and chunk consistency"):
+ * N chunks form the primary timeline and I chunks smooth the transitions
+ * between consecutive N chunks, in the order N0, N1, I0, N2, I1, N3, I2, ...
+ * I_k runs after N_k and N_{k+1} are finished.  Reading: an I chunk spans F
+ * latent frames whose first and last frames are anchors - the last frame of
+ * N_k (at t = 0) and the first frame of N_{k+1} (at t = F-1), both the
+ * pre-RoPE K and V of their chunk's final step - and whose F-2 interior
+ * frames are generated; anchor predictions are discarded, so only interior
+ * frames are queries.  Keys/values: [reference | anchors | interior].
+ * With interp_chunks set, the last step of every N chunk keeps its first and
+ * last frame in two fixed anchor slots.
+ *
+ * chunk_stream_istep: one denoising step of the pending I chunk I_k,
+ *   k = chunk_stream_ichunk_index().  q, k, v: bf16 [B][(F-2)*h*w][H][D]
+ *   interior tokens (before RoPE, chunk-local t = 1..F-2); x fp32
+ *   [B*(F-2)*h*w][H*D].  Needs N_k and N_{k+1} finished: SAVGB_ERR_STATE
+ *   otherwise.  If N_{k+2} has also finished, the anchors of I_k are gone and
+ *   the pending I chunk moves on to I_{done-2} (I chunks not run are skipped).
+ * chunk_stream_end_ichunk: the pending I chunk is done; the next one is pending.
+ * ------------------------------------------------------------------------ */
+int chunk_stream_istep(chunk_stream_t* s, const void* q, const void* k, const void* v,
+                       const void* w_o, const float* bias, float* x, float dt);
+int chunk_stream_end_ichunk(chunk_stream_t* s);
+/* Index of the pending I chunk (0 before the first). */
+int chunk_stream_ichunk_index(const chunk_stream_t* s, int64_t* index);
+
 /* Ends the current chunk: the boundary captured at its last step becomes the
  * boundary of the next chunk, and the chunk index advances.  Returns
  * SAVGB_ERR_STATE if no step of the chunk had is_last_step set (with
@@ -225,8 +253,8 @@ int chunk_stream_sync(chunk_stream_t* s);
 int chunk_stream_info(const chunk_stream_t* s, int64_t* chunk_index, int64_t* boundary_tokens,
                       int64_t* arena_bytes, const void** boundary_k, const void** boundary_v);
 
-/* Checkpoint of the rolling state (chunk index + boundary K/V in use) into a
- * host buffer.  With buf == NULL only *size_out is set.  Synchronises the
+/* Checkpoint of the rolling state (chunk index, boundary K/V in use, and with
+ * interp_chunks the I-chunk index and both anchor slots) into a host buffer.  With buf == NULL only *size_out is set.  Synchronises the
  * stream.  The reference is not part of the state (it is set again on
  * resume). */
 int chunk_stream_export_state(chunk_stream_t* s, void* buf, size_t cap, size_t* size_out);

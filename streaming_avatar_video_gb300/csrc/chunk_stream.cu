@@ -46,6 +46,11 @@ struct chunk_stream {
   __nv_bfloat16_raw* q_rot;
   __nv_bfloat16_raw* k_rot;
   __nv_bfloat16_raw* o;
+  // interpolation chunks: slot k%2 holds the anchors of I_k, [B][2 frames][H][D]:
+  // N_k's last frame rotated to t = 0, then N_{k+1}'s first frame rotated to t = F-1
+  __nv_bfloat16_raw* anc_k[2];
+  __nv_bfloat16_raw* anc_v[2];
+  int64_t ichunk_index;
   int cur;             // boundary slot in use
   int64_t bnd_in_use;  // 0 on chunk 0
   bool captured;
@@ -61,10 +66,12 @@ constexpr uint64_t kStateMagic = 0x5341564742535431ull;  // "SAVGBST1"
 
 struct StateHeader {
   uint64_t magic;
-  int32_t B, H, D, F, grid_h, grid_w, boundary_frames, pad;
+  int32_t B, H, D, F, grid_h, grid_w, boundary_frames, interp;
   int64_t chunk_index;
   int64_t bnd_in_use;
   int64_t payload_bytes;
+  int64_t ichunk_index;
+  int64_t reserved;
 };
 
 int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
@@ -81,6 +88,8 @@ int validate_config(const chunk_stream_config* c) {
     return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: rope_base must be finite and > 0");
   const int64_t hid = (int64_t)c->H * c->D;
   if (hid % 16) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: H*D must be a multiple of 16");
+  if (c->interp_chunks && c->F < 3)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: interpolation chunks need F >= 3");
   return SAVGB_OK;
 }
 
@@ -122,7 +131,8 @@ int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stre
   const int64_t ref_b = round_up(s->n_ref * tok_bytes, 256);
   const int64_t bnd_b = round_up((s->n_bnd > 0 ? s->n_bnd : 1) * tok_bytes, 256);
   const int64_t tok_b = round_up(s->n_tok * tok_bytes, 256);
-  s->arena_bytes = 2 * ref_b + 4 * bnd_b + 3 * tok_b;
+  const int64_t anc_b = c.interp_chunks ? round_up(2 * fr * tok_bytes, 256) : 0;
+  s->arena_bytes = 2 * ref_b + 4 * bnd_b + 3 * tok_b + 4 * anc_b;
   const char* cap = getenv("SAVGB_ARENA_LIMIT_BYTES");
   if (cap && *cap) {
     const long long lim = atoll(cap);
@@ -145,6 +155,11 @@ int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stre
   s->q_rot = take(tok_b);
   s->k_rot = take(tok_b);
   s->o = take(tok_b);
+  for (int i = 0; i < 2; ++i) {
+    s->anc_k[i] = anc_b ? take(anc_b) : nullptr;
+    s->anc_v[i] = anc_b ? take(anc_b) : nullptr;
+  }
+  s->ichunk_index = 0;
   s->cur = 0;
   s->bnd_in_use = 0;
   s->captured = false;
@@ -169,6 +184,7 @@ int chunk_stream_set_reference(chunk_stream_t* s, const void* k_ref, const void*
   s->bnd_in_use = 0;
   s->captured = false;
   s->chunk_index = 0;
+  s->ichunk_index = 0;
   return SAVGB_OK;
 }
 
@@ -220,6 +236,83 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
   } else if (is_last_step) {
     s->captured = true;
   }
+  if (is_last_step && c.interp_chunks) {
+    // anchors of the interpolation chunks on either side of this N chunk
+    const int64_t fr_el = (int64_t)c.grid_h * c.grid_w * s->hid;  // one frame, one session
+    const int64_t anc_per_b = 2 * fr_el;
+    const int64_t idx = s->chunk_index;
+    const int sl_prev = (int)(idx & 1);        // I_idx: this chunk's last frame at t = 0
+    const int64_t last = s->n_tok * s->hid - fr_el;
+    RopeArgs al = rope_args(s, static_cast<const __nv_bfloat16_raw*>(k) + last, s->anc_k[sl_prev], per_b,
+                            anc_per_b, 1, 0);
+    if ((rc = launch_rope(al, s->stream))) return rc;
+    SAVGB_CUDA(cudaMemcpy2DAsync(s->anc_v[sl_prev], (size_t)anc_per_b * 2,
+                                 static_cast<const __nv_bfloat16_raw*>(v) + last, (size_t)per_b * 2,
+                                 (size_t)fr_el * 2, (size_t)c.B, cudaMemcpyDeviceToDevice, s->stream));
+    if (idx >= 1) {
+      const int sl_next = (int)((idx - 1) & 1);  // I_{idx-1}: this chunk's first frame at t = F-1
+      RopeArgs af = rope_args(s, k, s->anc_k[sl_next] + fr_el, per_b, anc_per_b, 1, c.F - 1);
+      if ((rc = launch_rope(af, s->stream))) return rc;
+      SAVGB_CUDA(cudaMemcpy2DAsync(s->anc_v[sl_next] + fr_el, (size_t)anc_per_b * 2, v, (size_t)per_b * 2,
+                                   (size_t)fr_el * 2, (size_t)c.B, cudaMemcpyDeviceToDevice, s->stream));
+    }
+  }
+  return SAVGB_OK;
+}
+
+int chunk_stream_istep(chunk_stream_t* s, const void* q, const void* k, const void* v,
+                       const void* w_o, const float* bias, float* x, float dt) {
+  clear_error();
+  if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_istep: null handle");
+  const chunk_stream_config& c = s->cfg;
+  if (!c.interp_chunks) return fail(SAVGB_ERR_STATE, "chunk_stream_istep: the stream was created without interp_chunks");
+  if (!s->ref_set) return fail(SAVGB_ERR_STATE, "chunk_stream_istep: set_reference has not been called");
+  if (!q || !k || !v || !w_o || !x) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_istep: null argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(w_o) || !aligned16(x) ||
+      (bias && !aligned16(bias)))
+    return fail(SAVGB_ERR_ALIGNMENT, "chunk_stream_istep: pointers must be 16-byte aligned");
+  if (!std::isfinite(dt)) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_istep: dt must be finite");
+  if (s->chunk_index > s->ichunk_index + 2) s->ichunk_index = s->chunk_index - 2;  // anchors of older ones are gone
+  if (s->captured && s->chunk_index == s->ichunk_index + 2)
+    return fail(SAVGB_ERR_STATE, "chunk_stream_istep: I chunk %lld must run before the last step of N chunk %lld",
+                (long long)s->ichunk_index, (long long)s->chunk_index);
+  if (s->chunk_index < s->ichunk_index + 2)
+    return fail(SAVGB_ERR_STATE, "chunk_stream_istep: I chunk %lld needs N chunks %lld and %lld finished (%lld are)",
+                (long long)s->ichunk_index, (long long)s->ichunk_index, (long long)s->ichunk_index + 1,
+                (long long)s->chunk_index);
+  const int64_t fr = (int64_t)c.grid_h * c.grid_w;
+  const int64_t n_int = (c.F - 2) * fr;
+  const int64_t per_b = n_int * s->hid;
+  RopeArgs aq = rope_args(s, q, s->q_rot, per_b, per_b, c.F - 2, 1);
+  RopeArgs ak = rope_args(s, k, s->k_rot, per_b, per_b, c.F - 2, 1);
+  int rc = launch_rope_pair(aq, ak, s->stream);
+  if (rc) return rc;
+  const int sl = (int)(s->ichunk_index & 1);
+  AttnSeg segs[3] = {
+      {s->ref_k, s->ref_v, s->n_ref},
+      {s->anc_k[sl], s->anc_v[sl], 2 * fr},
+      {s->k_rot, v, n_int},
+  };
+  rc = launch_attention(s->q_rot, c.B, n_int, c.H, c.D, segs, 3, c.softmax_scale, s->o, nullptr, s->stream);
+  if (rc) return rc;
+  return launch_out_proj_euler(s->o, w_o, bias, x, c.B * n_int, (int)s->hid, (int)s->hid, dt, nullptr,
+                               s->stream);
+}
+
+int chunk_stream_end_ichunk(chunk_stream_t* s) {
+  clear_error();
+  if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_end_ichunk: null handle");
+  if (!s->cfg.interp_chunks) return fail(SAVGB_ERR_STATE, "chunk_stream_end_ichunk: no interpolation chunks");
+  if (s->chunk_index < s->ichunk_index + 2)
+    return fail(SAVGB_ERR_STATE, "chunk_stream_end_ichunk: I chunk %lld has not started", (long long)s->ichunk_index);
+  s->ichunk_index += 1;
+  return SAVGB_OK;
+}
+
+int chunk_stream_ichunk_index(const chunk_stream_t* s, int64_t* index) {
+  clear_error();
+  if (!s || !index) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_ichunk_index: null argument");
+  *index = s->ichunk_index;
   return SAVGB_OK;
 }
 
@@ -273,7 +366,9 @@ int chunk_stream_info(const chunk_stream_t* s, int64_t* chunk_index, int64_t* bo
 int chunk_stream_export_state(chunk_stream_t* s, void* buf, size_t cap, size_t* size_out) {
   clear_error();
   if (!s || !size_out) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_export_state: null argument");
-  const int64_t payload = 2 * s->bnd_in_use * s->hid * 2 * s->cfg.B;
+  const int64_t fr = (int64_t)s->cfg.grid_h * s->cfg.grid_w;
+  const int64_t anc_bytes = s->cfg.interp_chunks ? 2 * fr * s->hid * 2 * s->cfg.B : 0;  // one slot, K or V
+  const int64_t payload = 2 * s->bnd_in_use * s->hid * 2 * s->cfg.B + 4 * anc_bytes;
   const size_t total = sizeof(StateHeader) + (size_t)payload;
   *size_out = total;
   if (!buf) return SAVGB_OK;
@@ -283,15 +378,23 @@ int chunk_stream_export_state(chunk_stream_t* s, void* buf, size_t cap, size_t* 
   const chunk_stream_config& c = s->cfg;
   h.B = c.B; h.H = c.H; h.D = c.D; h.F = c.F; h.grid_h = c.grid_h; h.grid_w = c.grid_w;
   h.boundary_frames = c.boundary_frames;
+  h.interp = c.interp_chunks ? 1 : 0;
   h.chunk_index = s->chunk_index;
   h.bnd_in_use = s->bnd_in_use;
   h.payload_bytes = payload;
+  h.ichunk_index = s->ichunk_index;
   memcpy(buf, &h, sizeof(h));
-  if (payload > 0) {
-    uint8_t* dst = static_cast<uint8_t*>(buf) + sizeof(h);
-    const size_t half = (size_t)payload / 2;
+  uint8_t* dst = static_cast<uint8_t*>(buf) + sizeof(h);
+  const size_t half = (size_t)(s->bnd_in_use * s->hid * 2 * c.B);
+  if (half > 0) {
     SAVGB_CUDA(cudaMemcpyAsync(dst, s->bnd_k[s->cur], half, cudaMemcpyDeviceToHost, s->stream));
     SAVGB_CUDA(cudaMemcpyAsync(dst + half, s->bnd_v[s->cur], half, cudaMemcpyDeviceToHost, s->stream));
+  }
+  dst += 2 * half;
+  for (int i = 0; i < 2 && anc_bytes > 0; ++i) {
+    SAVGB_CUDA(cudaMemcpyAsync(dst, s->anc_k[i], (size_t)anc_bytes, cudaMemcpyDeviceToHost, s->stream));
+    SAVGB_CUDA(cudaMemcpyAsync(dst + anc_bytes, s->anc_v[i], (size_t)anc_bytes, cudaMemcpyDeviceToHost, s->stream));
+    dst += 2 * anc_bytes;
   }
   SAVGB_CUDA(cudaStreamSynchronize(s->stream));
   return SAVGB_OK;
@@ -305,22 +408,32 @@ int chunk_stream_import_state(chunk_stream_t* s, const void* buf, size_t size) {
   memcpy(&h, buf, sizeof(h));
   const chunk_stream_config& c = s->cfg;
   if (h.magic != kStateMagic || h.B != c.B || h.H != c.H || h.D != c.D || h.F != c.F ||
-      h.grid_h != c.grid_h || h.grid_w != c.grid_w || h.boundary_frames != c.boundary_frames)
+      h.grid_h != c.grid_h || h.grid_w != c.grid_w || h.boundary_frames != c.boundary_frames ||
+      h.interp != (c.interp_chunks ? 1 : 0))
     return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_import_state: state of another configuration");
+  const int64_t fr = (int64_t)c.grid_h * c.grid_w;
+  const int64_t anc_bytes = c.interp_chunks ? 2 * fr * s->hid * 2 * c.B : 0;
   if ((h.bnd_in_use != 0 && h.bnd_in_use != s->n_bnd) ||
-      h.payload_bytes != 2 * h.bnd_in_use * s->hid * 2 * c.B ||
-      size != sizeof(StateHeader) + (size_t)h.payload_bytes || h.chunk_index < 0)
+      h.payload_bytes != 2 * h.bnd_in_use * s->hid * 2 * c.B + 4 * anc_bytes ||
+      size != sizeof(StateHeader) + (size_t)h.payload_bytes || h.chunk_index < 0 || h.ichunk_index < 0)
     return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_import_state: inconsistent sizes");
   if (!s->ref_set) return fail(SAVGB_ERR_STATE, "chunk_stream_import_state: set_reference first");
-  if (h.payload_bytes > 0) {
-    const uint8_t* src = static_cast<const uint8_t*>(buf) + sizeof(h);
-    const size_t half = (size_t)h.payload_bytes / 2;
+  const uint8_t* src = static_cast<const uint8_t*>(buf) + sizeof(h);
+  const size_t half = (size_t)(h.bnd_in_use * s->hid * 2 * c.B);
+  if (half > 0) {
     SAVGB_CUDA(cudaMemcpyAsync(s->bnd_k[s->cur], src, half, cudaMemcpyHostToDevice, s->stream));
     SAVGB_CUDA(cudaMemcpyAsync(s->bnd_v[s->cur], src + half, half, cudaMemcpyHostToDevice, s->stream));
-    SAVGB_CUDA(cudaStreamSynchronize(s->stream));
   }
+  src += 2 * half;
+  for (int i = 0; i < 2 && anc_bytes > 0; ++i) {
+    SAVGB_CUDA(cudaMemcpyAsync(s->anc_k[i], src, (size_t)anc_bytes, cudaMemcpyHostToDevice, s->stream));
+    SAVGB_CUDA(cudaMemcpyAsync(s->anc_v[i], src + anc_bytes, (size_t)anc_bytes, cudaMemcpyHostToDevice, s->stream));
+    src += 2 * anc_bytes;
+  }
+  SAVGB_CUDA(cudaStreamSynchronize(s->stream));
   s->bnd_in_use = h.bnd_in_use;
   s->chunk_index = h.chunk_index;
+  s->ichunk_index = h.ichunk_index;
   s->captured = false;
   return SAVGB_OK;
 }

@@ -142,6 +142,17 @@ def step_inputs(w: Workload, seed: int, chunk: int, step: int) -> StepInputs:
     )
 
 
+def istep_inputs(w: Workload, seed: int, ichunk: int, step: int) -> StepInputs:
+    """Interior tokens of an interpolation chunk: bf16 [B][(F-2)*h*w][H][D]."""
+    shp = (w.B, (w.F - 2) * w.frame_tokens, w.H, w.D)
+    key = 0x4000 + ichunk
+    return StepInputs(
+        q=normal_bf16(shp, 1.0, seed, KIND_Q, key, step),
+        k=normal_bf16(shp, 1.0, seed, KIND_K, key, step),
+        v=normal_bf16(shp, 1.0, seed, KIND_V, key, step),
+    )
+
+
 def reference_kv(w: Workload, seed: int):
     """Static reference tokens' K and V, bf16 [B][n_ref][H][D], before RoPE."""
     shp = (w.B, w.n_ref, w.H, w.D)

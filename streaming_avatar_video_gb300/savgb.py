@@ -31,6 +31,7 @@ EXPORTS = (
     "flow_time_grid", "chunk_stream_create", "chunk_stream_set_reference", "chunk_stream_step",
     "chunk_stream_end_chunk", "chunk_stream_set_step_events", "chunk_stream_sync", "chunk_stream_info", "chunk_stream_export_state",
     "chunk_stream_import_state", "chunk_stream_destroy", "chunk_step_noalloc",
+    "chunk_stream_istep", "chunk_stream_end_ichunk", "chunk_stream_ichunk_index",
 )
 
 
@@ -48,7 +49,8 @@ class ChunkStreamConfig(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("D", ctypes.c_int), ("F", ctypes.c_int),
                 ("grid_h", ctypes.c_int), ("grid_w", ctypes.c_int), ("ref_frames", ctypes.c_int),
                 ("boundary_frames", ctypes.c_int), ("ref_t", ctypes.c_int),
-                ("rope_base", ctypes.c_double), ("softmax_scale", ctypes.c_float)]
+                ("rope_base", ctypes.c_double), ("softmax_scale", ctypes.c_float),
+                ("interp_chunks", ctypes.c_int)]
 
 
 _lib = None
@@ -79,6 +81,9 @@ def lib() -> ctypes.CDLL:
         "chunk_stream_set_reference": (c_int, [c_vp, c_vp, c_vp]),
         "chunk_stream_step": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f, c_int]),
         "chunk_stream_end_chunk": (c_int, [c_vp]),
+        "chunk_stream_istep": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f]),
+        "chunk_stream_end_ichunk": (c_int, [c_vp]),
+        "chunk_stream_ichunk_index": (c_int, [c_vp, ctypes.POINTER(c_i64)]),
         "chunk_stream_set_step_events": (c_int, [c_vp, ctypes.POINTER(c_vp)]),
         "chunk_stream_sync": (c_int, [c_vp]),
         "chunk_stream_info": (c_int, [c_vp, ctypes.POINTER(c_i64), ctypes.POINTER(c_i64), ctypes.POINTER(c_i64),
@@ -226,9 +231,9 @@ class ChunkStream:
 
     def __init__(self, B: int, H: int, D: int, F: int, grid_h: int, grid_w: int, ref_frames: int = 1,
                  boundary_frames: int = 0, ref_t: int = -1, rope_base: float = 10000.0,
-                 softmax_scale: float = 0.0, stream=None):
+                 softmax_scale: float = 0.0, stream=None, interp_chunks: bool = False):
         self.cfg = ChunkStreamConfig(B, H, D, F, grid_h, grid_w, ref_frames, boundary_frames, ref_t,
-                                     float(rope_base), float(softmax_scale))
+                                     float(rope_base), float(softmax_scale), int(bool(interp_chunks)))
         self.stream = _stream(stream)
         h = ctypes.c_void_p()
         _check(lib().chunk_stream_create(ctypes.byref(self.cfg), self.stream, ctypes.byref(h)))
@@ -263,6 +268,29 @@ class ChunkStream:
     def end_chunk(self) -> None:
         _check(lib().chunk_stream_end_chunk(self.handle))
 
+    def istep(self, q, k, v, w_o, x, dt: float, bias=None) -> None:
+        """One step of the pending interpolation chunk (interior frames only)."""
+        c = self.cfg
+        shp = (c.B, (c.F - 2) * c.grid_h * c.grid_w, c.H, c.D)
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            _need(t, name, torch.bfloat16, 4)
+            if tuple(t.shape) != shp:
+                raise ValueError(f"{name} must be {shp}")
+        _need(w_o, "w_o", torch.bfloat16, 2)
+        _need(x, "x", torch.float32)
+        if bias is not None:
+            _need(bias, "bias", torch.float32, 1)
+        _check(lib().chunk_stream_istep(self.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(), w_o.data_ptr(),
+                                        _ptr(bias), x.data_ptr(), float(dt)))
+
+    def end_ichunk(self) -> None:
+        _check(lib().chunk_stream_end_ichunk(self.handle))
+
+    def ichunk_index(self) -> int:
+        i = ctypes.c_int64()
+        _check(lib().chunk_stream_ichunk_index(self.handle, ctypes.byref(i)))
+        return i.value
+
     def set_step_events(self, events) -> None:
         """events: 4 torch.cuda.Event (created with enable_timing) recorded by
         the next step at its start, after RoPE, after attention and after
@@ -289,7 +317,8 @@ class ChunkStream:
         return {"chunk_index": ci.value, "boundary_tokens": bt.value, "arena_bytes": ab.value,
                 "boundary_k": bk.value, "boundary_v": bv.value}
 
-    STATE_HEADER_BYTES = 64  # magic u64, 8 x int32, chunk index, boundary tokens, payload bytes (int64)
+    # magic u64, 8 x int32, chunk index, boundary tokens, payload bytes, I-chunk index, reserved (int64)
+    STATE_HEADER_BYTES = 80
 
     def boundary(self):
         """Host copies of the boundary K (rotated) and V in use, bf16 [B][n_b][H][D]

@@ -370,3 +370,116 @@ def test_stream_step_full_size_sampled_rows(S, name):
     o = O.attention(q_rot, [(rk_rot, f64(rv)), (bk_rot, bv), (k_rot, f64(st1.v))])
     want = O.euler_update(f64(x0)[rows], O.out_proj(o.reshape(len(rows), w.hid), f64(wo)), dt)
     assert_close(f64(got)[rows], want, what=f"{name} step x (sampled rows)")
+
+
+# ---------------------------------------------------- interpolation chunks
+
+def _ni_workload(D):
+    if D == 64:
+        return I.Workload("ni64", B=1, H=4, D=64, F=4, grid_h=8, grid_w=12, ref_frames=1, boundary_frames=1,
+                          steps=2, shift=1.0)
+    return I.Workload("ni128", B=2, H=2, D=128, F=5, grid_h=6, grid_w=10, ref_frames=1, boundary_frames=2,
+                      steps=2, shift=3.0)
+
+
+def _run_ni_gpu(S, w, seed, n_chunks, stop_after=None, cs=None):
+    """N0, N1, I0, N2, I1, ... through the driver; returns the x of every chunk."""
+    dts = S.flow_time_grid(w.steps, w.shift)
+    rk, rv = I.reference_kv(w, seed)
+    wo = I.out_proj_weight(w, seed).cuda()
+    if cs is None:
+        cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                           w.rope_base, interp_chunks=True)
+        cs.set_reference(rk.cuda(), rv.cuda())
+    xs_n, xs_i = [], []
+    n_int = (w.F - 2) * w.frame_tokens
+    for c in range(n_chunks):
+        x = torch.from_numpy(I.normal_f32((w.B * w.n_q, w.hid), 1.0, seed, I.KIND_X, c)).cuda()
+        for s, dt in enumerate(dts):
+            st = I.step_inputs(w, seed, c, s)
+            cs.step(st.q.cuda(), st.k.cuda(), st.v.cuda(), wo, x, dt, s == len(dts) - 1)
+        cs.end_chunk()
+        xs_n.append(x.cpu())
+        if stop_after is not None and c == stop_after:
+            return cs, xs_n, xs_i
+        if c >= 1:
+            assert cs.ichunk_index() == c - 1
+            xi = torch.from_numpy(I.normal_f32((w.B * n_int, w.hid), 1.0, seed, I.KIND_X, 0x4000 + c - 1)).cuda()
+            for s, dt in enumerate(dts):
+                st = I.istep_inputs(w, seed, c - 1, s)
+                cs.istep(st.q.cuda(), st.k.cuda(), st.v.cuda(), wo, xi, dt)
+            cs.end_ichunk()
+            xs_i.append(xi.cpu())
+    cs.sync()
+    return cs, xs_n, xs_i
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_stream_interp_chunks(S, D):
+    """N0, N1, I0, N2, I1: every N and I chunk's x against the oracle."""
+    w = _ni_workload(D)
+    seed = 8
+    cs, xs_n, xs_i = _run_ni_gpu(S, w, seed, 3)
+    cs.close()
+    rk, rv = I.reference_kv(w, seed)
+    wo = I.out_proj_weight(w, seed)
+    n_int = (w.F - 2) * w.frame_tokens
+
+    def n_in(c, s):
+        st = I.step_inputs(w, seed, c, s)
+        return f64(st.q), f64(st.k), f64(st.v)
+
+    def i_in(c, s):
+        st = I.istep_inputs(w, seed, c, s)
+        return f64(st.q), f64(st.k), f64(st.v)
+
+    want_n, want_i, _ = O.run_stream_ni(
+        w, f64(rk), f64(rv), f64(wo),
+        lambda c: I.normal_f32((w.B * w.n_q, w.hid), 1.0, seed, I.KIND_X, c).astype(np.float64),
+        lambda c: I.normal_f32((w.B * n_int, w.hid), 1.0, seed, I.KIND_X, 0x4000 + c).astype(np.float64),
+        n_in, i_in, O.time_grid(w.steps, w.shift), O.time_grid(w.steps, w.shift), 3)
+    for c in range(3):
+        assert_close(f64(xs_n[c]), want_n[c], what=f"N{c} x")
+    for c in range(2):
+        assert_close(f64(xs_i[c]), want_i[c], what=f"I{c} x")
+
+
+def test_interp_state_and_resume(S):
+    w = _ni_workload(128)
+    seed = 4
+    wo = I.out_proj_weight(w, seed).cuda()
+    n_int = (w.F - 2) * w.frame_tokens
+    st = I.istep_inputs(w, seed, 0, 0)
+    xi = torch.zeros((w.B * n_int, w.hid), dtype=torch.float32, device="cuda")
+    # an I step needs two finished N chunks
+    cs, _, _ = _run_ni_gpu(S, w, seed, 1, stop_after=0)
+    with pytest.raises(S.SavgbError) as e:
+        cs.istep(st.q.cuda(), st.k.cuda(), st.v.cuda(), wo, xi, 0.5)
+    assert e.value.status == -7
+    cs.close()
+    # without interp_chunks there is no I step
+    plain = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, 1, 2)
+    with pytest.raises(S.SavgbError):
+        plain.istep(st.q.cuda(), st.k.cuda(), st.v.cuda(), wo, xi, 0.5)
+    plain.close()
+    # checkpoint between N1 and I0, resume in a fresh handle: I0 and N2 equal the uninterrupted run
+    cs_full, xs_n, xs_i = _run_ni_gpu(S, w, seed, 3)
+    cs_full.close()
+    cs_a, _, _ = _run_ni_gpu(S, w, seed, 2, stop_after=1)
+    state = cs_a.export_state()
+    cs_a.close()
+    rk, rv = I.reference_kv(w, seed)
+    cs_b = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                         w.rope_base, interp_chunks=True)
+    cs_b.set_reference(rk.cuda(), rv.cuda())
+    cs_b.import_state(state)
+    assert cs_b.info()["chunk_index"] == 2 and cs_b.ichunk_index() == 0
+    dts = S.flow_time_grid(w.steps, w.shift)
+    xi = torch.from_numpy(I.normal_f32((w.B * n_int, w.hid), 1.0, seed, I.KIND_X, 0x4000)).cuda()
+    for s, dt in enumerate(dts):
+        sti = I.istep_inputs(w, seed, 0, s)
+        cs_b.istep(sti.q.cuda(), sti.k.cuda(), sti.v.cuda(), wo, xi, dt)
+    cs_b.end_ichunk()
+    cs_b.sync()
+    assert torch.equal(xi.cpu(), xs_i[0])
+    cs_b.close()
