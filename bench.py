@@ -286,7 +286,7 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
             "rope3d_gbs": round(rope_bytes / (rope_ms * 1e-3) / 1e9, 1),
         },
         "roofline": {
-            "kernel": "chunk_attention (attn_fwd_kernel<128>)",
+            "kernel": "chunk_attention (attn_fwd_kernel<128, 3, 2, false>)",
             "bound": "tensor",
             "achieved": round(attn_tflops, 1),
             "peak": peak,

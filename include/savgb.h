@@ -123,6 +123,22 @@ typedef struct {
 int chunk_attention(const void* q, int B, int64_t n_q, int H, int D, const savgb_kv_segment* segs,
                     int n_segs, float scale, void* o, float* lse, void* stream);
 
+/* chunk_attention_qrope - chunk_attention with the 3D RoPE of the queries
+ * applied inside the kernel: q holds the chunk's queries BEFORE rotation,
+ * laid out as a grid_t x grid_h x grid_w token grid starting at time t0 (the
+ * rope3d_apply reading: D/2 pairs split [t | h | w], pair j of an axis with P
+ * pairs turning at base^(-j/P)).  Each block rotates its query tiles in
+ * shared memory after loading them, which removes one read and one write of
+ * q from HBM (on GB300 the block's start-up hand-off costs more than that
+ * pass; chunk_stream_step keeps the separate rope3d pass).  Keys must already
+ * be rotated.  Other arguments and errors as
+ * chunk_attention; n_q must equal grid_t*grid_h*grid_w.
+ * ("The underlying model architecture": chunked latent video, reference and
+ * boundary tokens as context.) */
+int chunk_attention_qrope(const void* q, int B, int64_t n_q, int H, int D, int grid_t, int grid_h,
+                          int grid_w, int t0, double base, const savgb_kv_segment* segs, int n_segs,
+                          float scale, void* o, float* lse, void* stream);
+
 /* --------------------------------------------------------------------------
  * out_proj_euler_step - output projection of the attention, taken as the
  * flow-matching velocity, followed by one explicit Euler step of the flow

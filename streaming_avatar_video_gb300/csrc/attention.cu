@@ -28,6 +28,7 @@
 // error word and every role leaves its loop.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "common.h"
@@ -68,6 +69,12 @@ struct AttnParams {
   __nv_bfloat16* o;
   float* lse;
   DeviceErrorWord* err;
+  // 3D RoPE of the queries, applied in shared memory when the kernel is built
+  // with ROPE_Q: query token n sits at (t0 + n/(gh*gw), (n/gw)%gh, n%gw)
+  int gh, gw, t0;
+  int p_t, p_h, p_w;
+  float log2_base;
+  int tab_t_rows;  // time rows of the table (time values one block's 256 queries can span)
 };
 
 template <int D, int KS, int VS>
@@ -89,12 +96,15 @@ struct Layout {
   static constexpr int kPHi = kPLo + 2;    // last 64 written
   static constexpr int kODone = kPHi + 2;
   static constexpr int kDrain = kODone + 2;
-  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kQReady = kDrain + 1;  // queries rotated in place (ROPE_Q)
+  static constexpr int kNumBars = kQReady + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kTab = kMisc + 16;  // cos/sin tables of the query RoPE (ROPE_Q only)
+  static constexpr int kBytes = kTab;
   // request at least 120 KiB so two blocks never share an SM (each holds all 512 TMEM columns)
   static constexpr int kDynSmem = (kBytes + 1024 > 120 * 1024) ? kBytes + 1024 : 120 * 1024;
   static_assert(kBytes + 1024 <= 227 * 1024, "shared memory budget");
+  static constexpr int kTabMax = 227 * 1024 - kDynSmem;  // room left for the RoPE tables
 };
 
 __device__ __forceinline__ void tile_of(const AttnParams& p, int j, int& seg, int& row0, int& valid) {
@@ -116,7 +126,62 @@ __device__ __forceinline__ void give_up(const AttnParams& p, volatile int* abort
   }
 }
 
-template <int D, int KS, int VS>
+// RoPE tables of one block: float2 (cos, sin) for [t rows | h values | w
+// values] x their axis's pairs; the time rows start at the block's first
+// query frame.  Built by the 256 softmax threads before the rotation.
+__device__ __forceinline__ void build_rope_tables(float2* tab, int q0, const AttnParams& p, int tid256) {
+  const int hw = p.gh * p.gw;
+  const int t_first = p.t0 + q0 / hw;
+  const int n_t = p.tab_t_rows * p.p_t, n_h = p.gh * p.p_h, n_w = p.gw * p.p_w;
+  for (int i = tid256; i < n_t + n_h + n_w; i += 256) {
+    int pos, j, P;
+    if (i < n_t) { pos = t_first + i / p.p_t; j = i % p.p_t; P = p.p_t; }
+    else if (i < n_t + n_h) { const int k = i - n_t; pos = k / p.p_h; j = k % p.p_h; P = p.p_h; }
+    else { const int k = i - n_t - n_h; pos = k / p.p_w; j = k % p.p_w; P = p.p_w; }
+    const float omega = exp2f(-static_cast<float>(j) / static_cast<float>(P) * p.log2_base);
+    float sn, cs;
+    sincosf(static_cast<float>(pos) * omega, &sn, &cs);
+    tab[i] = make_float2(cs, sn);
+  }
+}
+
+// Rotates, in place, one query row of the two swizzled Q tiles: row r of the
+// block (tile r/128), token q = q0 + r, by table lookup.
+template <int D>
+__device__ __forceinline__ void rope_q_row(uint8_t* sQ, int tile_bytes, const float2* tab, int r, int q0,
+                                           const AttnParams& p) {
+  const int x = r >> 7, rr = r & 127;
+  const int hw = p.gh * p.gw;
+  const int q = q0 + r;
+  const int tt = q / hw - q0 / hw;  // time row within the block's table
+  const int r2 = q % hw;
+  const int hh = r2 / p.gw;
+  const int ww = r2 - hh * p.gw;
+  const float2* tr = tab + tt * p.p_t;
+  const float2* hr = tab + p.tab_t_rows * p.p_t + hh * p.p_h - p.p_t;
+  const float2* wr = tab + p.tab_t_rows * p.p_t + p.gh * p.p_h + ww * p.p_w - p.p_t - p.p_h;
+  const int ph_end = p.p_t + p.p_h;
+  #pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    #pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint4* cell = reinterpret_cast<uint4*>(sQ + x * tile_bytes + c * 16384 + rr * 128 + ((j ^ (rr & 7)) << 4));
+      uint4 v = *cell;
+      uint32_t w0 = v.x, w1 = v.y, w2 = v.z, w3 = v.w;
+      #define SAVGB_QROT(W, U) { const int pr = c * 32 + 4 * j + (U);                                   \
+        const float2 cs = pr < p.p_t ? tr[pr] : (pr < ph_end ? hr[pr] : wr[pr]);                     \
+        __nv_bfloat162 e = *reinterpret_cast<__nv_bfloat162*>(&W);                                    \
+        const float a = __low2float(e), b = __high2float(e);                                          \
+        __nv_bfloat162 o2 = __floats2bfloat162_rn(a * cs.x - b * cs.y, a * cs.y + b * cs.x);          \
+        W = *reinterpret_cast<uint32_t*>(&o2); }
+      SAVGB_QROT(w0, 0) SAVGB_QROT(w1, 1) SAVGB_QROT(w2, 2) SAVGB_QROT(w3, 3)
+      #undef SAVGB_QROT
+      *cell = make_uint4(w0, w1, w2, w3);
+    }
+  }
+}
+
+template <int D, int KS, int VS, bool ROPE_Q>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p) {
   using L = Layout<D, KS, VS>;
@@ -151,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       dev::mbar_init(&bars[L::kODone + x], 1);
     }
     dev::mbar_init(&bars[L::kDrain], 1);
+    dev::mbar_init(&bars[L::kQReady], 8);  // one elected lane per softmax warp
     *abort = 0;
     dev::fence_barrier_init();
   }
@@ -248,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           dev::mma_ts(d, tmem + x * 128 + kk * 8, b0 + static_cast<uint32_t>(kk * (2048 >> 4)), idesc_o,
                       (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = dev::mbar_wait(&bars[L::kQFull], 0, abort) && dev::mbar_wait(&bars[L::kKFull], 0, abort);
+      bool ok = dev::mbar_wait(&bars[ROPE_Q ? L::kQReady : L::kQFull], 0, abort) &&
+                dev::mbar_wait(&bars[L::kKFull], 0, abort);
       if (!ok) give_up(p, abort, 3);
       if (ok) {
         dev::tc_fence_after();
@@ -314,6 +381,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     dev::setmaxnreg_inc<kRegsHigh>();
+    if constexpr (ROPE_Q) {
+      // ------------------------------------------------ RoPE of the Q tiles
+      float2* tab = reinterpret_cast<float2*>(smem + L::kTab);
+      const int r = (warp - 4) * 32 + lane;  // 0..255
+      build_rope_tables(tab, q0, p, r);
+      dev::named_barrier_256();  // every softmax thread reaches this (no waits before it)
+      bool qok = true;
+      if (lane == 0) qok = dev::mbar_wait(&bars[L::kQFull], 0, abort);
+      qok = __shfl_sync(0xffffffffu, qok ? 1 : 0, 0) != 0;
+      if (qok) {
+        if (q0 + r < p.n_q) rope_q_row<D>(smem + L::kQ, L::kTileBytes, tab, r, q0, p);
+        // the rotated tiles are read by the tensor core (async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(&bars[L::kQReady]);
+      } else {
+        give_up(p, abort, 10);
+      }
+    }
     // ------------------------------------------------------------ softmax
     const int x = (warp - 4) >> 2;
     const int quad = warp & 3;
@@ -452,22 +538,22 @@ int make_token_map(CUtensorMap* m, const void* ptr, int B, int64_t N, int H, int
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int D, int KS, int VS>
+template <int D, int KS, int VS, bool ROPE_Q>
 int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, int n_segs,
-                float scale, void* o, float* lse, cudaStream_t stream) {
+                float scale, void* o, float* lse, const QRope* rope, cudaStream_t stream) {
   using L = Layout<D, KS, VS>;
   static bool attr_done[64] = {false};
   int dev_id = 0;
   SAVGB_CUDA(cudaGetDevice(&dev_id));
   if (!attr_done[dev_id & 63]) {
-    SAVGB_CUDA(cudaFuncSetAttribute(attn_fwd_kernel<D, KS, VS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    L::kDynSmem));
+    SAVGB_CUDA(cudaFuncSetAttribute(attn_fwd_kernel<D, KS, VS, ROPE_Q>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    227 * 1024));
     attr_done[dev_id & 63] = true;
   }
   static int regs_checked[64] = {0};
   if (!regs_checked[dev_id & 63]) {
     cudaFuncAttributes fa;
-    SAVGB_CUDA(cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, KS, VS>));
+    SAVGB_CUDA(cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, KS, VS, ROPE_Q>));
     if (fa.numRegs * kThreads < kRegPoolNeeded)
       return fail(SAVGB_ERR_UNSUPPORTED,
                   "chunk_attention: kernel built with %d registers/thread; its register split needs %d",
@@ -498,9 +584,26 @@ int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, i
   p.scale_log2 = scale * 1.4426950408889634f;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
+  int dyn_smem = L::kDynSmem;
+  if (rope) {
+    p.gh = rope->grid_h;
+    p.gw = rope->grid_w;
+    p.t0 = rope->t0;
+    const int P = D / 2;
+    p.p_h = P / 3;
+    p.p_w = P / 3;
+    p.p_t = P - 2 * (P / 3);
+    p.log2_base = (float)std::log2(rope->base);
+    const int64_t hw = (int64_t)rope->grid_h * rope->grid_w;
+    p.tab_t_rows = (int)((kBlockQ - 1) / hw + 2);
+    const int64_t tab = 8 * ((int64_t)p.tab_t_rows * p.p_t + (int64_t)p.gh * p.p_h + (int64_t)p.gw * p.p_w);
+    if (tab > L::kTabMax)
+      return fail(SAVGB_ERR_UNSUPPORTED, "chunk_attention_qrope: RoPE tables of %lld bytes do not fit", (long long)tab);
+    dyn_smem = std::max<int>(dyn_smem, L::kBytes + 1024 + (int)tab);
+  }
   if ((rc = error_word(&p.err))) return rc;
   dim3 grid((unsigned)((n_q + kBlockQ - 1) / kBlockQ), (unsigned)H, (unsigned)B);
-  attn_fwd_kernel<D, KS, VS><<<grid, kThreads, L::kDynSmem, stream>>>(maps, p);
+  attn_fwd_kernel<D, KS, VS, ROPE_Q><<<grid, kThreads, dyn_smem, stream>>>(maps, p);
   SAVGB_CUDA(cudaGetLastError());
   return SAVGB_OK;
 }
@@ -531,8 +634,33 @@ int launch_attention(const void* q, int B, int64_t n_q, int H, int D, const Attn
                      int n_segs, float scale, void* o, float* lse, cudaStream_t stream) {
   int rc = check_device(nullptr);
   if (rc) return rc;
-  if (D == 64) return launch_impl<64, kStagesK64, kStagesV64>(q, B, n_q, H, segs, n_segs, scale, o, lse, stream);
-  return launch_impl<128, kStagesK128, kStagesV128>(q, B, n_q, H, segs, n_segs, scale, o, lse, stream);
+  if (D == 64)
+    return launch_impl<64, kStagesK64, kStagesV64, false>(q, B, n_q, H, segs, n_segs, scale, o, lse, nullptr, stream);
+  return launch_impl<128, kStagesK128, kStagesV128, false>(q, B, n_q, H, segs, n_segs, scale, o, lse, nullptr,
+                                                          stream);
+}
+
+int validate_qrope(const QRope& r, int64_t n_q, int D) {
+  if (r.grid_t < 1 || r.grid_h < 1 || r.grid_w < 1 || r.grid_h > 4096 || r.grid_w > 4096)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope: grid sizes must be >= 1 (h, w <= 4096)");
+  if ((int64_t)r.grid_t * r.grid_h * r.grid_w != n_q)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope: n_q != grid_t*grid_h*grid_w");
+  if (!(r.base > 0.0) || !std::isfinite(r.base))
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope: base must be finite and > 0");
+  if (r.t0 < -(1 << 20) || r.t0 > (1 << 20)) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope: |t0| > 2^20");
+  if (D != 64 && D != 128) return fail(SAVGB_ERR_UNSUPPORTED, "chunk_attention_qrope: head_dim %d", D);
+  return SAVGB_OK;
+}
+
+int launch_attention_qrope(const void* q, int B, int64_t n_q, int H, int D, const AttnSeg* segs,
+                           int n_segs, float scale, const QRope& rope, void* o, float* lse,
+                           cudaStream_t stream) {
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  if (D == 64)
+    return launch_impl<64, kStagesK64, kStagesV64, true>(q, B, n_q, H, segs, n_segs, scale, o, lse, &rope, stream);
+  // two K stages leave room for the tables
+  return launch_impl<128, 2, kStagesV128, true>(q, B, n_q, H, segs, n_segs, scale, o, lse, &rope, stream);
 }
 
 }  // namespace savgb
@@ -549,4 +677,19 @@ extern "C" int chunk_attention(const void* q, int B, int64_t n_q, int H, int D,
   if (rc) return rc;
   return launch_attention(q, B, n_q, H, D, s, n_segs, scale, o, lse,
                           static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int chunk_attention_qrope(const void* q, int B, int64_t n_q, int H, int D, int grid_t, int grid_h,
+                                     int grid_w, int t0, double base, const savgb_kv_segment* segs, int n_segs,
+                                     float scale, void* o, float* lse, void* stream) {
+  using namespace savgb;
+  clear_error();
+  AttnSeg sg[3] = {};
+  if (segs && n_segs >= 1 && n_segs <= 3)
+    for (int i = 0; i < n_segs; ++i) sg[i] = AttnSeg{segs[i].k, segs[i].v, segs[i].n_tokens};
+  int rc = validate_attention(q, B, n_q, H, D, segs ? sg : nullptr, n_segs, o);
+  if (rc) return rc;
+  const QRope r{grid_t, grid_h, grid_w, t0, base};
+  if ((rc = validate_qrope(r, n_q, D))) return rc;
+  return launch_attention_qrope(q, B, n_q, H, D, sg, n_segs, scale, r, o, lse, static_cast<cudaStream_t>(stream));
 }

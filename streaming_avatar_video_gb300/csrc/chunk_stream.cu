@@ -203,6 +203,8 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
   const bool ev = s->have_events;
   s->have_events = false;
   if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[0], s->stream));
+  // one launch rotates q and k (rotating q inside the attention kernel
+  // measured slower: its start-up hand-off outweighs the saved HBM pass)
   RopeArgs aq = rope_args(s, q, s->q_rot, per_b, per_b, c.F, 0);
   RopeArgs ak = rope_args(s, k, s->k_rot, per_b, per_b, c.F, 0);
   int rc = launch_rope_pair(aq, ak, s->stream);

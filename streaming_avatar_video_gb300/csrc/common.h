@@ -74,6 +74,15 @@ int validate_attention(const void* q, int B, int64_t n_q, int H, int D, const At
                        int n_segs, const void* o);
 int launch_attention(const void* q, int B, int64_t n_q, int H, int D, const AttnSeg* segs,
                      int n_segs, float scale, void* o, float* lse, cudaStream_t stream);
+// Grid of the (unrotated) queries for attention with RoPE of Q fused in.
+struct QRope {
+  int grid_t, grid_h, grid_w, t0;
+  double base;
+};
+int validate_qrope(const QRope& r, int64_t n_q, int D);
+int launch_attention_qrope(const void* q, int B, int64_t n_q, int H, int D, const AttnSeg* segs,
+                           int n_segs, float scale, const QRope& rope, void* o, float* lse,
+                           cudaStream_t stream);
 
 int validate_out_proj(const void* o, const void* w, const float* bias, const float* x, int64_t M,
                       int hid_in, int hid_out, const float* v_out);

@@ -233,6 +233,12 @@ __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Named barrier 1 among 256 threads (the eight softmax warps of the
+// attention kernel).
+__device__ __forceinline__ void named_barrier_256() {
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ numerics
 
 __device__ __forceinline__ float ex2_approx(float x) {

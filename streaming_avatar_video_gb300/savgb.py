@@ -31,7 +31,7 @@ EXPORTS = (
     "flow_time_grid", "chunk_stream_create", "chunk_stream_set_reference", "chunk_stream_step",
     "chunk_stream_end_chunk", "chunk_stream_set_step_events", "chunk_stream_sync", "chunk_stream_info", "chunk_stream_export_state",
     "chunk_stream_import_state", "chunk_stream_destroy", "chunk_step_noalloc",
-    "chunk_stream_istep", "chunk_stream_end_ichunk", "chunk_stream_ichunk_index",
+    "chunk_stream_istep", "chunk_stream_end_ichunk", "chunk_stream_ichunk_index", "chunk_attention_qrope",
 )
 
 
@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
         "chunk_attention": (c_int, [c_vp, c_int, c_i64, c_int, c_int, ctypes.POINTER(KVSegment), c_int, c_f,
                                     c_vp, c_vp, c_vp]),
         "out_proj_euler_step": (c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_int, c_int, c_f, c_vp, c_vp]),
+        "chunk_attention_qrope": (c_int, [c_vp, c_int, c_i64, c_int, c_int, c_int, c_int, c_int, c_int, c_d,
+                                          ctypes.POINTER(KVSegment), c_int, c_f, c_vp, c_vp, c_vp]),
         "flow_time_grid": (c_int, [c_int, c_d, ctypes.POINTER(c_d)]),
         "chunk_stream_create": (c_int, [ctypes.POINTER(ChunkStreamConfig), c_vp, ctypes.POINTER(c_vp)]),
         "chunk_stream_set_reference": (c_int, [c_vp, c_vp, c_vp]),
@@ -190,6 +192,33 @@ def chunk_attention(q: torch.Tensor, segments: Sequence[Tuple[torch.Tensor, torc
             raise ValueError("lse must hold B*H*n_q floats")
     _check(lib().chunk_attention(q.data_ptr(), B, Nq, H, D, segs, len(segments), float(scale),
                                  out.data_ptr(), _ptr(lse), _stream(stream)))
+    return out
+
+
+def chunk_attention_qrope(q: torch.Tensor, grid, segments: Sequence[Tuple[torch.Tensor, torch.Tensor]],
+                          t0: int = 0, base: float = 10000.0, out: Optional[torch.Tensor] = None,
+                          scale: float = 0.0, lse: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """chunk_attention with the 3D RoPE of the (unrotated) queries applied in
+    the kernel; grid = (grid_t, grid_h, grid_w) of the queries."""
+    _need(q, "q", torch.bfloat16, 4)
+    B, Nq, H, D = q.shape
+    if not 1 <= len(segments) <= 3:
+        raise ValueError("1 to 3 segments")
+    segs = (KVSegment * 3)()
+    for i, (k, v) in enumerate(segments):
+        n = k.shape[1] if k.dim() == 4 else 0
+        if n > 0:
+            _need(k, f"segments[{i}].k", torch.bfloat16, 4)
+            _need(v, f"segments[{i}].v", torch.bfloat16, 4)
+            segs[i] = KVSegment(k.data_ptr(), v.data_ptr(), n)
+        else:
+            segs[i] = KVSegment(None, None, 0)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 4)
+    gt, gh, gw = grid
+    _check(lib().chunk_attention_qrope(q.data_ptr(), B, Nq, H, D, gt, gh, gw, t0, float(base), segs, len(segments),
+                                       float(scale), out.data_ptr(), _ptr(lse), _stream(stream)))
     return out
 
 

@@ -483,3 +483,39 @@ def test_interp_state_and_resume(S):
     cs_b.sync()
     assert torch.equal(xi.cpu(), xs_i[0])
     cs_b.close()
+
+
+# ------------------------------------------------- RoPE of Q inside attention
+
+@pytest.mark.parametrize("D,B,gt,gh,gw,t0,segs", [
+    (64, 1, 2, 4, 4, 0, [16, 0]),            # tiny chunk
+    (128, 2, 3, 7, 9, 1, [63, 200, 0]),      # ragged: 189 queries, B = 2, t0 = 1
+    (128, 1, 8, 30, 52, 0, [1560, 3120]),    # base-DiT chunk (sampled rows)
+])
+def test_attention_qrope_parity(S, D, B, gt, gh, gw, t0, segs):
+    """Unrotated queries, rotated inside the kernel, against the oracle's
+    RoPE followed by attention (chunk keys rotated by the oracle)."""
+    H = 4 if D == 128 else 2
+    n_q = gt * gh * gw
+    seed = 40 + D
+    q = bf16((B, n_q, H, D), seed, I.KIND_Q)
+    kc = bf16((B, n_q, H, D), seed, I.KIND_K)
+    vc = bf16((B, n_q, H, D), seed, I.KIND_V)
+    ctx = [(bf16((B, n, H, D), seed, I.KIND_K, chunk=i + 1), bf16((B, n, H, D), seed, I.KIND_V, chunk=i + 1))
+           for i, n in enumerate(segs)]
+    kc_rot = torch.empty_like(kc).cuda()
+    S.rope3d_apply(kc.cuda(), kc_rot, gt, gh, gw, t0)
+    dsegs = [(k.cuda(), v.cuda()) for k, v in ctx] + [(kc_rot, vc.cuda())]
+    dsegs = [sg for sg in dsegs if sg[0].shape[1] > 0][:3]
+    o = S.chunk_attention_qrope(q.cuda(), (gt, gh, gw), dsegs, t0=t0)
+    torch.cuda.synchronize()
+    S.savgb_device_check()
+    rows = None if n_q <= 512 else np.unique(np.r_[np.random.default_rng(2).choice(n_q, 32, replace=False),
+                                                   [0, 127, 255, 256, n_q - 1]])
+    q_rot = O.rope3d(f64(q), gt, gh, gw, t0)
+    k_rot = O.rope3d(f64(kc), gt, gh, gw, t0)
+    osegs = [(f64(k), f64(v)) for k, v in ctx if k.shape[1] > 0] + [(k_rot, f64(vc))]
+    qq = q_rot if rows is None else q_rot[:, rows]
+    want = O.attention(qq, osegs)
+    got = f64(o) if rows is None else f64(o)[:, rows]
+    assert_close(got, want, what=f"attention with RoPE of q inside (D={D})")
