@@ -45,8 +45,8 @@ METRIC = "chunk-attention TFLOP/s (% of bf16 tensor peak); latent frames/s per d
 # launch, from one ncu capture per workload, keyed by the sha256 of the kernel
 # source the capture was taken on; any later change of the source reports null.
 ATTN_TRAFFIC = {
-    # profiles/chunk_attention_base.md: 292.735 MB read + 67.092 MB written
-    "dacd1c68419cf4d48a6914ea861c498fc466286f53c10aa3d261cc0e8311dc67": {"base": 359827456},
+    # profiles/chunk_attention_base.md: 294.978 MB read + 70.734 MB written
+    "2b48181744085dc6b420155dd87c4c0493940e8771d08b35917def5146d3414a": {"base": 365712384},
 }
 
 
