@@ -50,4 +50,7 @@ from .step import (  # noqa: F401
     anchors_from_chunk,
     ichunk_step,
     run_stream_ni,
+    qkv_project,
+    block_step,
+    run_stream_block,
 )

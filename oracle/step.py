@@ -299,3 +299,53 @@ def run_stream_ni(w, ref_k, ref_v, w_o, x0_n, x0_i, n_inputs, i_inputs, dts, idt
         if c >= 1:
             run_i(c - 1)
     return xs_n, xs_i, used
+
+
+# --------------------------------------------------------------------------
+# one attention block of the DiT with its own QKV projection
+# --------------------------------------------------------------------------
+
+def qkv_project(x: np.ndarray, w_qkv: np.ndarray, B: int, H: int, D: int):
+    """q, k, v [B][N][H][D] = x W_qkv^T split in three; x [B*N][hid],
+    W_qkv [3*hid][hid] = [W_q; W_k; W_v] (PyTorch Linear layout)."""
+    hid = H * D
+    qkv = x @ w_qkv.T
+    N = x.shape[0] // B
+    return tuple(qkv[:, i * hid:(i + 1) * hid].reshape(B, N, H, D) for i in range(3))
+
+
+def block_step(x, w_qkv, ref_k_rot, ref_v, bnd_k_rot, bnd_v, w_o, dt, grid, H, D, base=10000.0, scale=None,
+               bias=None):
+    """One denoising step of a chunk through one DiT attention block: the
+    state x [B*N][hid] is projected to q, k, v (qkv_project), then the chunk
+    step of chunk_step (RoPE, attention over [reference | boundary | chunk],
+    W_o, Euler).
+
+    Reading of "The underlying model architecture": the denoiser is a DiT; a
+    single attention block with stand-in weights (no MLP, normalisation or
+    timestep embedding) takes the place of the whole network.
+    Returns (x_next, k, v) with k, v the step's projected keys and values
+    before RoPE (the boundary is taken from those of the final step)."""
+    F, gh, gw = grid
+    B = x.shape[0] // (F * gh * gw)
+    q, k, v = qkv_project(x, w_qkv, B, H, D)
+    x_next, _ = chunk_step(q, k, v, ref_k_rot, ref_v, bnd_k_rot, bnd_v, w_o, x, dt, grid, base, scale, bias)
+    return x_next, k, v
+
+
+def run_stream_block(w, ref_k, ref_v, w_qkv, w_o, x0_per_chunk, dts, chunks, scale=None, bias=None):
+    """A stream of chunks through block_step, the boundary rolled from each
+    chunk's final-step projected k, v.  Returns the final x of every chunk."""
+    ref_k_rot = rope3d(ref_k, w.ref_frames, w.grid_h, w.grid_w, w.ref_t - w.ref_frames + 1, w.rope_base)
+    empty = np.zeros((w.B, 0, w.H, w.D))
+    bnd = (empty, empty)
+    xs = []
+    for c in range(chunks):
+        x = x0_per_chunk(c)
+        for dt in dts:
+            x, k, v = block_step(x, w_qkv, ref_k_rot, ref_v, bnd[0], bnd[1], w_o, dt,
+                                 (w.F, w.grid_h, w.grid_w), w.H, w.D, w.rope_base, scale, bias)
+        xs.append(x)
+        if w.boundary_frames > 0:
+            bnd = boundary_from_chunk(k, v, w.frame_tokens, w.boundary_frames, w.grid_h, w.grid_w, w.rope_base)
+    return xs

@@ -512,3 +512,51 @@ def _bad_ichunk(q, k, v, rk, rv, ap, an, w_o, x, dt, grid, base=10000.0, scale=N
     o = O.attention(q_rot, [(rk, rv), (a, np.concatenate([ap[1], an[1]], axis=1)), (k_rot, v)])
     B, Nq, H, D = o.shape
     return O.euler_update(x, O.out_proj(o.reshape(B * Nq, H * D), w_o), dt), o
+
+
+# ---------------------------------------------------- DiT attention block ----
+
+def pin_qkv_project(qkv=O.qkv_project):
+    """The projection is a literal triple loop, split as [q | k | v] along the
+    output features and reshaped head-major."""
+    rng = np.random.default_rng(21)
+    B, N, H, D = 2, 3, 2, 4
+    hid = H * D
+    x = rng.standard_normal((B * N, hid))
+    w = rng.standard_normal((3 * hid, hid))
+    q, k, v = qkv(x, w, B, H, D)
+    full = np.array(_brute.linear(x.tolist(), w.tolist()))
+    for i, t in enumerate((q, k, v)):
+        assert t.shape == (B, N, H, D)
+        assert np.allclose(t.reshape(B * N, hid), full[:, i * hid:(i + 1) * hid], atol=1e-12)
+    assert np.allclose(q[1, 2, 1], full[5, 4:8], atol=1e-12)
+
+
+def test_qkv_project():
+    pin_qkv_project()
+
+
+def test_planted_qkv_order():
+    def bad(x, w, B, H, D):
+        q, k, v = O.qkv_project(x, w, B, H, D)
+        return k, q, v
+    _expect_pin_failure(pin_qkv_project, bad)
+
+
+def test_block_step_is_projection_then_chunk_step():
+    rng = np.random.default_rng(4)
+    B, H, D, F, gh, gw = 1, 2, 64, 2, 2, 3
+    N, hid = F * gh * gw, H * D
+    x = rng.standard_normal((B * N, hid))
+    wq = rng.standard_normal((3 * hid, hid)) / math.sqrt(hid)
+    wo = rng.standard_normal((hid, hid)) / math.sqrt(hid)
+    rk, rv = rng.standard_normal((B, gh * gw, H, D)), rng.standard_normal((B, gh * gw, H, D))
+    empty = np.zeros((B, 0, H, D))
+    x1, k, v = O.block_step(x, wq, rk, rv, empty, empty, wo, 0.3, (F, gh, gw), H, D)
+    qkv = np.array(_brute.linear(x.tolist(), wq.tolist()))
+    q2 = qkv[:, :hid].reshape(B, N, H, D)
+    k2 = qkv[:, hid:2 * hid].reshape(B, N, H, D)
+    v2 = qkv[:, 2 * hid:].reshape(B, N, H, D)
+    x2, _ = O.chunk_step(q2, k2, v2, rk, rv, empty, empty, wo, x, 0.3, (F, gh, gw))
+    assert np.allclose(x1, x2, atol=1e-12)
+    assert np.allclose(k, k2, atol=1e-12) and np.allclose(v, v2, atol=1e-12)
