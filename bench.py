@@ -496,6 +496,90 @@ def run_interp(args, w: I.Workload, world: int, rank: int, local: int):
     }
 
 
+def run_block(args, w: I.Workload, world: int, rank: int, local: int):
+    """Block steps of a base-shaped stream: the chunk's q, k, v are projected
+    from the state x by the QKV GEMM (RoPE of q, k in its epilogue), then
+    attention and W_o + Euler.  One priming chunk end gives every timed step a
+    boundary."""
+    import __graft_entry__ as g
+    g.build()
+    from streaming_avatar_video_gb300 import savgb as S
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    seed = 1 + rank
+    dts = S.flow_time_grid(w.steps, w.shift)
+    rk, rv = I.reference_kv(w, seed)
+    wqkv = I.qkv_weight(w, seed).to(dev)
+    wo = I.out_proj_weight(w, seed).to(dev)
+    x = I.state_x(w, seed).to(dev)
+    cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                       w.rope_base, qkv_block=True)
+    cs.set_reference(rk.to(dev), rv.to(dev))
+    cs.block_step(wqkv, wo, x, dts[0], True)
+    cs.end_chunk()
+    state = {"i": 0, "launches": 0}
+
+    def one(events=None):
+        i = state["i"]
+        s_ = i % w.steps
+        last = s_ == w.steps - 1
+        if events is not None:
+            cs.set_step_events(events)
+        cs.block_step(wqkv, wo, x, dts[s_], last)
+        state["launches"] += 4 + (1 if last and w.boundary_frames else 0)
+        if last:
+            cs.end_chunk()
+        state["i"] = i + 1
+
+    for _ in range(args.warmup):
+        one()
+    cs.sync()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    state["launches"] = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        a.record(stream)
+        for k_ in range(args.steps):
+            one(ev[k_])
+        b.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    cs.sync()
+    cs.close()
+    ms = max_over_ranks(world, a.elapsed_time(b)) / args.steps
+    qkv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    wo_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    attn = w.attn_flops(True)
+    qkv_flops = 2.0 * w.B * w.n_q * w.hid * 3 * w.hid
+    total = attn + qkv_flops + w.wo_flops()
+    return {
+        "metric": METRIC,
+        "value": round(whole_job_rate(world, attn, ms) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded x ~ N(0,1), W_qkv, W_o ~ N(0,1/hid), reference ~ N(0,1))",
+        "config": {"workload": "DiT attention block steps of " + describe(w),
+                   "parallelism": f"replicas x{world}", "global_batch": world * w.B,
+                   "l2": "state and operands larger than L2"},
+        "latent_frames_per_s": round(whole_job_rate(world, w.B * w.F, ms), 1),
+        "block_tflops": round(whole_job_rate(world, total, ms) / 1e12, 1),
+        "kernels_ms": {"to_bf16+qkv_rope_project": round(qkv_ms, 4), "chunk_attention": round(attn_ms, 4),
+                       "out_proj_euler": round(wo_ms, 4)},
+        "kernel_rates": {"qkv_tflops": round(qkv_flops / (qkv_ms * 1e-3) / 1e12, 1),
+                         "chunk_attention_tflops": round(attn / (attn_ms * 1e-3) / 1e12, 1),
+                         "out_proj_euler_tflops": round(w.wo_flops() / (wo_ms * 1e-3) / 1e12, 1)},
+        "gpu_launches": state["launches"],
+        "clocks": clk.summary(),
+        "e2e": None, "cpu_baseline": None, "roofline": None,
+    }
+
+
 # ------------------------------------------------------------- oracle arm
 
 class OracleSample:
@@ -605,7 +689,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=600)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="base", choices=["base", "sr", "sr1", "long", "ibase", "small", "tiny"])
+    ap.add_argument("--config", default="base", choices=["base", "sr", "sr1", "long", "ibase", "block", "small", "tiny"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -614,15 +698,16 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = I.WORKLOADS["base" if args.config == "ibase" else args.config]
+    w = I.WORKLOADS["base" if args.config in ("ibase", "block") else args.config]
     world, rank, local = dist_setup()
     if args.impl == "reference":
         res = run_reference(args, w, world, rank)
         if rank == 0 and res is not None:
             print(json.dumps(res), flush=True)
         return
-    if args.config in ("long", "ibase"):
-        res = (run_long if args.config == "long" else run_interp)(args, w, world, rank, local)
+    if args.config in ("long", "ibase", "block"):
+        fn = {"long": run_long, "ibase": run_interp, "block": run_block}[args.config]
+        res = fn(args, w, world, rank, local)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return

@@ -158,6 +158,22 @@ int out_proj_euler_step(const void* o, const void* w_o, const float* bias, float
                         int hid_in, int hid_out, float dt, float* v_out, void* stream);
 
 /* --------------------------------------------------------------------------
+ * qkv_rope_project - QKV projection of one DiT attention block with the 3D
+ * RoPE of q and k fused into the GEMM epilogue ("The underlying model
+ * architecture": the denoiser is a Diffusion Transformer; a single attention
+ * block with stand-in weights takes the place of the network here).
+ *   [q | k | v] = x W_qkv^T;  q, k rotated at (t0 + n/(h*w), (n/w)%h, n%w)
+ *   x       bf16 [B][n_tokens][H*D]   (n_tokens = grid_t*grid_h*grid_w)
+ *   w_qkv   bf16 [3*H*D][H*D] = [W_q; W_k; W_v] (PyTorch Linear layout)
+ *   q, k, v bf16 [B][n_tokens][H][D] outputs.
+ * D must be 64 or 128; bf16 tensor-core product, fp32 accumulation, rotation
+ * in fp32, outputs rounded to bf16.
+ * ------------------------------------------------------------------------ */
+int qkv_rope_project(const void* x_bf16, const void* w_qkv, void* q, void* k, void* v, int B,
+                     int64_t n_tokens, int H, int D, int grid_t, int grid_h, int grid_w, int t0,
+                     double base, void* stream);
+
+/* --------------------------------------------------------------------------
  * flow_time_grid - step sizes of the sampling grid (host only).
  * Reading of "multi-step diffusion pass": noise levels sigma_i = 1 - i/steps,
  * warped by sigma' = shift*sigma / (1 + (shift-1)*sigma), dt_i = sigma'_i -
@@ -195,6 +211,7 @@ typedef struct {
   double rope_base;    /* rotary base, e.g. 10000 */
   float softmax_scale; /* <= 0 selects 1/sqrt(D) */
   int interp_chunks;   /* nonzero: keep the anchors of interpolation chunks (needs F >= 3) */
+  int qkv_block;       /* nonzero: reserve room for chunk_stream_block_step */
 } chunk_stream_config;
 
 typedef struct chunk_stream chunk_stream_t;
@@ -245,6 +262,17 @@ int chunk_stream_istep(chunk_stream_t* s, const void* q, const void* k, const vo
 int chunk_stream_end_ichunk(chunk_stream_t* s);
 /* Index of the pending I chunk (0 before the first). */
 int chunk_stream_ichunk_index(const chunk_stream_t* s, int64_t* index);
+
+/* One denoising step of the current chunk through one DiT attention block:
+ * the state itself is projected, x -> bf16 -> qkv_rope_project (q, k
+ * rotated) -> chunk_attention over [reference | boundary | chunk] ->
+ * out_proj_euler_step(x, dt).  Needs qkv_block in the config.
+ *   w_qkv bf16 [3*H*D][H*D]; w_o bf16 [H*D][H*D]; bias optional fp32 [H*D];
+ *   x fp32 [B*N][H*D], updated in place.
+ * With is_last_step the next chunk's boundary is taken from this step's
+ * projected k (before RoPE) and v.  Block steps keep no I-chunk anchors. */
+int chunk_stream_block_step(chunk_stream_t* s, const void* w_qkv, const void* w_o, const float* bias,
+                            float* x, float dt, int is_last_step);
 
 /* Ends the current chunk: the boundary captured at its last step becomes the
  * boundary of the next chunk, and the chunk index advances.  Returns

@@ -19,8 +19,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libsavgb.so")
 
 SOURCES = ["status.cu", "rope3d.cu", "attention.cu", "out_proj_euler.cu", "chunk_stream.cu",
-           "chunk_step_noalloc.cu"]
-HEADERS = ["common.h", "ptx.cuh"]
+           "chunk_step_noalloc.cu", "qkv_proj.cu"]
+HEADERS = ["common.h", "ptx.cuh", "gemm_tc.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

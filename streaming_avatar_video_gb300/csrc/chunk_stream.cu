@@ -50,6 +50,7 @@ struct chunk_stream {
   // N_k's last frame rotated to t = 0, then N_{k+1}'s first frame rotated to t = F-1
   __nv_bfloat16_raw* anc_k[2];
   __nv_bfloat16_raw* anc_v[2];
+  __nv_bfloat16_raw* v_buf;  // projected v of a block step (qkv_block); its bf16 x shares `o`
   int64_t ichunk_index;
   int cur;             // boundary slot in use
   int64_t bnd_in_use;  // 0 on chunk 0
@@ -132,7 +133,8 @@ int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stre
   const int64_t bnd_b = round_up((s->n_bnd > 0 ? s->n_bnd : 1) * tok_bytes, 256);
   const int64_t tok_b = round_up(s->n_tok * tok_bytes, 256);
   const int64_t anc_b = c.interp_chunks ? round_up(2 * fr * tok_bytes, 256) : 0;
-  s->arena_bytes = 2 * ref_b + 4 * bnd_b + 3 * tok_b + 4 * anc_b;
+  const int64_t vbuf_b = c.qkv_block ? tok_b : 0;
+  s->arena_bytes = 2 * ref_b + 4 * bnd_b + 3 * tok_b + 4 * anc_b + vbuf_b;
   const char* cap = getenv("SAVGB_ARENA_LIMIT_BYTES");
   if (cap && *cap) {
     const long long lim = atoll(cap);
@@ -159,6 +161,7 @@ int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stre
     s->anc_k[i] = anc_b ? take(anc_b) : nullptr;
     s->anc_v[i] = anc_b ? take(anc_b) : nullptr;
   }
+  s->v_buf = vbuf_b ? take(vbuf_b) : nullptr;
   s->ichunk_index = 0;
   s->cur = 0;
   s->bnd_in_use = 0;
@@ -315,6 +318,59 @@ int chunk_stream_ichunk_index(const chunk_stream_t* s, int64_t* index) {
   clear_error();
   if (!s || !index) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_ichunk_index: null argument");
   *index = s->ichunk_index;
+  return SAVGB_OK;
+}
+
+int chunk_stream_block_step(chunk_stream_t* s, const void* w_qkv, const void* w_o, const float* bias,
+                            float* x, float dt, int is_last_step) {
+  clear_error();
+  if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_block_step: null handle");
+  const chunk_stream_config& c = s->cfg;
+  if (!c.qkv_block) return fail(SAVGB_ERR_STATE, "chunk_stream_block_step: the stream was created without qkv_block");
+  if (!s->ref_set) return fail(SAVGB_ERR_STATE, "chunk_stream_block_step: set_reference has not been called");
+  if (!w_qkv || !w_o || !x) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_block_step: null argument");
+  if (!aligned16(w_qkv) || !aligned16(w_o) || !aligned16(x) || (bias && !aligned16(bias)))
+    return fail(SAVGB_ERR_ALIGNMENT, "chunk_stream_block_step: pointers must be 16-byte aligned");
+  if (!std::isfinite(dt)) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_block_step: dt must be finite");
+  const bool ev = s->have_events;
+  s->have_events = false;
+  if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[0], s->stream));
+  const int64_t M = (int64_t)c.B * s->n_tok;
+  void* xb = s->o;  // the bf16 copy of x is consumed by the projection before attention writes o
+  int rc = launch_to_bf16(x, xb, M * s->hid, s->stream);
+  if (rc) return rc;
+  const int nxt = s->cur ^ 1;
+  const bool capture = is_last_step && s->n_bnd > 0;
+  QkvArgs qa{xb, w_qkv, s->q_rot, s->k_rot, s->v_buf, capture ? s->bnd_k[nxt] : nullptr, s->n_bnd, c.B,
+             s->n_tok, c.H, c.D, c.F, c.grid_h, c.grid_w, 0, c.rope_base};
+  if ((rc = validate_qkv(qa))) return rc;
+  if ((rc = launch_qkv_rope(qa, s->stream))) return rc;
+  if (capture) {
+    // the boundary: the projected k (stored unrotated by the projection) and v
+    // of the last frames, k rotated in place to t = -T_b .. -1
+    const int64_t bnd_per_b = s->n_bnd * s->hid;
+    RopeArgs ab = rope_args(s, s->bnd_k[nxt], s->bnd_k[nxt], bnd_per_b, bnd_per_b, c.boundary_frames,
+                            -c.boundary_frames);
+    if ((rc = launch_rope(ab, s->stream))) return rc;
+    const int64_t per_b = s->n_tok * s->hid;
+    SAVGB_CUDA(cudaMemcpy2DAsync(s->bnd_v[nxt], (size_t)bnd_per_b * 2, s->v_buf + (per_b - bnd_per_b),
+                                 (size_t)per_b * 2, (size_t)bnd_per_b * 2, (size_t)c.B, cudaMemcpyDeviceToDevice,
+                                 s->stream));
+  }
+  if (is_last_step) s->captured = true;
+  if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[1], s->stream));
+  AttnSeg segs[3] = {
+      {s->ref_k, s->ref_v, s->n_ref},
+      {s->bnd_k[s->cur], s->bnd_v[s->cur], s->bnd_in_use},
+      {s->k_rot, s->v_buf, s->n_tok},
+  };
+  if ((rc = launch_attention(s->q_rot, c.B, s->n_tok, c.H, c.D, segs, 3, c.softmax_scale, s->o, nullptr,
+                             s->stream)))
+    return rc;
+  if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[2], s->stream));
+  if ((rc = launch_out_proj_euler(s->o, w_o, bias, x, M, (int)s->hid, (int)s->hid, dt, nullptr, s->stream)))
+    return rc;
+  if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[3], s->stream));
   return SAVGB_OK;
 }
 

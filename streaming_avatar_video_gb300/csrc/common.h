@@ -84,6 +84,25 @@ int launch_attention_qrope(const void* q, int B, int64_t n_q, int H, int D, cons
                            int n_segs, float scale, const QRope& rope, void* o, float* lse,
                            cudaStream_t stream);
 
+// QKV projection with the RoPE of q and k in the GEMM epilogue.
+struct QkvArgs {
+  const void* x_bf16;  // [B*n_tokens][H*D]
+  const void* w_qkv;   // [3*H*D][H*D]
+  void* q;
+  void* k;
+  void* v;
+  void* k_tail;        // optional: unrotated k of the last n_tail tokens of each batch
+  int64_t n_tail;
+  int B;
+  int64_t n_tokens;
+  int H, D;
+  int grid_t, grid_h, grid_w, t0;
+  double base;
+};
+int validate_qkv(const QkvArgs& a);
+int launch_qkv_rope(const QkvArgs& a, cudaStream_t stream);
+int launch_to_bf16(const float* x, void* y, int64_t n, cudaStream_t stream);
+
 int validate_out_proj(const void* o, const void* w, const float* bias, const float* x, int64_t M,
                       int hid_in, int hid_out, const float* v_out);
 int launch_out_proj_euler(const void* o, const void* w, const float* bias, float* x, int64_t M,

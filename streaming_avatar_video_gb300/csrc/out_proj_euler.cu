@@ -15,21 +15,16 @@
 // epilogue reads them back, turns each 32 x 32 chunk around in shared memory
 // and applies the Euler update to x (fp32, read-modify-write) with coalesced
 // 128-byte row segments, so v never goes through global memory.
-//   warp 0      TMA producer
-//   warp 1      TMEM allocation; lane 0 issues the MMAs
-//   warps 4-11  epilogue (warps 2-3 idle)
+// The mainloop (TMA producer, MMA issue, TMEM) is the shared 256-row GEMM of
+// gemm_tc.cuh; warps 4-11 run the Euler epilogue.
 #include <cuda_bf16.h>
 
 #include "common.h"
+#include "gemm_tc.cuh"
 #include "ptx.cuh"
 
 namespace savgb {
 namespace {
-
-constexpr int kThreads = 384;
-constexpr int kBM = 256;  // two 128-row MMA halves share every B tile
-constexpr int kBK = 64;
-constexpr int kStages = 3;
 
 struct WoParams {
   int M, N, K;
@@ -41,120 +36,21 @@ struct WoParams {
 };
 
 template <int BN>
-struct WoLayout {
-  static constexpr int kAHalf = 128 * kBK * 2;  // 16 KiB
-  static constexpr int kABytes = 2 * kAHalf;
-  static constexpr int kBBytes = BN * kBK * 2;  // 16 or 32 KiB
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kBar = kStages * kStageBytes;
-  static constexpr int kMisc = kBar + (2 * kStages + 2) * 8;
-  static constexpr int kBytes = kMisc + 16;
-  static constexpr int kDynSmem = kBytes + 1024;
-  static_assert(kDynSmem <= 227 * 1024, "shared memory budget");
-  static_assert(8 * 4096 <= kBar, "epilogue staging must fit in the ring");
-};
-
-__device__ __forceinline__ void give_up(const WoParams& p, volatile int* abort, unsigned code) {
-  if (atomicExch(const_cast<int*>(abort), 1) == 0) {
-    atomicOr(&p.err->flags, kErrGemmWait);
-    atomicCAS(&p.err->where, 0u, 0x100u + code);
-  }
-}
-
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm::kThreads, 1)
     wo_euler_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b, const WoParams p) {
-  using L = WoLayout<BN>;
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = dev::smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;
-  uint64_t* drain = acc_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
+  const gemm::Ctx c = gemm::setup<BN>(smem_raw, &map_a, &map_b);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
-  const int m0 = blockIdx.y * kBM;
-  const int kb_count = (p.K + kBK - 1) / kBK;
-
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      dev::mbar_init(&full[s], 1);
-      dev::mbar_init(&empty[s], 1);
-    }
-    dev::mbar_init(acc_full, 1);
-    dev::mbar_init(drain, 1);
-    *abort = 0;
-    dev::fence_barrier_init();
-  }
-  if (warp == 1) {
-    dev::tmem_alloc(tmem_slot, 2 * BN);
-    dev::tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
-    dev::tma_prefetch_desc(&map_a);
-    dev::tma_prefetch_desc(&map_b);
-  }
-  dev::tc_fence_before();
-  __syncthreads();
-  dev::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const int m0 = blockIdx.y * gemm::kBM;
+  const int kb_count = (p.K + gemm::kBK - 1) / gemm::kBK;
 
   if (warp == 0) {
-    if (lane == 0) {
-      int issued = 0;
-      for (int kb = 0; kb < kb_count; ++kb) {
-        const int st = kb % kStages;
-        const uint32_t use = kb / kStages;
-        if (kb >= kStages && !dev::mbar_wait(&empty[st], (use - 1) & 1, abort)) {
-          give_up(p, abort, 1);
-          break;
-        }
-        uint8_t* sa = smem + st * L::kStageBytes;
-        dev::mbar_arrive_expect_tx(&full[st], L::kStageBytes);
-        dev::tma_load_2d(sa, &map_a, &full[st], kb * kBK, m0);
-        dev::tma_load_2d(sa + L::kAHalf, &map_a, &full[st], kb * kBK, m0 + 128);
-        dev::tma_load_2d(sa + L::kABytes, &map_b, &full[st], kb * kBK, n0);
-        issued = kb + 1;
-      }
-      volatile int never = 0;
-      for (int t = (issued > kStages ? issued - kStages : 0); t < issued; ++t)
-        dev::mbar_wait(&full[t % kStages], (t / kStages) & 1, &never);
-    }
+    if (lane == 0) gemm::produce<BN>(c, &map_a, &map_b, m0, n0, kb_count, p.err, kErrGemmWait);
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = dev::idesc_bf16_f32(128, BN, false, false);
-      const uint64_t d0 = dev::sdesc_sw128(dev::smem_u32(smem), 16, 1024);
-      bool ok = true;
-      for (int kb = 0; kb < kb_count; ++kb) {
-        const int st = kb % kStages;
-        if (!dev::mbar_wait(&full[st], (kb / kStages) & 1, abort)) {
-          give_up(p, abort, 2);
-          ok = false;
-          break;
-        }
-        dev::tc_fence_after();
-        const uint64_t ds = d0 + static_cast<uint32_t>((st * L::kStageBytes) >> 4);
-        #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k) {
-          const uint32_t koff = (k * 32) >> 4;
-          const uint64_t bd = ds + ((L::kABytes >> 4) + koff);
-          dev::mma_ss(tmem, ds + koff, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-          dev::mma_ss(tmem + BN, ds + ((L::kAHalf >> 4) + koff), bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-        }
-        dev::mma_commit(&empty[st]);
-      }
-      if (ok) dev::mma_commit(acc_full);
-      dev::mma_commit(drain);
-      volatile int never = 0;
-      dev::mbar_wait(drain, 0, &never);
-    }
+    if (lane == 0) gemm::mma<BN>(c, kb_count, p.err, kErrGemmWait);
   } else if (warp >= 4) {
     // epilogue: warps 4-7 take rows 0-127 (accumulator columns [0, BN)),
     // warps 8-11 rows 128-255 ([BN, 2 BN)).  Each 32-row x 32-column chunk is
@@ -169,27 +65,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ncols = min(BN, p.N - n0);
       if (m < p.M && ncols > 0) dev::prefetch_l2(p.x + static_cast<int64_t>(m) * p.N + n0, ncols * 4);
     }
-    bool ok = true;
-    if (lane == 0) ok = dev::mbar_wait(acc_full, 0, abort);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (ok) {
-      dev::tc_fence_after();
+    if (gemm::wait_acc(c, p.err, kErrGemmWait)) {
       // the operand ring is idle once every MMA has completed: 4 KiB per warp
-      float4* stage = reinterpret_cast<float4*>(smem + (warp - 4) * 4096);
-      const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * BN;
+      float4* stage = reinterpret_cast<float4*>(c.smem + (warp - 4) * 4096);
+      const uint32_t t_row = c.tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * BN;
       const float dt = p.dt;
       const int seg = lane & 7;
       #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
+      for (int cc = 0; cc < BN; cc += 32) {
         uint32_t acc[32];
-        dev::tmem_ld32(t_row + c, acc);
+        dev::tmem_ld32(t_row + cc, acc);
         #pragma unroll
         for (int j = 0; j < 8; ++j)
           stage[lane * 8 + ((j + lane) & 7)] =
               make_float4(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]),
                           __uint_as_float(acc[4 * j + 2]), __uint_as_float(acc[4 * j + 3]));
         __syncwarp();
-        const int n = n0 + c + 4 * seg;
+        const int n = n0 + cc + 4 * seg;
         float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
         if (p.bias && n < p.N) bb = *reinterpret_cast<const float4*>(p.bias + n);
         // all eight loads of x first (the stores below could alias them as far
@@ -221,23 +113,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-    } else {
-      give_up(p, abort, 3);
     }
   }
-
-  dev::tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    dev::tc_fence_after();
-    dev::tmem_dealloc(tmem, 2 * BN);
-  }
+  gemm::teardown<BN>(c);
 }
 
 template <int BN>
 int launch_bn(const void* o, const void* w, const float* bias, float* x, int64_t M, int K, int N,
               float dt, float* v_out, cudaStream_t stream) {
-  using L = WoLayout<BN>;
+  using L = gemm::Layout<BN>;
   static bool attr_done[64] = {false};
   int dev_id = 0;
   SAVGB_CUDA(cudaGetDevice(&dev_id));
@@ -249,17 +133,17 @@ int launch_bn(const void* o, const void* w, const float* bias, float* x, int64_t
   CUtensorMap ma, mb;
   const uint64_t da[2] = {(uint64_t)K, (uint64_t)M};
   const uint64_t sa[1] = {(uint64_t)K * 2};
-  const uint32_t ba[2] = {kBK, 128};
+  const uint32_t ba[2] = {gemm::kBK, 128};
   int rc = encode_tiled(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o, da, sa, ba, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
   const uint64_t db[2] = {(uint64_t)K, (uint64_t)N};
-  const uint32_t bb[2] = {kBK, BN};
+  const uint32_t bb[2] = {gemm::kBK, BN};
   rc = encode_tiled(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, db, sa, bb, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
   WoParams p{(int)M, N, K, dt, bias, x, v_out, nullptr};
   if ((rc = error_word(&p.err))) return rc;
-  dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + kBM - 1) / kBM));
-  wo_euler_kernel<BN><<<grid, kThreads, L::kDynSmem, stream>>>(ma, mb, p);
+  dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + gemm::kBM - 1) / gemm::kBM));
+  wo_euler_kernel<BN><<<grid, gemm::kThreads, L::kDynSmem, stream>>>(ma, mb, p);
   SAVGB_CUDA(cudaGetLastError());
   return SAVGB_OK;
 }
@@ -272,7 +156,7 @@ int validate_out_proj(const void* o, const void* w, const float* bias, const flo
   if (!aligned16(o) || !aligned16(w) || !aligned16(x) || (bias && !aligned16(bias)) ||
       (v_out && !aligned16(v_out)))
     return fail(SAVGB_ERR_ALIGNMENT, "out_proj_euler_step: pointers must be 16-byte aligned");
-  if (M < 1 || M > ((int64_t)1 << 31) - 1 - kBM) return fail(SAVGB_ERR_INVALID_ARG, "out_proj_euler_step: M must be in [1, 2^31)");
+  if (M < 1 || M > ((int64_t)1 << 31) - 1 - gemm::kBM) return fail(SAVGB_ERR_INVALID_ARG, "out_proj_euler_step: M must be in [1, 2^31)");
   if (hid_in < 8 || hid_in % 8) return fail(SAVGB_ERR_INVALID_ARG, "out_proj_euler_step: hid_in must be a positive multiple of 8");
   if (hid_out < 16 || hid_out % 16) return fail(SAVGB_ERR_INVALID_ARG, "out_proj_euler_step: hid_out must be a positive multiple of 16");
   if (hid_in > (1 << 24) || hid_out > (1 << 24)) return fail(SAVGB_ERR_INVALID_ARG, "out_proj_euler_step: hidden size too large");

@@ -25,7 +25,7 @@ import numpy as np
 import torch
 
 # tensor kinds: part of each stream key
-KIND_Q, KIND_K, KIND_V, KIND_REF_K, KIND_REF_V, KIND_WO, KIND_X, KIND_BIAS = range(1, 9)
+KIND_Q, KIND_K, KIND_V, KIND_REF_K, KIND_REF_V, KIND_WO, KIND_X, KIND_BIAS, KIND_WQKV = range(1, 10)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -172,6 +172,11 @@ def boundary_kv(w: Workload, seed: int):
 def out_proj_weight(w: Workload, seed: int) -> torch.Tensor:
     """W_o, bf16 [hid_out][hid_in] ~ N(0, 1/hid)."""
     return normal_bf16((w.hid, w.hid), 1.0 / math.sqrt(w.hid), seed, KIND_WO)
+
+
+def qkv_weight(w: Workload, seed: int) -> torch.Tensor:
+    """W_qkv = [W_q; W_k; W_v], bf16 [3*hid][hid] ~ N(0, 1/hid)."""
+    return normal_bf16((3 * w.hid, w.hid), 1.0 / math.sqrt(w.hid), seed, KIND_WQKV)
 
 
 def state_x(w: Workload, seed: int) -> torch.Tensor:

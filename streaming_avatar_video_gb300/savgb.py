@@ -32,6 +32,7 @@ EXPORTS = (
     "chunk_stream_end_chunk", "chunk_stream_set_step_events", "chunk_stream_sync", "chunk_stream_info", "chunk_stream_export_state",
     "chunk_stream_import_state", "chunk_stream_destroy", "chunk_step_noalloc",
     "chunk_stream_istep", "chunk_stream_end_ichunk", "chunk_stream_ichunk_index", "chunk_attention_qrope",
+    "qkv_rope_project", "chunk_stream_block_step",
 )
 
 
@@ -50,7 +51,7 @@ class ChunkStreamConfig(ctypes.Structure):
                 ("grid_h", ctypes.c_int), ("grid_w", ctypes.c_int), ("ref_frames", ctypes.c_int),
                 ("boundary_frames", ctypes.c_int), ("ref_t", ctypes.c_int),
                 ("rope_base", ctypes.c_double), ("softmax_scale", ctypes.c_float),
-                ("interp_chunks", ctypes.c_int)]
+                ("interp_chunks", ctypes.c_int), ("qkv_block", ctypes.c_int)]
 
 
 _lib = None
@@ -84,6 +85,9 @@ def lib() -> ctypes.CDLL:
         "chunk_stream_step": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f, c_int]),
         "chunk_stream_end_chunk": (c_int, [c_vp]),
         "chunk_stream_istep": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f]),
+        "chunk_stream_block_step": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_f, c_int]),
+        "qkv_rope_project": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_i64, c_int, c_int, c_int, c_int, c_int,
+                                     c_int, c_d, c_vp]),
         "chunk_stream_end_ichunk": (c_int, [c_vp]),
         "chunk_stream_ichunk_index": (c_int, [c_vp, ctypes.POINTER(c_i64)]),
         "chunk_stream_set_step_events": (c_int, [c_vp, ctypes.POINTER(c_vp)]),
@@ -222,6 +226,22 @@ def chunk_attention_qrope(q: torch.Tensor, grid, segments: Sequence[Tuple[torch.
     return out
 
 
+def qkv_rope_project(x_bf16: torch.Tensor, w_qkv: torch.Tensor, grid, H: int, D: int, t0: int = 0,
+                     base: float = 10000.0, stream=None):
+    """q, k, v bf16 [B][N][H][D] = x W_qkv^T, q and k rotated (3D RoPE) in the
+    GEMM epilogue; x_bf16 [B][N][H*D], grid = (grid_t, grid_h, grid_w)."""
+    _need(x_bf16, "x_bf16", torch.bfloat16, 3)
+    _need(w_qkv, "w_qkv", torch.bfloat16, 2)
+    B, N, hid = x_bf16.shape
+    if hid != H * D or tuple(w_qkv.shape) != (3 * hid, hid):
+        raise ValueError("x must be [B][N][H*D] and w_qkv [3*H*D][H*D]")
+    q, k, v = (torch.empty((B, N, H, D), dtype=torch.bfloat16, device=x_bf16.device) for _ in range(3))
+    gt, gh, gw = grid
+    _check(lib().qkv_rope_project(x_bf16.data_ptr(), w_qkv.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), B, N,
+                                  H, D, gt, gh, gw, t0, float(base), _stream(stream)))
+    return q, k, v
+
+
 def out_proj_euler_step(o: torch.Tensor, w_o: torch.Tensor, x: torch.Tensor, dt: float,
                         bias: Optional[torch.Tensor] = None, v_out: Optional[torch.Tensor] = None,
                         stream=None) -> torch.Tensor:
@@ -260,9 +280,10 @@ class ChunkStream:
 
     def __init__(self, B: int, H: int, D: int, F: int, grid_h: int, grid_w: int, ref_frames: int = 1,
                  boundary_frames: int = 0, ref_t: int = -1, rope_base: float = 10000.0,
-                 softmax_scale: float = 0.0, stream=None, interp_chunks: bool = False):
+                 softmax_scale: float = 0.0, stream=None, interp_chunks: bool = False, qkv_block: bool = False):
         self.cfg = ChunkStreamConfig(B, H, D, F, grid_h, grid_w, ref_frames, boundary_frames, ref_t,
-                                     float(rope_base), float(softmax_scale), int(bool(interp_chunks)))
+                                     float(rope_base), float(softmax_scale), int(bool(interp_chunks)),
+                                     int(bool(qkv_block)))
         self.stream = _stream(stream)
         h = ctypes.c_void_p()
         _check(lib().chunk_stream_create(ctypes.byref(self.cfg), self.stream, ctypes.byref(h)))
@@ -311,6 +332,23 @@ class ChunkStream:
             _need(bias, "bias", torch.float32, 1)
         _check(lib().chunk_stream_istep(self.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(), w_o.data_ptr(),
                                         _ptr(bias), x.data_ptr(), float(dt)))
+
+    def block_step(self, w_qkv, w_o, x, dt: float, is_last_step: bool, bias=None) -> None:
+        """One denoising step through one DiT attention block: q, k, v are
+        projected from x itself (needs qkv_block)."""
+        c = self.cfg
+        hid = c.H * c.D
+        _need(w_qkv, "w_qkv", torch.bfloat16, 2)
+        _need(w_o, "w_o", torch.bfloat16, 2)
+        _need(x, "x", torch.float32)
+        if tuple(w_qkv.shape) != (3 * hid, hid) or tuple(w_o.shape) != (hid, hid):
+            raise ValueError("w_qkv must be [3*hid][hid] and w_o [hid][hid]")
+        if x.numel() != c.B * c.F * c.grid_h * c.grid_w * hid:
+            raise ValueError("x must be [B*N][hid]")
+        if bias is not None:
+            _need(bias, "bias", torch.float32, 1)
+        _check(lib().chunk_stream_block_step(self.handle, w_qkv.data_ptr(), w_o.data_ptr(), _ptr(bias), x.data_ptr(),
+                                             float(dt), int(bool(is_last_step))))
 
     def end_ichunk(self) -> None:
         _check(lib().chunk_stream_end_ichunk(self.handle))

@@ -519,3 +519,82 @@ def test_attention_qrope_parity(S, D, B, gt, gh, gw, t0, segs):
     want = O.attention(qq, osegs)
     got = f64(o) if rows is None else f64(o)[:, rows]
     assert_close(got, want, what=f"attention with RoPE of q inside (D={D})")
+
+
+# ------------------------------------------------------- DiT attention block
+
+@pytest.mark.parametrize("B,H,D,gt,gh,gw,t0", [
+    (1, 2, 64, 2, 4, 4, 0),     # tiny: 32 rows, 3*hid = 384 (128-column tiles)
+    (2, 2, 128, 3, 5, 7, 1),    # ragged: 210 rows over two batches, t0 = 1
+])
+def test_qkv_rope_project_parity(S, B, H, D, gt, gh, gw, t0):
+    N, hid = gt * gh * gw, H * D
+    x = torch.from_numpy(I.normal_f32((B, N, hid), 1.0, 50 + D, I.KIND_X))
+    xb = x.to(torch.bfloat16)
+    w = bf16((3 * hid, hid), 51, I.KIND_WQKV, std=1.0 / math.sqrt(hid))
+    q, k, v = S.qkv_rope_project(xb.cuda(), w.cuda(), (gt, gh, gw), H, D, t0=t0)
+    torch.cuda.synchronize()
+    S.savgb_device_check()
+    oq, ok_, ov = O.qkv_project(f64(xb).reshape(B * N, hid), f64(w), B, H, D)
+    assert_close(f64(q), O.rope3d(oq, gt, gh, gw, t0), what="q (rotated)")
+    assert_close(f64(k), O.rope3d(ok_, gt, gh, gw, t0), what="k (rotated)")
+    assert_close(f64(v), ov, what="v")
+
+
+def _block_workload():
+    return I.Workload("blk", B=1, H=4, D=64, F=3, grid_h=8, grid_w=8, ref_frames=1, boundary_frames=1, steps=2,
+                      shift=1.0)
+
+
+def test_stream_block_steps(S):
+    """Two chunks x two steps through one DiT attention block (q, k, v
+    projected from x): every chunk's x against the oracle."""
+    w = _block_workload()
+    seed = 12
+    rk, rv = I.reference_kv(w, seed)
+    wqkv, wo = I.qkv_weight(w, seed), I.out_proj_weight(w, seed)
+    dts = S.flow_time_grid(w.steps, w.shift)
+    cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                       w.rope_base, qkv_block=True)
+    cs.set_reference(rk.cuda(), rv.cuda())
+    xs = []
+    for c in range(2):
+        x = torch.from_numpy(I.normal_f32((w.B * w.n_q, w.hid), 1.0, seed, I.KIND_X, c)).cuda()
+        for s, dt in enumerate(dts):
+            cs.block_step(wqkv.cuda(), wo.cuda(), x, dt, s == len(dts) - 1)
+        cs.end_chunk()
+        xs.append(x.cpu())
+    cs.sync()
+    cs.close()
+    want = O.run_stream_block(w, f64(rk), f64(rv), f64(wqkv), f64(wo),
+                              lambda c: I.normal_f32((w.B * w.n_q, w.hid), 1.0, seed, I.KIND_X, c).astype(np.float64),
+                              O.time_grid(w.steps, w.shift), 2)
+    for c in range(2):
+        assert_close(f64(xs[c]), want[c], what=f"block chunk {c} x")
+
+
+def test_stream_block_full_base_sampled_rows(S):
+    """One base-shaped block step: sampled rows of x against the oracle
+    (projection of every token, attention for the sampled queries)."""
+    w = I.WORKLOADS["base"]
+    seed = 13
+    rk, rv = I.reference_kv(w, seed)
+    wqkv, wo = I.qkv_weight(w, seed), I.out_proj_weight(w, seed)
+    cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                       w.rope_base, qkv_block=True)
+    cs.set_reference(rk.cuda(), rv.cuda())
+    x0 = I.state_x(w, seed)
+    x = x0.cuda()
+    dt = S.flow_time_grid(w.steps, w.shift)[0]
+    cs.block_step(wqkv.cuda(), wo.cuda(), x, dt, False)
+    cs.sync()
+    got = x.cpu()
+    cs.close()
+    rows = np.unique(np.r_[np.random.default_rng(3).choice(w.n_q, 16, replace=False), [0, w.n_q - 1]])
+    q, k, v = O.qkv_project(f64(x0), f64(wqkv), w.B, w.H, w.D)
+    q_rot = O.rope3d(q, w.F, w.grid_h, w.grid_w, 0)[:, rows]
+    k_rot = O.rope3d(k, w.F, w.grid_h, w.grid_w, 0)
+    rk_rot = O.rope3d(f64(rk), 1, w.grid_h, w.grid_w, -1)
+    o = O.attention(q_rot, [(rk_rot, f64(rv)), (k_rot, v)])
+    want = O.euler_update(f64(x0)[rows], O.out_proj(o.reshape(len(rows), w.hid), f64(wo)), dt)
+    assert_close(f64(got)[rows], want, what="base block step x (sampled rows)")
