@@ -307,36 +307,69 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
 
 
 def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world):
-    """Same metric through ChunkStream.step with host buffers: every step copies
-    q, k, v from pinned host memory and reads x back into pinned memory."""
+    """Same metric through ChunkStream.step with host buffers.  Every step
+    uploads that step's q, k, v from pinned host memory and reads the updated
+    state x back into pinned host memory, all inside the timed region.  The
+    copies run on two copy streams: step i+1's inputs are uploaded into the
+    other half of a double buffer while step i computes, and step i's x is
+    snapshotted on the device and read back while step i+1 computes."""
     hsets = [tuple(t.pin_memory() for t in s) for s in sets]
-    dq, dk, dv = (torch.empty_like(t, device=dev) for t in sets[0])
+    dbuf = [tuple(torch.empty_like(t, device=dev) for t in sets[0]) for _ in range(2)]
+    x_stage = torch.empty_like(x)
     hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     n = max(3, min(args.steps, 60))
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    loaded = [ev(), ev()]
+    freed = [None, None]
+    staged_evt = [None]
+    out_done = [None]
     i0 = [0]
 
-    def step():
-        i = i0[0]
-        s = i % w.steps
+    def upload(i):
         hq, hk, hv = hsets[i & 1]
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        last = s == w.steps - 1
-        cs.step(dq, dk, dv, wo, x, dts[s], last)
+        with torch.cuda.stream(s_in):
+            if freed[i & 1] is not None:
+                s_in.wait_event(freed[i & 1])
+            for d, h in zip(dbuf[i & 1], (hq, hk, hv)):
+                d.copy_(h, non_blocking=True)
+            loaded[i & 1].record(s_in)
+
+    def step(i, upload_next=True):
+        if upload_next:
+            upload(i + 1)
+        s_idx = i % w.steps
+        last = s_idx == w.steps - 1
+        stream.wait_event(loaded[i & 1])
+        dq, dk, dv = dbuf[i & 1]
+        cs.step(dq, dk, dv, wo, x, dts[s_idx], last)
         if last:
             cs.end_chunk()
-        hx.copy_(x, non_blocking=True)
-        i0[0] = i + 1
+        freed[i & 1] = ev()
+        freed[i & 1].record(stream)
+        if out_done[0] is not None:
+            stream.wait_event(out_done[0])  # the previous snapshot has left the device
+        x_stage.copy_(x, non_blocking=True)
+        staged = ev()
+        staged.record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(staged)
+            hx.copy_(x_stage, non_blocking=True)
+            done = ev()
+            done.record(s_out)
+        out_done[0] = done
 
-    for _ in range(3):
-        step()
+    upload(0)
+    for i in range(3):
+        step(i)
     torch.cuda.synchronize()
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(n):
-        step()
+    base = 3
+    for i in range(base, base + n):
+        step(i, upload_next=True)
+    stream.wait_event(out_done[0])
     b.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(world, a.elapsed_time(b)) / n
@@ -344,7 +377,8 @@ def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world):
     d2h = x.numel() * x.element_size()
     return {"value": round(whole_job_rate(world, w.attn_flops(True), ms) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "api": "ChunkStream.step (C ABI chunk_stream_step) with pinned host q/k/v in, x out"}
+            "api": "ChunkStream.step (C ABI chunk_stream_step) with pinned host q/k/v in and x out; uploads of "
+                   "the next step and read-back of the previous one overlap the step on two copy streams"}
 
 
 def run_long(args, w: I.Workload, world: int, rank: int, local: int):
