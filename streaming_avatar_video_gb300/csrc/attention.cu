@@ -18,10 +18,12 @@
 // (setmaxnreg), so a thread holds a whole 128-column score row without spills.
 // TMEM columns: S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D,256+2D).
 // P (bf16) overwrites the first 64 columns of its S and feeds the PV product
-// straight from TMEM; each half of a row's probabilities is published as
-// soon as it is written, so PV over the first 64 keys overlaps the
-// exponentials of the last 64.  The two query tiles alternate so that the tensor core
+// straight from TMEM.  The two query tiles alternate so that the tensor core
 // works on one tile's QK^T / PV while the other tile's softmax runs.
+// tcgen05.mma issue is nearly synchronous with execution (the unit holds
+// about one instruction ahead), so every clock the issuing thread spends
+// between MMAs idles the tensor core: the issue loop has three wait points
+// per key tile (V and K together, P of tile 0, P of tile 1) and no other work.
 // The running max is updated lazily (only when it grows by more than 2^8 in
 // probability), and O is rescaled in TMEM by the softmax warps when it is.
 // Every wait is bounded; on a timeout the block records it in the device
@@ -92,9 +94,8 @@ struct Layout {
   static constexpr int kVFull = kKEmpty + KS;
   static constexpr int kVEmpty = kVFull + VS;
   static constexpr int kSFull = kVEmpty + VS;
-  static constexpr int kPLo = kSFull + 2;  // first 64 probabilities of a row written
-  static constexpr int kPHi = kPLo + 2;    // last 64 written
-  static constexpr int kODone = kPHi + 2;
+  static constexpr int kP = kSFull + 2;  // a tile's probabilities written to TMEM
+  static constexpr int kODone = kP + 2;
   static constexpr int kDrain = kODone + 2;
   static constexpr int kQReady = kDrain + 1;  // queries rotated in place (ROPE_Q)
   static constexpr int kNumBars = kQReady + 1;
@@ -211,8 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       dev::mbar_init(&bars[L::kSFull + x], 1);
-      dev::mbar_init(&bars[L::kPLo + x], 4);  // one elected lane per softmax warp
-      dev::mbar_init(&bars[L::kPHi + x], 4);
+      dev::mbar_init(&bars[L::kP + x], 4);  // one elected lane per softmax warp
       dev::mbar_init(&bars[L::kODone + x], 1);
     }
     dev::mbar_init(&bars[L::kDrain], 1);
@@ -330,40 +330,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool more = j + 1 < n;
           const int kst1 = (j + 1) % KS;
           const uint32_t kuse1 = (j + 1) / KS;
-          if (!dev::mbar_wait(&bars[L::kVFull + vst], vuse & 1, abort) ||
-              !dev::mbar_wait(&bars[L::kPLo + 0], j & 1, abort)) {
+          // V(j) and K(j+1) in one wait (both landed long before in steady state)
+          const bool kv_ok = more ? dev::mbar_wait2(&bars[L::kVFull + vst], vuse & 1, &bars[L::kKFull + kst1],
+                                                    kuse1 & 1, abort)
+                                  : dev::mbar_wait(&bars[L::kVFull + vst], vuse & 1, abort);
+          if (!kv_ok || !dev::mbar_wait(&bars[L::kP + 0], j & 1, abort)) {
             give_up(p, abort, 4);
             break;
           }
           dev::tc_fence_after();
-          issue_pv(0, vst, j > 0, 0, 4);
-          if (!dev::mbar_wait(&bars[L::kPHi + 0], j & 1, abort)) {
-            give_up(p, abort, 4);
-            break;
-          }
-          dev::tc_fence_after();
-          issue_pv(0, vst, j > 0, 4, 8);
+          issue_pv(0, vst, j > 0, 0, 8);
           if (more) {
-            if (!dev::mbar_wait(&bars[L::kKFull + kst1], kuse1 & 1, abort)) {
-              give_up(p, abort, 5);
-              break;
-            }
-            dev::tc_fence_after();
             issue_s(0, kst1);
             dev::mma_commit(&bars[L::kSFull + 0]);
           }
-          if (!dev::mbar_wait(&bars[L::kPLo + 1], j & 1, abort)) {
+          if (!dev::mbar_wait(&bars[L::kP + 1], j & 1, abort)) {
             give_up(p, abort, 6);
             break;
           }
           dev::tc_fence_after();
-          issue_pv(1, vst, j > 0, 0, 4);
-          if (!dev::mbar_wait(&bars[L::kPHi + 1], j & 1, abort)) {
-            give_up(p, abort, 6);
-            break;
-          }
-          dev::tc_fence_after();
-          issue_pv(1, vst, j > 0, 4, 8);
+          issue_pv(1, vst, j > 0, 0, 8);
           dev::mma_commit(&bars[L::kVEmpty + vst]);
           if (more) {
             issue_s(1, kst1);
@@ -485,11 +471,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[i] = dev::pack_bf16x2(p0, p1);
         }
         dev::tmem_st32(tS + half * 32, pk);
-        // publish this half: the PV product over its 64 keys may start
-        dev::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) dev::mbar_arrive(&bars[(half == 0 ? L::kPLo : L::kPHi) + x]);
       }
+      // publish the tile's probabilities: the PV product may start
+      dev::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(&bars[L::kP + x]);
       l += l0 + l1;
     }
     if (ok) ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kODone + x], 0, abort));

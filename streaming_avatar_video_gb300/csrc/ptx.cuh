@@ -50,6 +50,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Both phases complete?  The two probes are issued back to back, so their
+// latencies overlap.
+__device__ __forceinline__ bool mbar_try_wait2(uint64_t* bar_a, uint32_t parity_a, uint64_t* bar_b,
+                                               uint32_t parity_b) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred pa, pb;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 pa, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 pb, [%3], %4;\n\t"
+      "and.pred pa, pa, pb;\n\t"
+      "selp.u32 %0, 1, 0, pa;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar_a)), "r"(parity_a), "r"(smem_u32(bar_b)), "r"(parity_b)
+      : "memory");
+  return ok != 0;
+}
+
 // Default limit of every wait in the library's kernels.  No legitimate wait
 // comes near it; it only bounds a kernel whose partner stopped.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -68,6 +85,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// Waits for two phases (of two barriers); same limits as mbar_wait.
+__device__ __forceinline__ bool mbar_wait2(uint64_t* bar_a, uint32_t parity_a, uint64_t* bar_b, uint32_t parity_b,
+                                           volatile int* abort, uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait2(bar_a, parity_a, bar_b, parity_b)) return true;
+  return mbar_wait(bar_a, parity_a, abort, limit_ns) && mbar_wait(bar_b, parity_b, abort, limit_ns);
 }
 
 // ----------------------------------------------------------------------- TMA
