@@ -49,15 +49,8 @@ __device__ __forceinline__ void rotate_pair(uint32_t& packed, float2 cs) {
   packed = *reinterpret_cast<uint32_t*>(&r);
 }
 
-// grid: (token groups, B, tensors).  Each block builds the cos/sin tables of
-// the three axes in shared memory, then each warp takes whole tokens: the
-// token's (t, h, w) is decoded once and its H*D/8 vectors are streamed with
-// kRopeBatch loads in flight per lane.
-__global__ void __launch_bounds__(kRopeThreads) rope3d_kernel(const RopeKernelArgs a) {
-  extern __shared__ float2 tab[];
-  float2* tab_t = tab;
-  float2* tab_h = tab_t + a.gt * a.p_t;
-  float2* tab_w = tab_h + a.gh * a.p_h;
+// Builds the block's cos/sin tables of the three axes in shared memory.
+__device__ __forceinline__ void build_tables(float2* tab, const RopeKernelArgs& a) {
   const int n_t = a.gt * a.p_t, n_h = a.gh * a.p_h, n_w = a.gw * a.p_w;
   for (int i = threadIdx.x; i < n_t + n_h + n_w; i += blockDim.x) {
     int pos, j, P;
@@ -73,6 +66,18 @@ __global__ void __launch_bounds__(kRopeThreads) rope3d_kernel(const RopeKernelAr
     sincosf(static_cast<float>(pos) * omega, &s, &c);
     tab[i] = make_float2(c, s);
   }
+}
+
+// grid: (token groups, B, tensors).  Each block builds the cos/sin tables of
+// the three axes in shared memory, then each warp takes whole tokens: the
+// token's (t, h, w) is decoded once and its H*D/8 vectors are streamed with
+// kRopeBatch loads in flight per lane.  General shapes.
+__global__ void __launch_bounds__(kRopeThreads) rope3d_kernel(const RopeKernelArgs a) {
+  extern __shared__ float2 tab[];
+  float2* tab_t = tab;
+  float2* tab_h = tab_t + a.gt * a.p_t;
+  float2* tab_w = tab_h + a.gh * a.p_h;
+  build_tables(tab, a);
   __syncthreads();
 
   const int ti = blockIdx.z;
@@ -115,6 +120,70 @@ __global__ void __launch_bounds__(kRopeThreads) rope3d_kernel(const RopeKernelAr
         }
       }
     }
+  }
+}
+
+// Shapes whose token holds a whole number of warp-widths of 16-byte vectors
+// (vec_per_tok = 32*upl, upl <= kRopeFastMax) and whose head holds a divisor
+// of 32 vectors: lane L then always meets the same four channel pairs
+// ((L mod D/8)*4 ...), so it looks its four (cos, sin) up once per token and
+// applies them to all upl of its vectors.  A warp's first token is loaded
+// before the block builds its tables, so the table work overlaps that load.
+constexpr int kRopeFastMax = 12;
+
+__global__ void __launch_bounds__(kRopeThreads) rope3d_fast_kernel(const RopeKernelArgs a) {
+  extern __shared__ float2 tab[];
+  const int ti = blockIdx.z;
+  const int b = blockIdx.y;
+  const uint4* __restrict__ in = (ti == 0 ? a.t[0].in : a.t[1].in) + b * (ti == 0 ? a.t[0].in_bs : a.t[1].in_bs);
+  uint4* __restrict__ out = (ti == 0 ? a.t[0].out : a.t[1].out) + b * (ti == 0 ? a.t[0].out_bs : a.t[1].out_bs);
+  const int lane = threadIdx.x & 31;
+  const int vpt = a.vec_per_tok;
+  const int upl = vpt >> 5;
+  const int stride = gridDim.x * kRopeWarps;
+  int n = blockIdx.x * kRopeWarps + (threadIdx.x >> 5);
+  uint4 v[kRopeFastMax];
+  auto load = [&](int tok) {
+    const uint4* src = in + static_cast<int64_t>(tok) * vpt + lane;
+    #pragma unroll
+    for (int u = 0; u < kRopeFastMax; ++u)
+      if (u < upl) v[u] = __ldcs(src + 32 * u);
+  };
+  if (n < a.n_tokens) load(n);
+  build_tables(tab, a);
+  __syncthreads();
+
+  const float2* tab_t = tab;
+  const float2* tab_h = tab_t + a.gt * a.p_t;
+  const float2* tab_w = tab_h + a.gh * a.p_h;
+  const int hw = a.gh * a.gw;
+  const int ph_end = a.p_t + a.p_h;
+  const int p0 = (lane % a.vec_per_head) * 4;
+  for (; n < a.n_tokens; n += stride) {
+    const int tt = n / hw;
+    const int r2 = n - tt * hw;
+    const int hh = r2 / a.gw;
+    const int ww = r2 - hh * a.gw;
+    float2 cs[4];
+    #pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int p_ = p0 + q;
+      cs[q] = p_ < a.p_t ? tab_t[tt * a.p_t + p_]
+                         : (p_ < ph_end ? tab_h[hh * a.p_h + p_ - a.p_t] : tab_w[ww * a.p_w + p_ - ph_end]);
+    }
+    uint4* dst = out + static_cast<int64_t>(n) * vpt + lane;
+    #pragma unroll
+    for (int u = 0; u < kRopeFastMax; ++u) {
+      if (u < upl) {
+        uint32_t w0 = v[u].x, w1 = v[u].y, w2 = v[u].z, w3 = v[u].w;
+        rotate_pair(w0, cs[0]);
+        rotate_pair(w1, cs[1]);
+        rotate_pair(w2, cs[2]);
+        rotate_pair(w3, cs[3]);
+        __stcs(dst + 32 * u, make_uint4(w0, w1, w2, w3));
+      }
+    }
+    if (n + stride < a.n_tokens) load(n + stride);
   }
 }
 
@@ -172,23 +241,27 @@ static int launch_rope_multi(const RopeArgs* args, int n, cudaStream_t stream) {
   axis_split(a.D, &k.p_t, &k.p_h, &k.p_w);
   k.log2_base = (float)std::log2(a.base);
   const size_t smem = table_bytes(a);
+  const bool fast = k.vec_per_tok % 32 == 0 && k.vec_per_tok / 32 <= kRopeFastMax && 32 % k.vec_per_head == 0;
+  auto* kern = fast ? rope3d_fast_kernel : rope3d_kernel;
   static bool attr_done[64] = {false};
   int dev_id = 0;
   SAVGB_CUDA(cudaGetDevice(&dev_id));
   if (!attr_done[dev_id & 63]) {
     SAVGB_CUDA(cudaFuncSetAttribute(rope3d_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     kRopeMaxTableBytes));
+    SAVGB_CUDA(cudaFuncSetAttribute(rope3d_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kRopeMaxTableBytes));
     attr_done[dev_id & 63] = true;
   }
   // one wave: as many blocks as fit on the device at once, over all (batch, tensor) pairs
   int occ = 0;
-  SAVGB_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rope3d_kernel, kRopeThreads, smem));
+  SAVGB_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kRopeThreads, smem));
   if (occ < 1) occ = 1;
   const int groups = (k.n_tokens + kRopeWarps - 1) / kRopeWarps;
   int per = occ * sms / (a.B * n);
   if (per < 1) per = 1;
   dim3 grid((unsigned)(groups < per ? groups : per), (unsigned)a.B, (unsigned)n);
-  rope3d_kernel<<<grid, kRopeThreads, smem, stream>>>(k);
+  kern<<<grid, kRopeThreads, smem, stream>>>(k);
   SAVGB_CUDA(cudaGetLastError());
   return SAVGB_OK;
 }
