@@ -42,6 +42,10 @@ def rows_of(t, rows):
     (2, 3, 5, 7, 3, 128, -2),    # ragged grid, B = 2, negative start
     (1, 4, 16, 16, 8, 64, 0),    # small chunk
     (1, 8, 30, 52, 24, 128, 0),  # base-DiT chunk, every element
+    (2, 2, 3, 5, 2, 128, 0),     # 32 vectors a token: one per lane (lane-invariant path), B = 2
+    (1, 2, 3, 4, 1, 256, 3),     # D = 256: a head is a whole warp-width of vectors
+    (1, 1, 2, 3, 48, 128, 0),    # 768 vectors a token: general path, three batches a token
+    (2, 2, 2, 2, 32, 40, -3),    # D/8 = 5 does not divide 32: general path
 ])
 def test_rope3d_parity(S, B, gt, gh, gw, H, D, t0):
     N = gt * gh * gw
@@ -239,6 +243,24 @@ def test_stream_small_pair(S):
     inf = cs.info()
     assert inf["chunk_index"] == 2 and inf["boundary_tokens"] == w.n_b
     cs.close()
+
+
+def test_stream_two_sessions_ragged_blocks(S):
+    """B = 2 sessions of 1100 queries: the 256-row tiles of the W_o GEMM
+    straddle the sessions and the last 256-query attention block of each
+    session is ragged.  Two chunks x 3 steps against the oracle, and a second
+    run that must reproduce the first bit for bit."""
+    w = I.Workload("straddle", B=2, H=4, D=128, F=5, grid_h=10, grid_w=22, ref_frames=1,
+                   boundary_frames=1, steps=3, shift=1.0)
+    cs, xs, _ = run_stream_gpu(S, w, 3, 2)
+    cs.close()
+    want, _ = run_stream_oracle(w, 3, 2)
+    for c in range(2):
+        assert_close(f64(xs[c]), want[c], what=f"two-session chunk {c} x")
+    cs2, xs2, _ = run_stream_gpu(S, w, 3, 2)
+    cs2.close()
+    for c in range(2):
+        assert torch.equal(xs[c], xs2[c]), f"chunk {c}: rerun differs"
 
 
 def test_stream_export_import_resume(S):
