@@ -394,6 +394,69 @@ def test_stream_step_full_size_sampled_rows(S, name):
     assert_close(f64(got)[rows], want, what=f"{name} step x (sampled rows)")
 
 
+def _stream_sampled_rows(S, w, seed, chunk_dts, rows, check_chunks):
+    """Runs the chunks through chunk_stream_step (chunk c takes the steps
+    chunk_dts[c]; the last step of every chunk rolls the boundary) and replays
+    them on the oracle for the sampled query rows of every session, over every
+    key and head.  Compares x after each chunk in check_chunks."""
+    rk, rv = I.reference_kv(w, seed)
+    wo = I.out_proj_weight(w, seed)
+    cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                       w.rope_base)
+    cs.set_reference(rk.cuda(), rv.cuda())
+    dwo = wo.cuda()
+    rk_rot = O.rope3d(f64(rk), w.ref_frames, w.grid_h, w.grid_w, w.ref_t, w.rope_base)
+    segs_ref = (rk_rot, f64(rv))
+    bnd = None
+    x_rows_of = [b * w.n_q + rows for b in range(w.B)]
+    for c, dts in enumerate(chunk_dts):
+        x0 = I.normal_f32((w.B * w.n_q, w.hid), 1.0, seed, I.KIND_X, c)
+        x = torch.from_numpy(x0).cuda()
+        want = np.concatenate([x0[r] for r in x_rows_of]).astype(np.float64).reshape(w.B, len(rows), w.hid)
+        last_kv = None
+        for s_, dt in enumerate(dts):
+            st = I.step_inputs(w, seed, c, s_)
+            cs.step(st.q.cuda(), st.k.cuda(), st.v.cuda(), dwo, x, dt, s_ == len(dts) - 1)
+            q_rot = O.rope3d(f64(st.q), w.F, w.grid_h, w.grid_w, 0, w.rope_base)[:, rows]
+            k_rot = O.rope3d(f64(st.k), w.F, w.grid_h, w.grid_w, 0, w.rope_base)
+            segs = [segs_ref] + ([bnd] if bnd is not None else []) + [(k_rot, f64(st.v))]
+            o = O.attention(q_rot, segs)
+            for b in range(w.B):
+                want[b] = O.euler_update(want[b], O.out_proj(o[b].reshape(len(rows), w.hid), f64(wo)), dt)
+            last_kv = (st.k, st.v)
+        cs.end_chunk()
+        cs.sync()
+        if c in check_chunks:
+            got = x.cpu()
+            for b in range(w.B):
+                assert_close(f64(got)[x_rows_of[b]], want[b], what=f"{w.name} chunk {c} session {b} x (sampled rows)")
+        bnd = O.boundary_from_chunk(f64(last_kv[0]), f64(last_kv[1]), w.frame_tokens, w.boundary_frames,
+                                    w.grid_h, w.grid_w, w.rope_base)
+    cs.close()
+
+
+def test_stream_sr_chunk_all_steps_sampled_rows(S):
+    """The SR-shaped workload as configured: a chunk of 8 uniform Euler steps
+    (after a one-step chunk that supplies the boundary), sampled rows of x
+    after all 8 steps."""
+    w = I.WORKLOADS["sr"]
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([rng.choice(w.n_q, 12, replace=False), [0, 256, w.n_q - 1]]))
+    _stream_sampled_rows(S, w, 7, [[1.0], list(S.flow_time_grid(w.steps, w.shift))], rows, {1})
+
+
+def test_stream_long_sessions_sampled_rows(S):
+    """The long-session workload's shape: 4 batched sessions of base-DiT
+    chunks, 3 consecutive chunks (2 shifted steps each here) so that the
+    boundary rolls twice; sampled rows of every session's x."""
+    w = I.WORKLOADS["long"]
+    assert w.B == 4
+    rng = np.random.default_rng(4)
+    rows = np.unique(np.concatenate([rng.choice(w.n_q, 10, replace=False), [0, w.n_q - 1]]))
+    dts = list(S.flow_time_grid(2, w.shift))
+    _stream_sampled_rows(S, w, 8, [dts, dts, dts], rows, {1, 2})
+
+
 # ---------------------------------------------------- interpolation chunks
 
 def _ni_workload(D):
