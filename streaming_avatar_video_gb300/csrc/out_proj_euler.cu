@@ -12,9 +12,10 @@
 // every B (W_o) tile, so each byte fed from L2 does twice the work of a
 // 128-row tile.  bf16 operands sit in 128-byte-swizzled shared memory fed by
 // TMA through a 3-stage ring; the fp32 accumulators live in TMEM.  The
-// epilogue reads them back, turns each 32 x 32 chunk around in shared memory
-// and applies the Euler update to x (fp32, read-modify-write) with coalesced
-// 128-byte row segments, so v never goes through global memory.
+// epilogue stages x through the (then idle) ring with tensor-map loads and
+// stores, 32 x 32 fp32 chunks, several in flight per warp, and each thread
+// applies the Euler update to its row with v straight from its TMEM lane, so
+// v never goes through global memory.
 // The mainloop (TMA producer, MMA issue, TMEM) is the shared 256-row GEMM of
 // gemm_tc.cuh; warps 4-11 run the Euler epilogue.
 #include <cuda_bf16.h>
@@ -35,10 +36,18 @@ struct WoParams {
   DeviceErrorWord* err;
 };
 
+constexpr int kXChunk = 32;                   // columns of x per staged chunk
+constexpr int kXChunkBytes = 32 * kXChunk * 4;  // a warp's 32 rows x 32 fp32 columns
+constexpr int kXBufs = 4;                       // chunks of x in flight per warp
+
 template <int BN>
 __global__ void __launch_bounds__(gemm::kThreads, 1)
     wo_euler_kernel(const __grid_constant__ CUtensorMap map_a,
-                    const __grid_constant__ CUtensorMap map_b, const WoParams p) {
+                    const __grid_constant__ CUtensorMap map_b,
+                    const __grid_constant__ CUtensorMap map_x, const WoParams p) {
+  using L = gemm::Layout<BN>;
+  static_assert(8 * kXBufs * kXChunkBytes <= L::kBar, "x staging must fit in the operand ring");
+  static_assert(8 * kXBufs * 8 <= 1024, "x barriers must fit in the epilogue's shared memory");
   extern __shared__ uint8_t smem_raw[];
   const gemm::Ctx c = gemm::setup<BN>(smem_raw, &map_a, &map_b);
   const int warp = threadIdx.x >> 5;
@@ -53,9 +62,8 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
     if (lane == 0) gemm::mma<BN>(c, kb_count, p.err, kErrGemmWait);
   } else if (warp >= 4) {
     // epilogue: warps 4-7 take rows 0-127 (accumulator columns [0, BN)),
-    // warps 8-11 rows 128-255 ([BN, 2 BN)).  Each 32-row x 32-column chunk is
-    // loaded from TMEM (one row per lane), turned around in shared memory and
-    // applied to x with 8 lanes per 128-byte row segment (coalesced).
+    // warps 8-11 rows 128-255 ([BN, 2 BN)); a warp's 32 rows are its TMEM
+    // lane quadrant, one row per lane.
     const int half = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int row_base = m0 + half * 128 + quad * 32;
@@ -65,8 +73,76 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
       const int ncols = min(BN, p.N - n0);
       if (m < p.M && ncols > 0) dev::prefetch_l2(p.x + static_cast<int64_t>(m) * p.N + n0, ncols * 4);
     }
-    if (gemm::wait_acc(c, p.err, kErrGemmWait)) {
-      // the operand ring is idle once every MMA has completed: 4 KiB per warp
+    if (p.v_out == nullptr) {
+      // x in 32 x 32 fp32 chunks staged by tensor-map loads in the idle
+      // operand ring (128-byte swizzled, kXBufs in flight per warp); thread =
+      // row: it adds dt * (v + bias) to its row of the chunk in place, taking
+      // v straight from its TMEM lane, and a tensor-map store writes the
+      // chunk back.  The loads hit L2 (x was prefetched during the MMAs).
+      uint8_t* xb = c.smem + (warp - 4) * (kXBufs * kXChunkBytes);
+      uint64_t* xbar = reinterpret_cast<uint64_t*>(c.smem + L::kExtra) + (warp - 4) * kXBufs;
+      if (lane == 0) {
+        dev::tma_prefetch_desc(&map_x);
+        for (int i = 0; i < kXBufs; ++i) dev::mbar_init(&xbar[i], 1);
+        dev::fence_barrier_init();
+      }
+      __syncwarp();
+      const int nch = (min(BN, p.N - n0) + kXChunk - 1) / kXChunk;
+      if (gemm::wait_acc(c, p.err, kErrGemmWait) && row_base < p.M) {
+        if (lane == 0)
+          for (int i = 0; i < kXBufs && i < nch; ++i) {
+            dev::mbar_arrive_expect_tx(&xbar[i], kXChunkBytes);
+            dev::tma_load_2d(xb + i * kXChunkBytes, &map_x, &xbar[i], n0 + i * kXChunk, row_base);
+          }
+        const uint32_t t_row = c.tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * BN;
+        const float dt = p.dt;
+        #pragma unroll 1
+        for (int cc = 0; cc < nch; ++cc) {
+          const int bi = cc % kXBufs;
+          uint32_t acc[32];
+          dev::tmem_ld32(t_row + cc * kXChunk, acc);
+          bool got = true;
+          if (lane == 0) got = dev::mbar_wait(&xbar[bi], (cc / kXBufs) & 1, c.abort);
+          if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
+            gemm::give_up(p.err, c.abort, kErrGemmWait, 4);
+            break;
+          }
+          float4* row = reinterpret_cast<float4*>(xb + bi * kXChunkBytes + lane * 128);
+          const int ncol0 = n0 + cc * kXChunk;
+          #pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (p.bias && ncol0 + 4 * j < p.N) bb = *reinterpret_cast<const float4*>(p.bias + ncol0 + 4 * j);
+            float4* cell = row + (j ^ (lane & 7));
+            float4 y = *cell;
+            y.x = fmaf(dt, __uint_as_float(acc[4 * j]) + bb.x, y.x);
+            y.y = fmaf(dt, __uint_as_float(acc[4 * j + 1]) + bb.y, y.y);
+            y.z = fmaf(dt, __uint_as_float(acc[4 * j + 2]) + bb.z, y.z);
+            y.w = fmaf(dt, __uint_as_float(acc[4 * j + 3]) + bb.w, y.w);
+            *cell = y;
+          }
+          dev::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            dev::tma_store_2d(&map_x, xb + bi * kXChunkBytes, ncol0, row_base);
+            dev::bulk_commit();
+            if (cc + kXBufs < nch) {
+              // the buffer is reloaded once its store has read it
+              dev::bulk_wait_read_all();
+              dev::mbar_arrive_expect_tx(&xbar[bi], kXChunkBytes);
+              dev::tma_load_2d(xb + bi * kXChunkBytes, &map_x, &xbar[bi], n0 + (cc + kXBufs) * kXChunk,
+                               row_base);
+            }
+          }
+        }
+        if (lane == 0) dev::bulk_wait_all();
+        __syncwarp();
+      }
+    } else if (gemm::wait_acc(c, p.err, kErrGemmWait)) {
+      // with the velocity written out too (a debugging aid): each 32 x 32
+      // chunk is turned around in shared memory and applied to x and v_out
+      // with coalesced 128-byte row segments.  The operand ring is idle once
+      // every MMA has completed: 4 KiB per warp
       float4* stage = reinterpret_cast<float4*>(c.smem + (warp - 4) * 4096);
       const uint32_t t_row = c.tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * BN;
       const float dt = p.dt;
@@ -140,10 +216,16 @@ int launch_bn(const void* o, const void* w, const float* bias, float* x, int64_t
   const uint32_t bb[2] = {gemm::kBK, BN};
   rc = encode_tiled(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, db, sa, bb, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
+  CUtensorMap mx;
+  const uint64_t dx[2] = {(uint64_t)N, (uint64_t)M};
+  const uint64_t sx[1] = {(uint64_t)N * 4};
+  const uint32_t bx[2] = {kXChunk, 32};
+  rc = encode_tiled(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, x, dx, sx, bx, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
   WoParams p{(int)M, N, K, dt, bias, x, v_out, nullptr};
   if ((rc = error_word(&p.err))) return rc;
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + gemm::kBM - 1) / gemm::kBM));
-  wo_euler_kernel<BN><<<grid, gemm::kThreads, L::kDynSmem, stream>>>(ma, mb, p);
+  wo_euler_kernel<BN><<<grid, gemm::kThreads, L::kDynSmem, stream>>>(ma, mb, mx, p);
   SAVGB_CUDA(cudaGetLastError());
   return SAVGB_OK;
 }
