@@ -8,7 +8,11 @@
 // trained with flow matching; section "The streaming framework and pipeline
 // loop": a multi-step diffusion pass per chunk).
 //
-// One CTA computes a 256 x BN tile of v: two 128-row tcgen05.mma halves share
+// Two kernels.  When only x is updated and the output width is a multiple of
+// 256, a persistent CTA-pair kernel (below) computes 256 x 256 tiles with
+// double-buffered accumulators, so each tile's Euler epilogue overlaps the
+// next tile's MMAs.  Otherwise (other widths, or the velocity also written
+// out) one CTA computes a 256 x BN tile of v: two 128-row tcgen05.mma halves share
 // every B (W_o) tile, so each byte fed from L2 does twice the work of a
 // 128-row tile.  bf16 operands sit in 128-byte-swizzled shared memory fed by
 // TMA through a 3-stage ring; the fp32 accumulators live in TMEM.  The
@@ -19,6 +23,8 @@
 // The mainloop (TMA producer, MMA issue, TMEM) is the shared 256-row GEMM of
 // gemm_tc.cuh; warps 4-11 run the Euler epilogue.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "common.h"
 #include "gemm_tc.cuh"
@@ -194,6 +200,288 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
   gemm::teardown<BN>(c);
 }
 
+// ------------------------------------------------------------ CTA-pair kernel
+// Persistent CTA-pair GEMM: a cluster of two CTAs computes 256 x 256 tiles of
+// v with tcgen05.mma.cta_group::2 (M = 256: each CTA holds 128 rows of O and
+// 128 of the 256 rows of the W_o tile).  Each CTA keeps two 128 x 256 fp32
+// accumulators in TMEM, so the Euler epilogue of one tile (x through the
+// shared-memory chunk staging above) runs while the next tile's MMAs
+// accumulate into the other buffer, and the x read-modify-write traffic no
+// longer idles the tensor cores.
+//   warp 0      TMA producer of this CTA's A rows and B half (6-stage ring)
+//   warp 1      TMEM allocation (both CTAs); lane 0 of the even CTA issues
+//               every MMA and commits to both CTAs' barriers
+//   warp 2      (odd CTA) relays "stage full" to the even CTA's barrier
+//   warps 4-11  epilogue: warp -> 32 rows (its TMEM lane quadrant) x 128
+//               columns (one half of the tile)
+namespace pair {
+constexpr int kThreads = 384;
+constexpr int kBK = 64;
+constexpr int kStages = 6;
+constexpr int kABytes = 128 * kBK * 2;  // 16 KiB: this CTA's 128 rows of O
+constexpr int kBBytes = 128 * kBK * 2;  // 16 KiB: this CTA's 128 rows of the W_o tile
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kPairXBufs = 1;
+constexpr int kXStage = kStages * kStageBytes;
+constexpr int kBar = kXStage + 8 * kPairXBufs * kXChunkBytes;
+constexpr int kFull = 0, kEmpty = kStages, kAccFull = 2 * kStages, kAccEmpty = kAccFull + 2, kDrain = kAccEmpty + 2;
+constexpr int kXBar = kDrain + 1;
+constexpr int kNumBars = kXBar + 8 * kPairXBufs;
+constexpr int kMisc = kBar + kNumBars * 8;
+constexpr int kDynSmem = kMisc + 16 + 1024;
+static_assert(kDynSmem <= 227 * 1024, "shared memory budget");
+
+__device__ __forceinline__ void give_up(const WoParams& p, volatile int* abort, unsigned code) {
+  if (atomicExch(const_cast<int*>(abort), 1) == 0) {
+    atomicOr(&p.err->flags, kErrGemmWait);
+    atomicCAS(&p.err->where, 0u, code);
+  }
+}
+}  // namespace pair
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
+    wo_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   const __grid_constant__ CUtensorMap map_x, const WoParams p, int n_tiles_n, int n_tiles) {
+  using namespace pair;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = dev::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + kMisc + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = dev::cluster_rank();
+  const bool leader = rank == 0;
+  const int cluster = static_cast<int>(blockIdx.x >> 1);
+  const int n_clusters = static_cast<int>(gridDim.x >> 1);
+  const int kb_count = (p.K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      dev::mbar_init(&bars[kFull + s], leader ? 2 : 1);  // the even CTA's: its own load + the odd CTA's relay
+      dev::mbar_init(&bars[kEmpty + s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      dev::mbar_init(&bars[kAccFull + b], 1);
+      dev::mbar_init(&bars[kAccEmpty + b], 16);  // the 8 epilogue warps of both CTAs (even CTA's copy)
+    }
+    dev::mbar_init(&bars[kDrain], 1);
+    for (int i = 0; i < 8 * kPairXBufs; ++i) dev::mbar_init(&bars[kXBar + i], 1);
+    *abort = 0;
+    dev::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    dev::tma_prefetch_desc(&map_a);
+    dev::tma_prefetch_desc(&map_b);
+    dev::tma_prefetch_desc(&map_x);
+  }
+  __syncthreads();
+  dev::cluster_sync();  // both CTAs' barriers exist before any remote arrive
+  if (warp == 1) {
+    dev::tmem_alloc_pair(tmem_slot, 512);
+    dev::tmem_relinquish_pair();
+  }
+  dev::tc_fence_before();
+  __syncthreads();
+  dev::cluster_sync();
+  dev::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = cluster; t < n_tiles && ok; t += n_clusters) {
+        const int m0 = (t / n_tiles_n) * 256 + static_cast<int>(rank) * 128;
+        const int nb = (t % n_tiles_n) * 256 + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < kb_count; ++kb, ++it) {
+          const int st = static_cast<int>(it % kStages);
+          const uint32_t use = it / kStages;
+          if (use > 0 && !dev::mbar_wait(&bars[kEmpty + st], (use - 1) & 1, abort)) {
+            give_up(p, abort, 11);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + st * kStageBytes;
+          dev::mbar_arrive_expect_tx(&bars[kFull + st], kStageBytes);
+          dev::tma_load_2d(sa, &map_a, &bars[kFull + st], kb * kBK, m0);
+          dev::tma_load_2d(sa + kABytes, &map_b, &bars[kFull + st], kb * kBK, nb);
+        }
+      }
+      // every issued copy has landed in this CTA before it may exit
+      volatile int never = 0;
+      const uint32_t first = it > static_cast<uint32_t>(kStages) ? it - kStages : 0;
+      for (uint32_t t = first; t < it; ++t) {
+        if (leader) dev::mbar_wait_cluster(&bars[kFull + t % kStages], (t / kStages) & 1, &never);
+        else dev::mbar_wait(&bars[kFull + t % kStages], (t / kStages) & 1, &never);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = dev::idesc_bf16_f32(256, 256, false, false);
+      const uint64_t d0 = dev::sdesc_sw128(dev::smem_u32(smem), 16, 1024);
+      uint32_t it = 0;
+      int tile_i = 0;
+      bool ok = true;
+      for (int t = cluster; t < n_tiles && ok; t += n_clusters, ++tile_i) {
+        const int buf = tile_i & 1;
+        const uint32_t buse = static_cast<uint32_t>(tile_i >> 1);
+        if (buse > 0 && !dev::mbar_wait_cluster(&bars[kAccEmpty + buf], (buse - 1) & 1, abort)) {
+          give_up(p, abort, 12);
+          break;
+        }
+        dev::tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(buf * 256);
+        for (int kb = 0; kb < kb_count; ++kb, ++it) {
+          const int st = static_cast<int>(it % kStages);
+          if (!dev::mbar_wait(&bars[kFull + st], (it / kStages) & 1, abort)) {
+            give_up(p, abort, 13);
+            ok = false;
+            break;
+          }
+          dev::tc_fence_after();
+          const uint64_t ds = d0 + static_cast<uint32_t>((st * kStageBytes) >> 4);
+          #pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint32_t koff = (k * 32) >> 4;
+            dev::mma_ss_pair(d, ds + koff, ds + ((kABytes >> 4) + koff), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          dev::mma_commit_pair(&bars[kEmpty + st], 3);
+        }
+        if (ok) dev::mma_commit_pair(&bars[kAccFull + buf], 3);
+      }
+      // every MMA has completed before TMEM is released
+      dev::mma_commit_pair(&bars[kDrain], 1);
+      volatile int never = 0;
+      dev::mbar_wait(&bars[kDrain], 0, &never);
+    }
+  } else if (warp == 2) {
+    if (lane == 0 && !leader) {
+      // ----------------------------------------------- relay (odd CTA only)
+      const uint32_t full0 = dev::mapa_shared(&bars[kFull], 0);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = cluster; t < n_tiles && ok; t += n_clusters) {
+        for (int kb = 0; kb < kb_count; ++kb, ++it) {
+          const int st = static_cast<int>(it % kStages);
+          if (!dev::mbar_wait(&bars[kFull + st], (it / kStages) & 1, abort)) {
+            give_up(p, abort, 14);
+            ok = false;
+            break;
+          }
+          // relaxed: the TMA completion just observed already placed the
+          // data; a release arrive at cluster scope held this thread ~0.8 us
+          // per stage and throttled the whole pipeline to half speed
+          dev::mbar_arrive_cluster_relaxed(full0 + static_cast<uint32_t>(st * 8));
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 4;
+    const int quad = warp & 3;
+    const int ch = ew >> 2;
+    uint8_t* xb = smem + kXStage + ew * (kPairXBufs * kXChunkBytes);
+    uint64_t* xbar = &bars[kXBar + ew * kPairXBufs];
+    const uint32_t acc_empty0 = dev::mapa_shared(&bars[kAccEmpty], 0);
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const float dt = p.dt;
+    uint32_t xwaits[kPairXBufs] = {};
+    int tile_i = 0;
+    for (int t = cluster; t < n_tiles; t += n_clusters, ++tile_i) {
+      const int buf = tile_i & 1;
+      const int row_base = (t / n_tiles_n) * 256 + static_cast<int>(rank) * 128 + quad * 32;
+      const int ncol0 = (t % n_tiles_n) * 256 + ch * 128;
+      {
+        // pull this warp's rows of x for the tile into L2 while the MMAs run
+        const int m = row_base + lane;
+        const int ncols = min(128, p.N - ncol0);
+        if (m < p.M && ncols > 0) dev::prefetch_l2(p.x + static_cast<int64_t>(m) * p.N + ncol0, ncols * 4);
+      }
+      bool got = true;
+      if (lane == 0) got = dev::mbar_wait_cluster(&bars[kAccFull + buf], (tile_i >> 1) & 1, abort);
+      if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
+        give_up(p, abort, 15);
+        break;
+      }
+      dev::tc_fence_after();
+      const int nch = row_base < p.M ? max(0, (min(128, p.N - ncol0) + kXChunk - 1) / kXChunk) : 0;
+      if (lane == 0)
+        for (int i = 0; i < kPairXBufs && i < nch; ++i) {
+          dev::mbar_arrive_expect_tx(&xbar[i], kXChunkBytes);
+          dev::tma_load_2d(xb + i * kXChunkBytes, &map_x, &xbar[i], ncol0 + i * kXChunk, row_base);
+        }
+      bool ok = true;
+      #pragma unroll 1
+      for (int cc = 0; cc < nch; ++cc) {
+        const int bi = cc % kPairXBufs;
+        uint32_t acc[32];
+        dev::tmem_ld32(t_lane + static_cast<uint32_t>(buf * 256 + ch * 128 + cc * kXChunk), acc);
+        bool xg = true;
+        if (lane == 0) xg = dev::mbar_wait(&xbar[bi], xwaits[bi] & 1, abort);
+        ++xwaits[bi];
+        if (__shfl_sync(0xffffffffu, xg ? 1 : 0, 0) == 0) {
+          give_up(p, abort, 16);
+          ok = false;
+          break;
+        }
+        float4* row = reinterpret_cast<float4*>(xb + bi * kXChunkBytes + lane * 128);
+        const int n = ncol0 + cc * kXChunk;
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (p.bias && n + 4 * j < p.N) bb = *reinterpret_cast<const float4*>(p.bias + n + 4 * j);
+          float4* cell = row + (j ^ (lane & 7));
+          float4 y = *cell;
+          y.x = fmaf(dt, __uint_as_float(acc[4 * j]) + bb.x, y.x);
+          y.y = fmaf(dt, __uint_as_float(acc[4 * j + 1]) + bb.y, y.y);
+          y.z = fmaf(dt, __uint_as_float(acc[4 * j + 2]) + bb.z, y.z);
+          y.w = fmaf(dt, __uint_as_float(acc[4 * j + 3]) + bb.w, y.w);
+          *cell = y;
+        }
+        dev::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          dev::tma_store_2d(&map_x, xb + bi * kXChunkBytes, n, row_base);
+          dev::bulk_commit();
+          if (cc + kPairXBufs < nch) {
+            dev::bulk_wait_read_all();
+            dev::mbar_arrive_expect_tx(&xbar[bi], kXChunkBytes);
+            dev::tma_load_2d(xb + bi * kXChunkBytes, &map_x, &xbar[bi], n + kPairXBufs * kXChunk, row_base);
+          }
+        }
+      }
+      // this warp has read its part of the accumulator: release the buffer
+      dev::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) dev::mbar_arrive(&bars[kAccEmpty + buf]);
+        else dev::mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(buf * 8));
+        dev::bulk_wait_read_all();  // the staging buffers are reloaded by the next tile
+      }
+      __syncwarp();
+      if (!ok) break;
+    }
+    if (lane == 0) dev::bulk_wait_all();
+    __syncwarp();
+  }
+
+  // neither CTA leaves (or frees TMEM) while its peer may still use its
+  // shared memory or run pair MMAs
+  dev::tc_fence_before();
+  __syncthreads();
+  dev::cluster_sync();
+  if (warp == 1) {
+    dev::tc_fence_after();
+    dev::tmem_dealloc_pair(tmem, 512);
+  }
+  __syncthreads();
+  dev::cluster_sync();
+}
+
 template <int BN>
 int launch_bn(const void* o, const void* w, const float* bias, float* x, int64_t M, int K, int N,
               float dt, float* v_out, cudaStream_t stream) {
@@ -245,10 +533,68 @@ int validate_out_proj(const void* o, const void* w, const float* bias, const flo
   return SAVGB_OK;
 }
 
+// The persistent CTA-pair kernel: x updated alone (no velocity output), the
+// output width a multiple of 256.
+int launch_pair(const void* o, const void* w, const float* bias, float* x, int64_t M, int K, int N, float dt,
+                int sms, cudaStream_t stream) {
+  static bool attr_done[64] = {false};
+  int dev_id = 0;
+  SAVGB_CUDA(cudaGetDevice(&dev_id));
+  if (!attr_done[dev_id & 63]) {
+    SAVGB_CUDA(cudaFuncSetAttribute(wo_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    pair::kDynSmem));
+    attr_done[dev_id & 63] = true;
+  }
+  CUtensorMap ma, mb, mx;
+  const uint64_t da[2] = {(uint64_t)K, (uint64_t)M};
+  const uint64_t sa[1] = {(uint64_t)K * 2};
+  const uint32_t box128[2] = {pair::kBK, 128};
+  int rc = encode_tiled(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o, da, sa, box128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  const uint64_t db[2] = {(uint64_t)K, (uint64_t)N};
+  rc = encode_tiled(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, db, sa, box128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  const uint64_t dx[2] = {(uint64_t)N, (uint64_t)M};
+  const uint64_t sx[1] = {(uint64_t)N * 4};
+  const uint32_t bx[2] = {kXChunk, 32};
+  rc = encode_tiled(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, x, dx, sx, bx, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  WoParams p{(int)M, N, K, dt, bias, x, nullptr, nullptr};
+  if ((rc = error_word(&p.err))) return rc;
+  const int n_tiles_n = N / 256;
+  const int n_tiles = (int)((M + 255) / 256) * n_tiles_n;
+  // one wave of pairs: as many clusters as can be resident at once
+  static int max_clusters[64] = {0};
+  if (max_clusters[dev_id & 63] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * (sms / 2)));
+    cfg.blockDim = dim3(pair::kThreads);
+    cfg.dynamicSmemBytes = pair::kDynSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    SAVGB_CUDA(cudaOccupancyMaxActiveClusters(&n, wo_pair_kernel, &cfg));
+    max_clusters[dev_id & 63] = n > 0 ? n : 1;
+  }
+  const int clusters = std::min(n_tiles, max_clusters[dev_id & 63]);
+  wo_pair_kernel<<<dim3((unsigned)(2 * clusters)), pair::kThreads, pair::kDynSmem, stream>>>(ma, mb, mx, p, n_tiles_n,
+                                                                                             n_tiles);
+  SAVGB_CUDA(cudaGetLastError());
+  return SAVGB_OK;
+}
+
 int launch_out_proj_euler(const void* o, const void* w, const float* bias, float* x, int64_t M,
                           int hid_in, int hid_out, float dt, float* v_out, cudaStream_t stream) {
-  int rc = check_device(nullptr);
+  int sms = 0;
+  int rc = check_device(&sms);
   if (rc) return rc;
+  if (v_out == nullptr && hid_out % 256 == 0)
+    return launch_pair(o, w, bias, x, M, hid_in, hid_out, dt, sms, stream);
   if (hid_out % 256 == 0)
     return launch_bn<256>(o, w, bias, x, M, hid_in, hid_out, dt, v_out, stream);
   return launch_bn<128>(o, w, bias, x, M, hid_in, hid_out, dt, v_out, stream);
