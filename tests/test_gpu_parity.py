@@ -153,6 +153,11 @@ def test_attention_full_size_sampled_rows(S, name):
     (1024, 512, 512, True),     # small
     (300, 384, 400, True),      # ragged M (whole 32-row groups past M), hid_out not a multiple of 32
     (1000, 3072, 3072, False),  # base width, ragged M
+    # the CTA-pair kernel (x only, hid_out % 256 == 0):
+    (300, 384, 512, True),      # the odd CTA's 128 rows of the second tile lie wholly past M
+    (700, 200, 256, False),     # K tail: hid_in not a multiple of 64
+    (32, 128, 256, True),       # a single tile: one cluster
+    (2560, 1024, 768, False),   # several tiles per cluster, both accumulator buffers reused
 ])
 def test_out_proj_euler_parity(S, M, hid_in, hid_out, bias, with_v):
     o = bf16((M, hid_in), 31, I.KIND_Q)
