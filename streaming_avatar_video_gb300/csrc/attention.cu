@@ -238,6 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   dev::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int n = p.n_tiles;
+  // the set-up above overlaps the previous kernel of the stream (RoPE of q, k)
+  dev::griddep_launch_dependents();
+  dev::griddep_wait();
 
   if (warp < 4) {
     dev::setmaxnreg_dec<kRegsLow>();
@@ -589,7 +592,7 @@ int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, i
   }
   if ((rc = error_word(&p.err))) return rc;
   dim3 grid((unsigned)((n_q + kBlockQ - 1) / kBlockQ), (unsigned)H, (unsigned)B);
-  attn_fwd_kernel<D, KS, VS, ROPE_Q><<<grid, kThreads, dyn_smem, stream>>>(maps, p);
+  SAVGB_CUDA(launch_dependent(attn_fwd_kernel<D, KS, VS, ROPE_Q>, grid, dim3(kThreads), dyn_smem, stream, maps, p));
   SAVGB_CUDA(cudaGetLastError());
   return SAVGB_OK;
 }

@@ -49,6 +49,25 @@ int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
                  CUtensorMapSwizzle swizzle);
 
 // Internal launchers (all validate nothing: the entry points do that).
+// Launches `kernel` as a programmatic dependent of the previous kernel of the
+// stream (it may start while that one drains; the kernel itself waits with
+// griddepcontrol.wait before touching memory that earlier work uses).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 struct RopeArgs {
   const void* in;
   void* out;

@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
   static_assert(8 * kXBufs * 8 <= 1024, "x barriers must fit in the epilogue's shared memory");
   extern __shared__ uint8_t smem_raw[];
   const gemm::Ctx c = gemm::setup<BN>(smem_raw, &map_a, &map_b);
+  dev::griddep_launch_dependents();
+  dev::griddep_wait();  // the set-up above overlaps the previous kernel (the attention)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
@@ -287,6 +289,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
   dev::cluster_sync();
   dev::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  dev::griddep_launch_dependents();
+  dev::griddep_wait();  // the set-up above overlaps the previous kernel (the attention)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -513,7 +517,7 @@ int launch_bn(const void* o, const void* w, const float* bias, float* x, int64_t
   WoParams p{(int)M, N, K, dt, bias, x, v_out, nullptr};
   if ((rc = error_word(&p.err))) return rc;
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + gemm::kBM - 1) / gemm::kBM));
-  wo_euler_kernel<BN><<<grid, gemm::kThreads, L::kDynSmem, stream>>>(ma, mb, mx, p);
+  SAVGB_CUDA(launch_dependent(wo_euler_kernel<BN>, grid, dim3(gemm::kThreads), L::kDynSmem, stream, ma, mb, mx, p));
   SAVGB_CUDA(cudaGetLastError());
   return SAVGB_OK;
 }
@@ -582,8 +586,8 @@ int launch_pair(const void* o, const void* w, const float* bias, float* x, int64
     max_clusters[dev_id & 63] = n > 0 ? n : 1;
   }
   const int clusters = std::min(n_tiles, max_clusters[dev_id & 63]);
-  wo_pair_kernel<<<dim3((unsigned)(2 * clusters)), pair::kThreads, pair::kDynSmem, stream>>>(ma, mb, mx, p, n_tiles_n,
-                                                                                             n_tiles);
+  SAVGB_CUDA(launch_dependent(wo_pair_kernel, dim3((unsigned)(2 * clusters)), dim3(pair::kThreads), pair::kDynSmem,
+                              stream, ma, mb, mx, p, n_tiles_n, n_tiles));
   SAVGB_CUDA(cudaGetLastError());
   return SAVGB_OK;
 }

@@ -297,6 +297,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 #undef SAVGB_R8
 #undef SAVGB_W8
 
+// --------------------------------------------- programmatic dependent launch
+// A kernel launched as a programmatic dependent may start while the previous
+// kernel of its stream drains.  griddep_wait() returns once every earlier
+// kernel of the stream has completed and its memory is visible: each kernel
+// calls it before its first access to global memory that earlier work may
+// write or read (a no-op when launched normally).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel of the stream be scheduled once every block of this
+// one has executed it (or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- CTA pairs
 // A cluster of two CTAs on two SMs sharing tcgen05 work (cta_group::2):
 // TMEM is allocated collectively (one warp of each CTA, same columns in

@@ -15,6 +15,7 @@
 #include <cmath>
 
 #include "common.h"
+#include "ptx.cuh"
 
 namespace savgb {
 namespace {
@@ -77,8 +78,10 @@ __global__ void __launch_bounds__(kRopeThreads) rope3d_kernel(const RopeKernelAr
   float2* tab_t = tab;
   float2* tab_h = tab_t + a.gt * a.p_t;
   float2* tab_w = tab_h + a.gh * a.p_h;
+  dev::griddep_launch_dependents();
   build_tables(tab, a);
   __syncthreads();
+  dev::griddep_wait();
 
   const int ti = blockIdx.z;
   const int b = blockIdx.y;
@@ -127,8 +130,8 @@ __global__ void __launch_bounds__(kRopeThreads) rope3d_kernel(const RopeKernelAr
 // (vec_per_tok = 32*upl, upl <= kRopeFastMax) and whose head holds a divisor
 // of 32 vectors: lane L then always meets the same four channel pairs
 // ((L mod D/8)*4 ...), so it looks its four (cos, sin) up once per token and
-// applies them to all upl of its vectors.  A warp's first token is loaded
-// before the block builds its tables, so the table work overlaps that load.
+// applies them to all upl of its vectors.  The tables are built before the
+// wait on the previous kernel of the stream, so they overlap its tail.
 constexpr int kRopeFastMax = 12;
 
 __global__ void __launch_bounds__(kRopeThreads) rope3d_fast_kernel(const RopeKernelArgs a) {
@@ -149,8 +152,10 @@ __global__ void __launch_bounds__(kRopeThreads) rope3d_fast_kernel(const RopeKer
     for (int u = 0; u < kRopeFastMax; ++u)
       if (u < upl) v[u] = __ldcs(src + 32 * u);
   };
-  if (n < a.n_tokens) load(n);
+  dev::griddep_launch_dependents();
   build_tables(tab, a);
+  dev::griddep_wait();
+  if (n < a.n_tokens) load(n);
   __syncthreads();
 
   const float2* tab_t = tab;
@@ -261,7 +266,7 @@ static int launch_rope_multi(const RopeArgs* args, int n, cudaStream_t stream) {
   int per = occ * sms / (a.B * n);
   if (per < 1) per = 1;
   dim3 grid((unsigned)(groups < per ? groups : per), (unsigned)a.B, (unsigned)n);
-  kern<<<grid, kRopeThreads, smem, stream>>>(k);
+  SAVGB_CUDA(launch_dependent(kern, grid, dim3(kRopeThreads), smem, stream, k));
   SAVGB_CUDA(cudaGetLastError());
   return SAVGB_OK;
 }
