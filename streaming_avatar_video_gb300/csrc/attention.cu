@@ -26,6 +26,8 @@
 // per key tile (V and K together, P of tile 0, P of tile 1) and no other work.
 // The running max is updated lazily (only when it grows by more than 2^8 in
 // probability), and O is rescaled in TMEM by the softmax warps when it is.
+// At the end each softmax warp normalises its 32 rows of O into the Q tile's
+// shared memory (free by then) and writes them with tensor-map stores.
 // Every wait is bounded; on a timeout the block records it in the device
 // error word and every role leaves its loop.
 #include <cuda_bf16.h>
@@ -61,6 +63,7 @@ struct AttnMaps {
   CUtensorMap q;
   CUtensorMap k[3];
   CUtensorMap v[3];
+  CUtensorMap o;  // 32-row boxes: one softmax warp's rows
 };
 
 struct AttnParams {
@@ -68,7 +71,6 @@ struct AttnParams {
   int seg_tiles[3];
   int seg_len[3];
   float scale_log2;
-  __nv_bfloat16* o;
   float* lse;
   DeviceErrorWord* err;
   // 3D RoPE of the queries, applied in shared memory when the kernel is built
@@ -108,15 +110,15 @@ struct Layout {
   static constexpr int kTabMax = 227 * 1024 - kDynSmem;  // room left for the RoPE tables
 };
 
+// Key tile j of the concatenated segments: its segment, first row and valid
+// rows.  Only constant indices into the parameters, so nothing is copied to
+// local memory.
 __device__ __forceinline__ void tile_of(const AttnParams& p, int j, int& seg, int& row0, int& valid) {
-  int jj = j;
-  seg = 0;
-  while (seg < 2 && jj >= p.seg_tiles[seg]) {
-    jj -= p.seg_tiles[seg];
-    ++seg;
-  }
-  row0 = jj * kTileKV;
-  const int rest = p.seg_len[seg] - row0;
+  const int e0 = p.seg_tiles[0], e1 = e0 + p.seg_tiles[1];
+  seg = j < e0 ? 0 : (j < e1 ? 1 : 2);
+  row0 = (j - (seg == 0 ? 0 : (seg == 1 ? e0 : e1))) * kTileKV;
+  const int len = seg == 0 ? p.seg_len[0] : (seg == 1 ? p.seg_len[1] : p.seg_len[2]);
+  const int rest = len - row0;
   valid = rest < kTileKV ? rest : kTileKV;
 }
 
@@ -184,7 +186,7 @@ __device__ __forceinline__ void rope_q_row(uint8_t* sQ, int tile_bytes, const fl
 
 template <int D, int KS, int VS, bool ROPE_Q>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p) {
+    attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ AttnParams p) {
   using L = Layout<D, KS, VS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = dev::smem_u32(smem_raw);
@@ -251,8 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* ring = smem + (is_k ? L::kK : L::kV);
       uint64_t* full = &bars[is_k ? L::kKFull : L::kVFull];
       uint64_t* empty = &bars[is_k ? L::kKEmpty : L::kVEmpty];
-      const CUtensorMap* seg_map[3] = {is_k ? &maps.k[0] : &maps.v[0], is_k ? &maps.k[1] : &maps.v[1],
-                                       is_k ? &maps.k[2] : &maps.v[2]};
       if (is_k) {
         uint8_t* sQ = smem + L::kQ;
         dev::mbar_arrive_expect_tx(&bars[L::kQFull], 2 * L::kTileBytes);
@@ -276,7 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         dev::mbar_arrive_expect_tx(&full[st], L::kTileBytes);
         #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          dev::tma_load_4d(ring + st * L::kTileBytes + c * 16384, seg_map[seg], &full[st], c * 64, h,
+          dev::tma_load_4d(ring + st * L::kTileBytes + c * 16384,
+                           is_k ? (seg == 0 ? &maps.k[0] : (seg == 1 ? &maps.k[1] : &maps.k[2]))
+                                : (seg == 0 ? &maps.v[0] : (seg == 1 ? &maps.v[1] : &maps.v[2])),
+                           &full[st], c * 64, h,
                            row0, b);
         issued = j + 1;
       }
@@ -486,7 +489,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       dev::tc_fence_after();
       const int q = q0 + x * 128 + row;
       const float inv_l = 1.f / l;
-      __nv_bfloat16* dst = p.o + ((static_cast<int64_t>(b) * p.n_q + q) * p.H + h) * D;
+      // O leaves through shared memory: Q tile x is free (every MMA, and so
+      // every read of Q, has completed once O is done).  Each thread writes
+      // its row in the same 128-byte-swizzled layout the loads use; then one
+      // tensor-map store per 64 columns writes the warp's 32 rows, clipped
+      // at n_q.
+      uint8_t* sO = smem + L::kQ + x * L::kTileBytes;
       #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
@@ -496,12 +504,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i)
           pk[i] = dev::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
                                    __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (q < p.n_q) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-          #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
+        uint8_t* rowp = sO + (c >> 6) * 16384 + row * 128;
+        const int j0 = (c & 63) >> 3;
+        #pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(rowp + (((j0 + i) ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+      dev::fence_proxy_async_smem();
+      __syncwarp();
+      const int wrow0 = q0 + x * 128 + quad * 32;
+      if (lane == 0 && wrow0 < p.n_q) {
+        #pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb)
+          dev::tma_store_4d(&maps.o, sO + cb * 16384 + quad * 32 * 128, cb * 64, h, wrow0, b);
+        dev::bulk_commit();
+        // the block's shared memory must outlive the reads of the stores
+        dev::bulk_wait_read_all();
       }
       if (p.lse != nullptr && q < p.n_q)
         p.lse[(static_cast<int64_t>(b) * p.H + h) * p.n_q + q] =
@@ -519,10 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-int make_token_map(CUtensorMap* m, const void* ptr, int B, int64_t N, int H, int D) {
+int make_token_map(CUtensorMap* m, const void* ptr, int B, int64_t N, int H, int D, uint32_t box_rows = 128) {
   const uint64_t dims[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)N, (uint64_t)B};
   const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)N * H * D * 2};
-  const uint32_t box[4] = {64, 1, 128, 1};
+  const uint32_t box[4] = {64, 1, box_rows, 1};
   return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -552,6 +571,7 @@ int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, i
   AttnMaps maps;
   int rc = make_token_map(&maps.q, q, B, n_q, H, D);
   if (rc) return rc;
+  if ((rc = make_token_map(&maps.o, o, B, n_q, H, D, 32))) return rc;
   AttnParams p{};
   p.n_q = (int)n_q;
   p.H = H;
@@ -571,7 +591,6 @@ int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, i
   }
   if (!(scale > 0.f)) scale = 1.0f / std::sqrt((float)D);
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   int dyn_smem = L::kDynSmem;
   if (rope) {
