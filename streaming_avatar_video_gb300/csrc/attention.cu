@@ -9,7 +9,8 @@
 // Design (one CTA = two 128-row query tiles of one (batch, head)):
 //   warp 0      TMA producer: Q tiles once, then K and V tiles of the
 //               concatenated segments through a 2-stage ring each.
-//   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma.
+//   warp 1      allocates 512 TMEM columns and runs the MMA issue loop; one
+//               elected lane issues every tcgen05.mma.
 //   warps 2-3   idle (they complete the first warpgroup).
 //   warps 4-7   softmax of query tile 0, warps 8-11 of query tile 1; thread =
 //               one query row (TMEM lane), so row max and sum need no shuffle.
@@ -288,8 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (is_k) dev::mbar_wait(&bars[L::kQFull], 0, &never);
       for (int t = (issued > stages ? issued - stages : 0); t < issued; ++t)
         dev::mbar_wait(&full[t % stages], (t / stages) & 1, &never);
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
+      // The whole warp runs the loop, so its state is warp-uniform; one
+      // elected lane issues the MMAs and commits.  Every lane waits, and a
+      // vote keeps the warp on one path when a wait gives up.
+      const bool leader = dev::elect_one();
       const uint32_t sQ = dev::smem_u32(smem + L::kQ);
       const uint32_t sK = dev::smem_u32(smem + L::kK);
       const uint32_t sV = dev::smem_u32(smem + L::kV);
@@ -320,16 +325,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           dev::mma_ts(d, tmem + x * 128 + kk * 8, b0 + static_cast<uint32_t>(kk * (2048 >> 4)), idesc_o,
                       (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = dev::mbar_wait(&bars[ROPE_Q ? L::kQReady : L::kQFull], 0, abort) &&
-                dev::mbar_wait(&bars[L::kKFull], 0, abort);
-      if (!ok) give_up(p, abort, 3);
+      const bool ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[ROPE_Q ? L::kQReady : L::kQFull], 0, abort) &&
+                                                  dev::mbar_wait(&bars[L::kKFull], 0, abort));
+      if (!ok && leader) give_up(p, abort, 3);
       if (ok) {
         dev::tc_fence_after();
-        issue_s(0, 0);
-        dev::mma_commit(&bars[L::kSFull + 0]);
-        issue_s(1, 0);
-        dev::mma_commit(&bars[L::kSFull + 1]);
-        dev::mma_commit(&bars[L::kKEmpty + 0]);
+        if (leader) {
+          issue_s(0, 0);
+          dev::mma_commit(&bars[L::kSFull + 0]);
+          issue_s(1, 0);
+          dev::mma_commit(&bars[L::kSFull + 1]);
+          dev::mma_commit(&bars[L::kKEmpty + 0]);
+        }
         for (int j = 0; j < n; ++j) {
           const int vst = j % VS;
           const uint32_t vuse = j / VS;
@@ -340,34 +347,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool kv_ok = more ? dev::mbar_wait2(&bars[L::kVFull + vst], vuse & 1, &bars[L::kKFull + kst1],
                                                     kuse1 & 1, abort)
                                   : dev::mbar_wait(&bars[L::kVFull + vst], vuse & 1, abort);
-          if (!kv_ok || !dev::mbar_wait(&bars[L::kP + 0], j & 1, abort)) {
-            give_up(p, abort, 4);
+          if (!__all_sync(0xffffffffu, kv_ok && dev::mbar_wait(&bars[L::kP + 0], j & 1, abort))) {
+            if (leader) give_up(p, abort, 4);
             break;
           }
           dev::tc_fence_after();
-          issue_pv(0, vst, j > 0, 0, 8);
-          if (more) {
-            issue_s(0, kst1);
-            dev::mma_commit(&bars[L::kSFull + 0]);
+          if (leader) {
+            issue_pv(0, vst, j > 0, 0, 8);
+            if (more) {
+              issue_s(0, kst1);
+              dev::mma_commit(&bars[L::kSFull + 0]);
+            }
           }
-          if (!dev::mbar_wait(&bars[L::kP + 1], j & 1, abort)) {
-            give_up(p, abort, 6);
+          if (!__all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kP + 1], j & 1, abort))) {
+            if (leader) give_up(p, abort, 6);
             break;
           }
           dev::tc_fence_after();
-          issue_pv(1, vst, j > 0, 0, 8);
-          dev::mma_commit(&bars[L::kVEmpty + vst]);
-          if (more) {
-            issue_s(1, kst1);
-            dev::mma_commit(&bars[L::kSFull + 1]);
-            dev::mma_commit(&bars[L::kKEmpty + kst1]);
+          if (leader) {
+            issue_pv(1, vst, j > 0, 0, 8);
+            dev::mma_commit(&bars[L::kVEmpty + vst]);
+            if (more) {
+              issue_s(1, kst1);
+              dev::mma_commit(&bars[L::kSFull + 1]);
+              dev::mma_commit(&bars[L::kKEmpty + kst1]);
+            }
           }
         }
-        dev::mma_commit(&bars[L::kODone + 0]);
-        dev::mma_commit(&bars[L::kODone + 1]);
+        if (leader) {
+          dev::mma_commit(&bars[L::kODone + 0]);
+          dev::mma_commit(&bars[L::kODone + 1]);
+        }
       }
       // drain: all issued MMAs complete before TMEM is released
-      dev::mma_commit(&bars[L::kDrain]);
+      if (leader) dev::mma_commit(&bars[L::kDrain]);
+      __syncwarp();
       volatile int never = 0;
       dev::mbar_wait(&bars[L::kDrain], 0, &never);
     }
