@@ -43,18 +43,23 @@ METRIC = "chunk-attention TFLOP/s (% of bf16 tensor peak); latent frames/s per d
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one attention
 # launch, from one ncu capture per workload, keyed by the sha256 of the kernel
-# source the capture was taken on; any later change of the source reports null.
+# sources the capture was taken on (attention.cu, ptx.cuh, common.h); any later
+# change of them reports null.
 ATTN_TRAFFIC = {
-    # profiles/chunk_attention_base.md: 293.423 MB read + 70.729 MB written
-    "ca9ea76ae9c6cb2e245c5893b843d3d8fff3496051fb51d1c026b579d7da991d": {"base": 364152064},
+    # profiles/chunk_attention_base.md: 291.184 MB read + 61.465 MB written
+    "88db786bfc1296fda93d14c888d6eae57a5054fda15ced1cded2dc0f150fb763": {"base": 352648960},
 }
 
 
 def attn_traffic(workload: str):
     import hashlib
-    path = os.path.join(ROOT, "streaming_avatar_video_gb300", "csrc", "attention.cu")
-    sha = hashlib.sha256(open(path, "rb").read()).hexdigest()
-    return ATTN_TRAFFIC.get(sha, {}).get(workload)
+    h = hashlib.sha256()
+    for f in ("attention.cu", "ptx.cuh", "common.h"):
+        with open(os.path.join(ROOT, "streaming_avatar_video_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return ATTN_TRAFFIC.get(h.hexdigest(), {}).get(workload)
+
+
 NOMINAL_BF16_TFLOPS = 2250.0
 
 

@@ -7,11 +7,13 @@
 // per (batch, head), no mask.
 //
 // Design (one CTA = two 128-row query tiles of one (batch, head)):
-//   warp 0      TMA producer: Q tiles once, then K and V tiles of the
-//               concatenated segments through a 2-stage ring each.
+//   warp 0      TMA producer of Q (once) and of the K tiles of the
+//               concatenated segments (3-stage ring); warp 2 that of the V
+//               tiles (2-stage ring).  Both run their loop warp-wide and one
+//               elected lane issues the copies.
 //   warp 1      allocates 512 TMEM columns and runs the MMA issue loop; one
 //               elected lane issues every tcgen05.mma.
-//   warps 2-3   idle (they complete the first warpgroup).
+//   warp 3      idle (it completes the first warpgroup).
 //   warps 4-7   softmax of query tile 0, warps 8-11 of query tile 1; thread =
 //               one query row (TMEM lane), so row max and sum need no shuffle.
 // Registers: the block launches with 168 per thread; the first warpgroup
@@ -247,14 +249,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     dev::setmaxnreg_dec<kRegsLow>();
-    if ((warp == 0 || warp == 2) && lane == 0) {
+    if (warp == 0 || warp == 2) {
       // ------------------------------------------- producers: K (warp 0), V (warp 2)
+      // the whole warp runs the loop; one elected lane issues the copies
+      const bool elected = dev::elect_one();
       const bool is_k = warp == 0;
       const int stages = is_k ? KS : VS;
       uint8_t* ring = smem + (is_k ? L::kK : L::kV);
       uint64_t* full = &bars[is_k ? L::kKFull : L::kVFull];
       uint64_t* empty = &bars[is_k ? L::kKEmpty : L::kVEmpty];
-      if (is_k) {
+      if (is_k && elected) {
         uint8_t* sQ = smem + L::kQ;
         dev::mbar_arrive_expect_tx(&bars[L::kQFull], 2 * L::kTileBytes);
         #pragma unroll
@@ -270,18 +274,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_of(p, j, seg, row0, valid);
         const int st = j % stages;
         const uint32_t use = j / stages;
-        if (j >= stages && !dev::mbar_wait(&empty[st], (use - 1) & 1, abort)) {
-          give_up(p, abort, is_k ? 1 : 2);
+        if (j >= stages && !__all_sync(0xffffffffu, dev::mbar_wait(&empty[st], (use - 1) & 1, abort))) {
+          if (elected) give_up(p, abort, is_k ? 1 : 2);
           break;
         }
-        dev::mbar_arrive_expect_tx(&full[st], L::kTileBytes);
-        #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          dev::tma_load_4d(ring + st * L::kTileBytes + c * 16384,
-                           is_k ? (seg == 0 ? &maps.k[0] : (seg == 1 ? &maps.k[1] : &maps.k[2]))
-                                : (seg == 0 ? &maps.v[0] : (seg == 1 ? &maps.v[1] : &maps.v[2])),
-                           &full[st], c * 64, h,
-                           row0, b);
+        if (elected) {
+          dev::mbar_arrive_expect_tx(&full[st], L::kTileBytes);
+          #pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            dev::tma_load_4d(ring + st * L::kTileBytes + c * 16384,
+                             is_k ? (seg == 0 ? &maps.k[0] : (seg == 1 ? &maps.k[1] : &maps.k[2]))
+                                  : (seg == 0 ? &maps.v[0] : (seg == 1 ? &maps.v[1] : &maps.v[2])),
+                             &full[st], c * 64, h, row0, b);
+        }
         issued = j + 1;
       }
       // drain: every issued copy has landed before the block may exit
@@ -393,9 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = (warp - 4) * 32 + lane;  // 0..255
       build_rope_tables(tab, q0, p, r);
       dev::named_barrier_256();  // every softmax thread reaches this (no waits before it)
-      bool qok = true;
-      if (lane == 0) qok = dev::mbar_wait(&bars[L::kQFull], 0, abort);
-      qok = __shfl_sync(0xffffffffu, qok ? 1 : 0, 0) != 0;
+      const bool qok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kQFull], 0, abort));
       if (qok) {
         if (q0 + r < p.n_q) rope_q_row<D>(smem + L::kQ, L::kTileBytes, tab, r, q0, p);
         // the rotated tiles are read by the tensor core (async proxy)
@@ -420,10 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < n; ++j) {
       int seg, row0, valid;
       tile_of(p, j, seg, row0, valid);
-      // one lane polls the barrier; the warp follows it
-      bool got = true;
-      if (lane == 0) got = dev::mbar_wait(&bars[L::kSFull + x], j & 1, abort);
-      ok = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+      // every lane polls the barrier; a vote keeps the warp on one path
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kSFull + x], j & 1, abort));
       if (!ok) {
         give_up(p, abort, 7);
         break;

@@ -119,39 +119,46 @@ __device__ __forceinline__ void produce(const Ctx& c, const CUtensorMap* map_a, 
 // Warp 1, lane 0: issues the MMAs, then signals acc_full; drains before exit.
 template <int BN>
 __device__ __forceinline__ void mma(const Ctx& c, int kb_count, DeviceErrorWord* err, unsigned flag) {
+  // the whole warp runs the loop (warp-uniform state); one elected lane
+  // issues the MMAs and commits
   using L = Layout<BN>;
+  const bool leader = dev::elect_one();
   constexpr uint32_t idesc = dev::idesc_bf16_f32(128, BN, false, false);
   const uint64_t d0 = dev::sdesc_sw128(dev::smem_u32(c.smem), 16, 1024);
   bool ok = true;
   for (int kb = 0; kb < kb_count; ++kb) {
     const int st = kb % kStages;
-    if (!dev::mbar_wait(&c.full[st], (kb / kStages) & 1, c.abort)) {
-      give_up(err, c.abort, flag, 2);
+    if (!__all_sync(0xffffffffu, dev::mbar_wait(&c.full[st], (kb / kStages) & 1, c.abort))) {
+      if (leader) give_up(err, c.abort, flag, 2);
       ok = false;
       break;
     }
     dev::tc_fence_after();
-    const uint64_t ds = d0 + static_cast<uint32_t>((st * L::kStageBytes) >> 4);
-    #pragma unroll
-    for (int k = 0; k < kBK / 16; ++k) {
-      const uint32_t koff = (k * 32) >> 4;
-      const uint64_t bd = ds + ((L::kABytes >> 4) + koff);
-      dev::mma_ss(c.tmem, ds + koff, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-      dev::mma_ss(c.tmem + BN, ds + ((L::kAHalf >> 4) + koff), bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+    if (leader) {
+      const uint64_t ds = d0 + static_cast<uint32_t>((st * L::kStageBytes) >> 4);
+      #pragma unroll
+      for (int k = 0; k < kBK / 16; ++k) {
+        const uint32_t koff = (k * 32) >> 4;
+        const uint64_t bd = ds + ((L::kABytes >> 4) + koff);
+        dev::mma_ss(c.tmem, ds + koff, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        dev::mma_ss(c.tmem + BN, ds + ((L::kAHalf >> 4) + koff), bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+      }
+      dev::mma_commit(&c.empty[st]);
     }
-    dev::mma_commit(&c.empty[st]);
   }
-  if (ok) dev::mma_commit(c.acc_full);
-  dev::mma_commit(c.drain);
+  if (leader) {
+    if (ok) dev::mma_commit(c.acc_full);
+    dev::mma_commit(c.drain);
+  }
+  __syncwarp();
   volatile int never = 0;
   dev::mbar_wait(c.drain, 0, &never);
 }
 
-// Epilogue warps: wait for the accumulators (lane 0 polls); false on abort.
+// Epilogue warps: wait for the accumulators (every lane polls, a vote keeps
+// the warp on one path); false on abort.
 __device__ __forceinline__ bool wait_acc(const Ctx& c, DeviceErrorWord* err, unsigned flag) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = dev::mbar_wait(c.acc_full, 0, c.abort);
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  const bool ok = __all_sync(0xffffffffu, dev::mbar_wait(c.acc_full, 0, c.abort));
   if (ok) dev::tc_fence_after();
   else give_up(err, c.abort, flag, 3);
   return ok;

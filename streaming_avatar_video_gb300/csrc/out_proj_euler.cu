@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
   if (warp == 0) {
     if (lane == 0) gemm::produce<BN>(c, &map_a, &map_b, m0, n0, kb_count, p.err, kErrGemmWait);
   } else if (warp == 1) {
-    if (lane == 0) gemm::mma<BN>(c, kb_count, p.err, kErrGemmWait);
+    gemm::mma<BN>(c, kb_count, p.err, kErrGemmWait);
   } else if (warp >= 4) {
     // epilogue: warps 4-7 take rows 0-127 (accumulator columns [0, BN)),
     // warps 8-11 rows 128-255 ([BN, 2 BN)); a warp's 32 rows are its TMEM
@@ -109,9 +109,7 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
           const int bi = cc % kXBufs;
           uint32_t acc[32];
           dev::tmem_ld32(t_row + cc * kXChunk, acc);
-          bool got = true;
-          if (lane == 0) got = dev::mbar_wait(&xbar[bi], (cc / kXBufs) & 1, c.abort);
-          if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
+          if (!__all_sync(0xffffffffu, dev::mbar_wait(&xbar[bi], (cc / kXBufs) & 1, c.abort))) {
             gemm::give_up(p.err, c.abort, kErrGemmWait, 4);
             break;
           }
@@ -323,8 +321,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && leader) {
+    if (leader) {
       // ---------------------------------------------------------- MMA issuer
+      // the whole warp runs the loop (warp-uniform state); one elected lane
+      // issues the MMAs and commits
+      const bool issuer = dev::elect_one();
       constexpr uint32_t idesc = dev::idesc_bf16_f32(256, 256, false, false);
       const uint64_t d0 = dev::sdesc_sw128(dev::smem_u32(smem), 16, 1024);
       uint32_t it = 0;
@@ -333,32 +334,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       for (int t = cluster; t < n_tiles && ok; t += n_clusters, ++tile_i) {
         const int buf = tile_i & 1;
         const uint32_t buse = static_cast<uint32_t>(tile_i >> 1);
-        if (buse > 0 && !dev::mbar_wait_cluster(&bars[kAccEmpty + buf], (buse - 1) & 1, abort)) {
-          give_up(p, abort, 12);
+        if (buse > 0 &&
+            !__all_sync(0xffffffffu, dev::mbar_wait_cluster(&bars[kAccEmpty + buf], (buse - 1) & 1, abort))) {
+          if (issuer) give_up(p, abort, 12);
           break;
         }
         dev::tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(buf * 256);
         for (int kb = 0; kb < kb_count; ++kb, ++it) {
           const int st = static_cast<int>(it % kStages);
-          if (!dev::mbar_wait(&bars[kFull + st], (it / kStages) & 1, abort)) {
-            give_up(p, abort, 13);
+          if (!__all_sync(0xffffffffu, dev::mbar_wait(&bars[kFull + st], (it / kStages) & 1, abort))) {
+            if (issuer) give_up(p, abort, 13);
             ok = false;
             break;
           }
           dev::tc_fence_after();
-          const uint64_t ds = d0 + static_cast<uint32_t>((st * kStageBytes) >> 4);
-          #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint32_t koff = (k * 32) >> 4;
-            dev::mma_ss_pair(d, ds + koff, ds + ((kABytes >> 4) + koff), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          if (issuer) {
+            const uint64_t ds = d0 + static_cast<uint32_t>((st * kStageBytes) >> 4);
+            #pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint32_t koff = (k * 32) >> 4;
+              dev::mma_ss_pair(d, ds + koff, ds + ((kABytes >> 4) + koff), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            }
+            dev::mma_commit_pair(&bars[kEmpty + st], 3);
           }
-          dev::mma_commit_pair(&bars[kEmpty + st], 3);
         }
-        if (ok) dev::mma_commit_pair(&bars[kAccFull + buf], 3);
+        if (ok && issuer) dev::mma_commit_pair(&bars[kAccFull + buf], 3);
       }
       // every MMA has completed before TMEM is released
-      dev::mma_commit_pair(&bars[kDrain], 1);
+      if (issuer) dev::mma_commit_pair(&bars[kDrain], 1);
+      __syncwarp();
       volatile int never = 0;
       dev::mbar_wait(&bars[kDrain], 0, &never);
     }
@@ -405,9 +410,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         const int ncols = min(128, p.N - ncol0);
         if (m < p.M && ncols > 0) dev::prefetch_l2(p.x + static_cast<int64_t>(m) * p.N + ncol0, ncols * 4);
       }
-      bool got = true;
-      if (lane == 0) got = dev::mbar_wait_cluster(&bars[kAccFull + buf], (tile_i >> 1) & 1, abort);
-      if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
+      // every lane polls; a vote keeps the warp on one path
+      if (!__all_sync(0xffffffffu, dev::mbar_wait_cluster(&bars[kAccFull + buf], (tile_i >> 1) & 1, abort))) {
         give_up(p, abort, 15);
         break;
       }
@@ -424,10 +428,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         const int bi = cc % kPairXBufs;
         uint32_t acc[32];
         dev::tmem_ld32(t_lane + static_cast<uint32_t>(buf * 256 + ch * 128 + cc * kXChunk), acc);
-        bool xg = true;
-        if (lane == 0) xg = dev::mbar_wait(&xbar[bi], xwaits[bi] & 1, abort);
+        const bool xg = __all_sync(0xffffffffu, dev::mbar_wait(&xbar[bi], xwaits[bi] & 1, abort));
         ++xwaits[bi];
-        if (__shfl_sync(0xffffffffu, xg ? 1 : 0, 0) == 0) {
+        if (!xg) {
           give_up(p, abort, 16);
           ok = false;
           break;

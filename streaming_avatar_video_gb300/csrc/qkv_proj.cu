@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
   if (warp == 0) {
     if (lane == 0) gemm::produce<BN>(c, &map_a, &map_b, m0, n0, kb_count, p.err, kErrGemmWait);
   } else if (warp == 1) {
-    if (lane == 0) gemm::mma<BN>(c, kb_count, p.err, kErrGemmWait);
+    gemm::mma<BN>(c, kb_count, p.err, kErrGemmWait);
   } else if (warp >= 4) {
     // cos/sin tables [t | h | w] x pairs of each axis, built while the MMAs run
     float2* tab = reinterpret_cast<float2*>(c.smem + L::kExtra);
