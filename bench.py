@@ -251,7 +251,10 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
     attn_tflops = attn_flops / (attn_ms * 1e-3) / 1e12
     pk, pk_kind = peaks()
     peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-    rope_bytes = 2 * 2 * 2 * w.B * w.n_q * w.hid  # q and k, read + write, 2 bytes each
+    # the stream rotates q inside the attention kernel when its RoPE table fits;
+    # the RoPE pass then moves k alone
+    fused = cs.fused_q_rope
+    rope_bytes = 2 * 2 * (1 if fused else 2) * w.B * w.n_q * w.hid  # read + write, 2 bytes each
     wo_flops = w.wo_flops()
 
     # end-to-end through the public API with host buffers
@@ -283,7 +286,8 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
         "latent_frames_per_s": round(frames_per_s, 1),
         "pct_of_bf16_peak": {"nominal_2250": round(100 * attn_tflops / NOMINAL_BF16_TFLOPS, 1),
                              f"{pk_kind}_sustained": round(100 * attn_tflops / peak, 1)},
-        "kernels_ms": {"rope3d_qk": round(rope_ms, 4), "chunk_attention": round(attn_ms, 4),
+        "kernels_ms": {("rope3d_k" if fused else "rope3d_qk"): round(rope_ms, 4),
+                       ("chunk_attention_qrope" if fused else "chunk_attention"): round(attn_ms, 4),
                        "out_proj_euler": round(wo_ms, 4)},
         "kernel_rates": {
             "chunk_attention_tflops": round(attn_tflops, 1),
@@ -291,7 +295,8 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
             "rope3d_gbs": round(rope_bytes / (rope_ms * 1e-3) / 1e9, 1),
         },
         "roofline": {
-            "kernel": "chunk_attention (attn_fwd_kernel<128, 3, 2, false>)",
+            "kernel": ("chunk_attention_qrope (attn_fwd_kernel<128, 2, 2, true>: RoPE of q fused)" if fused
+                       else "chunk_attention (attn_fwd_kernel<128, 3, 2, false>)"),
             "bound": "tensor",
             "achieved": round(attn_tflops, 1),
             "peak": peak,

@@ -297,6 +297,14 @@ int chunk_stream_sync(chunk_stream_t* s);
 int chunk_stream_info(const chunk_stream_t* s, int64_t* chunk_index, int64_t* boundary_tokens,
                       int64_t* arena_bytes, const void** boundary_k, const void** boundary_v);
 
+/* *fused = 1 when the steps of this stream rotate q inside the attention
+ * kernel (chunk_attention_qrope with a cos/sin table built once at create and
+ * kept in the arena; the RoPE pass then rotates k only), 0 when one pass
+ * rotates q and k before chunk_attention.  The fused form is used whenever its
+ * table fits in the kernel's shared memory; both give the same results to
+ * bf16 rounding. */
+int chunk_stream_fused_q_rope(const chunk_stream_t* s, int* fused);
+
 /* Checkpoint of the rolling state (chunk index, boundary K/V in use, and with
  * interp_chunks the I-chunk index and both anchor slots) into a host buffer.  With buf == NULL only *size_out is set.  Synchronises the
  * stream.  The reference is not part of the state (it is set again on

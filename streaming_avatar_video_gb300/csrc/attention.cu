@@ -77,11 +77,16 @@ struct AttnParams {
   float* lse;
   DeviceErrorWord* err;
   // 3D RoPE of the queries, applied in shared memory when the kernel is built
-  // with ROPE_Q: query token n sits at (t0 + n/(gh*gw), (n/gw)%gh, n%gw)
+  // with ROPE_Q: query token n sits at (t0 + n/(gh*gw), (n/gw)%gh, n%gw).
+  // The cos/sin table in global memory is [t rows (tab_t_n from tab_t_lo) |
+  // h section (tab_h_sec entries) | w section]; a block copies its own t rows
+  // (at most tab_t_rows) and the h and w sections into shared memory.
   int gh, gw, t0;
-  int p_t, p_h, p_w;
-  float log2_base;
-  int tab_t_rows;  // time rows of the table (time values one block's 256 queries can span)
+  const float2* rope_tab;
+  int tab_t_lo, tab_t_n;
+  int tab_t_rows;      // time rows one block's 256 queries can span
+  int tab_h_sec;       // entries of the h section (padded to 16 bytes)
+  int tab_hw_entries;  // entries of the h and w sections
 };
 
 template <int D, int KS, int VS>
@@ -105,12 +110,11 @@ struct Layout {
   static constexpr int kQReady = kDrain + 1;  // queries rotated in place (ROPE_Q)
   static constexpr int kNumBars = kQReady + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kTab = kMisc + 16;  // cos/sin tables of the query RoPE (ROPE_Q only)
+  static constexpr int kTab = (kMisc + 16 + 127) / 128 * 128;  // cos/sin tables of the query RoPE (ROPE_Q only)
   static constexpr int kBytes = kTab;
   // request at least 120 KiB so two blocks never share an SM (each holds all 512 TMEM columns)
   static constexpr int kDynSmem = (kBytes + 1024 > 120 * 1024) ? kBytes + 1024 : 120 * 1024;
   static_assert(kBytes + 1024 <= 227 * 1024, "shared memory budget");
-  static constexpr int kTabMax = 227 * 1024 - kDynSmem;  // room left for the RoPE tables
 };
 
 // Key tile j of the concatenated segments: its segment, first row and valid
@@ -132,19 +136,33 @@ __device__ __forceinline__ void give_up(const AttnParams& p, volatile int* abort
   }
 }
 
-// RoPE tables of one block: float2 (cos, sin) for [t rows | h values | w
-// values] x their axis's pairs; the time rows start at the block's first
-// query frame.  Built by the 256 softmax threads before the rotation.
-__device__ __forceinline__ void build_rope_tables(float2* tab, int q0, const AttnParams& p, int tid256) {
-  const int hw = p.gh * p.gw;
-  const int t_first = p.t0 + q0 / hw;
-  const int n_t = p.tab_t_rows * p.p_t, n_h = p.gh * p.p_h, n_w = p.gw * p.p_w;
-  for (int i = tid256; i < n_t + n_h + n_w; i += 256) {
+// Channel pairs of each RoPE axis: D/2 pairs, a third each (rounded down)
+// for h and w and the rest for t, in the order [t | h | w].
+template <int D>
+struct RopeSplit {
+  static constexpr int kP = D / 2, kH = kP / 3, kW = kP / 3, kT = kP - 2 * (kP / 3);
+};
+
+__host__ __device__ constexpr int64_t even_up(int64_t n) { return (n + 1) & ~static_cast<int64_t>(1); }
+
+// The cos/sin table of the query RoPE in global memory: float2 (cos, sin)
+// for [n_t time rows from t_lo | grid_h rows | grid_w rows] x their axis's
+// pairs, each section padded to an even number of entries (16 bytes).
+// Pair j of an axis with P pairs turns at base^(-j/P) per unit of position.
+template <int D>
+__global__ void rope_q_table_kernel(float2* tab, int t_lo, int n_t, int gh, int gw, float log2_base) {
+  using R = RopeSplit<D>;
+  const int n_tt = n_t * R::kT, n_h = gh * R::kH, n_w = gw * R::kW;
+  const int h_off = static_cast<int>(even_up(n_tt));
+  const int w_off = h_off + static_cast<int>(even_up(n_h));
+  const int total = w_off + static_cast<int>(even_up(n_w));
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     int pos, j, P;
-    if (i < n_t) { pos = t_first + i / p.p_t; j = i % p.p_t; P = p.p_t; }
-    else if (i < n_t + n_h) { const int k = i - n_t; pos = k / p.p_h; j = k % p.p_h; P = p.p_h; }
-    else { const int k = i - n_t - n_h; pos = k / p.p_w; j = k % p.p_w; P = p.p_w; }
-    const float omega = exp2f(-static_cast<float>(j) / static_cast<float>(P) * p.log2_base);
+    if (i < n_tt) { pos = t_lo + i / R::kT; j = i % R::kT; P = R::kT; }
+    else if (i >= h_off && i < h_off + n_h) { const int k = i - h_off; pos = k / R::kH; j = k % R::kH; P = R::kH; }
+    else if (i >= w_off && i < w_off + n_w) { const int k = i - w_off; pos = k / R::kW; j = k % R::kW; P = R::kW; }
+    else { tab[i] = make_float2(1.f, 0.f); continue; }  // padding, never read
+    const float omega = exp2f(-static_cast<float>(j) / static_cast<float>(P) * log2_base);
     float sn, cs;
     sincosf(static_cast<float>(pos) * omega, &sn, &cs);
     tab[i] = make_float2(cs, sn);
@@ -163,10 +181,10 @@ __device__ __forceinline__ void rope_q_row(uint8_t* sQ, int tile_bytes, const fl
   const int r2 = q % hw;
   const int hh = r2 / p.gw;
   const int ww = r2 - hh * p.gw;
-  const float2* tr = tab + tt * p.p_t;
-  const float2* hr = tab + p.tab_t_rows * p.p_t + hh * p.p_h - p.p_t;
-  const float2* wr = tab + p.tab_t_rows * p.p_t + p.gh * p.p_h + ww * p.p_w - p.p_t - p.p_h;
-  const int ph_end = p.p_t + p.p_h;
+  using R = RopeSplit<D>;
+  const float2* tr = tab + tt * R::kT;
+  const float2* hr = tab + p.tab_t_rows * R::kT + hh * R::kH - R::kT;
+  const float2* wr = tab + p.tab_t_rows * R::kT + p.tab_h_sec + ww * R::kW - R::kT - R::kH;
   #pragma unroll
   for (int c = 0; c < D / 64; ++c) {
     #pragma unroll
@@ -175,7 +193,7 @@ __device__ __forceinline__ void rope_q_row(uint8_t* sQ, int tile_bytes, const fl
       uint4 v = *cell;
       uint32_t w0 = v.x, w1 = v.y, w2 = v.z, w3 = v.w;
       #define SAVGB_QROT(W, U) { const int pr = c * 32 + 4 * j + (U);                                   \
-        const float2 cs = pr < p.p_t ? tr[pr] : (pr < ph_end ? hr[pr] : wr[pr]);                     \
+        const float2 cs = pr < R::kT ? tr[pr] : (pr < R::kT + R::kH ? hr[pr] : wr[pr]);              \
         __nv_bfloat162 e = *reinterpret_cast<__nv_bfloat162*>(&W);                                    \
         const float a = __low2float(e), b = __high2float(e);                                          \
         __nv_bfloat162 o2 = __floats2bfloat162_rn(a * cs.x - b * cs.y, a * cs.y + b * cs.x);          \
@@ -260,7 +278,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t* empty = &bars[is_k ? L::kKEmpty : L::kVEmpty];
       if (is_k && elected) {
         uint8_t* sQ = smem + L::kQ;
-        dev::mbar_arrive_expect_tx(&bars[L::kQFull], 2 * L::kTileBytes);
+        if constexpr (ROPE_Q) {
+          // this block's time rows and the h and w sections of the RoPE table,
+          // on the Q barrier
+          using R = RopeSplit<D>;
+          const int r0 = p.t0 + q0 / (p.gh * p.gw) - p.tab_t_lo;
+          const int rows = min(p.tab_t_rows, p.tab_t_n - r0);
+          const uint32_t tb = static_cast<uint32_t>(rows * R::kT * 8);
+          const uint32_t hb = static_cast<uint32_t>(p.tab_hw_entries * 8);
+          float2* st = reinterpret_cast<float2*>(smem + L::kTab);
+          dev::mbar_arrive_expect_tx(&bars[L::kQFull], 2 * L::kTileBytes + tb + hb);
+          dev::bulk_load(st, p.rope_tab + r0 * R::kT, tb, &bars[L::kQFull]);
+          dev::bulk_load(st + p.tab_t_rows * R::kT, p.rope_tab + p.tab_t_n * R::kT, hb, &bars[L::kQFull]);
+        } else {
+          dev::mbar_arrive_expect_tx(&bars[L::kQFull], 2 * L::kTileBytes);
+        }
         #pragma unroll
         for (int x = 0; x < 2; ++x)
           #pragma unroll
@@ -394,15 +426,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     dev::setmaxnreg_inc<kRegsHigh>();
     if constexpr (ROPE_Q) {
       // ------------------------------------------------ RoPE of the Q tiles
-      float2* tab = reinterpret_cast<float2*>(smem + L::kTab);
+      // the table arrived with Q; one thread rotates one query row
+      const float2* tab = reinterpret_cast<const float2*>(smem + L::kTab);
       const int r = (warp - 4) * 32 + lane;  // 0..255
-      build_rope_tables(tab, q0, p, r);
-      dev::named_barrier_256();  // every softmax thread reaches this (no waits before it)
       const bool qok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kQFull], 0, abort));
       if (qok) {
         if (q0 + r < p.n_q) rope_q_row<D>(smem + L::kQ, L::kTileBytes, tab, r, q0, p);
         // the rotated tiles are read by the tensor core (async proxy)
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        dev::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) dev::mbar_arrive(&bars[L::kQReady]);
       } else {
@@ -609,20 +640,21 @@ int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, i
   p.lse = lse;
   int dyn_smem = L::kDynSmem;
   if (rope) {
+    using R = RopeSplit<D>;
     p.gh = rope->grid_h;
     p.gw = rope->grid_w;
     p.t0 = rope->t0;
-    const int P = D / 2;
-    p.p_h = P / 3;
-    p.p_w = P / 3;
-    p.p_t = P - 2 * (P / 3);
-    p.log2_base = (float)std::log2(rope->base);
+    p.rope_tab = static_cast<const float2*>(rope->tab);
+    p.tab_t_lo = rope->tab_t_lo;
+    p.tab_t_n = rope->tab_t_n;
     const int64_t hw = (int64_t)rope->grid_h * rope->grid_w;
-    p.tab_t_rows = (int)((kBlockQ - 1) / hw + 2);
-    const int64_t tab = 8 * ((int64_t)p.tab_t_rows * p.p_t + (int64_t)p.gh * p.p_h + (int64_t)p.gw * p.p_w);
-    if (tab > L::kTabMax)
+    p.tab_t_rows = (int)std::min<int64_t>((kBlockQ - 1) / hw + 2, rope->tab_t_n);
+    p.tab_h_sec = (int)even_up((int64_t)p.gh * R::kH);
+    p.tab_hw_entries = p.tab_h_sec + (int)even_up((int64_t)p.gw * R::kW);
+    const int64_t tab = 8 * ((int64_t)p.tab_t_rows * R::kT + p.tab_hw_entries);
+    if (L::kTab + tab + 1024 > 227 * 1024)
       return fail(SAVGB_ERR_UNSUPPORTED, "chunk_attention_qrope: RoPE tables of %lld bytes do not fit", (long long)tab);
-    dyn_smem = std::max<int>(dyn_smem, L::kBytes + 1024 + (int)tab);
+    dyn_smem = std::max<int>(dyn_smem, L::kTab + 1024 + (int)tab);
   }
   if ((rc = error_word(&p.err))) return rc;
   dim3 grid((unsigned)((n_q + kBlockQ - 1) / kBlockQ), (unsigned)H, (unsigned)B);
@@ -672,6 +704,55 @@ int validate_qrope(const QRope& r, int64_t n_q, int D) {
     return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope: base must be finite and > 0");
   if (r.t0 < -(1 << 20) || r.t0 > (1 << 20)) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope: |t0| > 2^20");
   if (D != 64 && D != 128) return fail(SAVGB_ERR_UNSUPPORTED, "chunk_attention_qrope: head_dim %d", D);
+  if (r.tab && (!aligned16(r.tab) || r.t0 < r.tab_t_lo || (int64_t)r.t0 + r.grid_t > (int64_t)r.tab_t_lo + r.tab_t_n))
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope: the RoPE table does not cover the query frames");
+  return SAVGB_OK;
+}
+
+namespace {
+
+template <int D>
+int64_t table_entries(int n_t, int grid_h, int grid_w) {
+  using R = RopeSplit<D>;
+  return even_up((int64_t)n_t * R::kT) + even_up((int64_t)grid_h * R::kH) + even_up((int64_t)grid_w * R::kW);
+}
+
+template <int D, int KS, int VS>
+bool fits(int grid_t, int grid_h, int grid_w) {
+  using R = RopeSplit<D>;
+  using L = Layout<D, KS, VS>;
+  const int64_t hw = (int64_t)grid_h * grid_w;
+  const int64_t rows = std::min<int64_t>((kBlockQ - 1) / hw + 2, grid_t);
+  const int64_t tab = 8 * (rows * R::kT + even_up((int64_t)grid_h * R::kH) + even_up((int64_t)grid_w * R::kW));
+  return L::kTab + tab + 1024 <= 227 * 1024;
+}
+
+}  // namespace
+
+int64_t rope_q_table_bytes(int D, int n_t, int grid_h, int grid_w) {
+  return 8 * (D == 64 ? table_entries<64>(n_t, grid_h, grid_w) : table_entries<128>(n_t, grid_h, grid_w));
+}
+
+bool qrope_fits(int D, int grid_t, int grid_h, int grid_w) {
+  if (D == 64) return fits<64, kStagesK64, kStagesV64>(grid_t, grid_h, grid_w);
+  if (D == 128) return fits<128, 2, kStagesV128>(grid_t, grid_h, grid_w);
+  return false;
+}
+
+int rope_q_table_build(void* tab, int D, int t_lo, int n_t, int grid_h, int grid_w, double base,
+                       cudaStream_t stream) {
+  const int64_t entries = rope_q_table_bytes(D, n_t, grid_h, grid_w) / 8;
+  const int threads = 256;
+  const int blocks = (int)std::min<int64_t>((entries + threads - 1) / threads, 1024);
+  const float log2_base = (float)std::log2(base);
+  // an ordinary launch: it starts after everything before it on the stream
+  if (D == 64)
+    rope_q_table_kernel<64><<<blocks, threads, 0, stream>>>(static_cast<float2*>(tab), t_lo, n_t, grid_h, grid_w,
+                                                             log2_base);
+  else
+    rope_q_table_kernel<128><<<blocks, threads, 0, stream>>>(static_cast<float2*>(tab), t_lo, n_t, grid_h, grid_w,
+                                                              log2_base);
+  SAVGB_CUDA(cudaGetLastError());
   return SAVGB_OK;
 }
 
@@ -680,10 +761,30 @@ int launch_attention_qrope(const void* q, int B, int64_t n_q, int H, int D, cons
                            cudaStream_t stream) {
   int rc = check_device(nullptr);
   if (rc) return rc;
-  if (D == 64)
-    return launch_impl<64, kStagesK64, kStagesV64, true>(q, B, n_q, H, segs, n_segs, scale, o, lse, &rope, stream);
-  // two K stages leave room for the tables
-  return launch_impl<128, 2, kStagesV128, true>(q, B, n_q, H, segs, n_segs, scale, o, lse, &rope, stream);
+  if (!qrope_fits(D, rope.tab ? rope.tab_t_n : rope.grid_t, rope.grid_h, rope.grid_w))
+    return fail(SAVGB_ERR_UNSUPPORTED, "chunk_attention_qrope: the RoPE tables of a %d x %d grid do not fit in "
+                "shared memory", rope.grid_h, rope.grid_w);
+  QRope r = rope;
+  void* tmp = nullptr;
+  if (!r.tab) {
+    // a table for this call only, stream-ordered
+    SAVGB_CUDA(cudaMallocAsync(&tmp, (size_t)rope_q_table_bytes(D, r.grid_t, r.grid_h, r.grid_w), stream));
+    rc = rope_q_table_build(tmp, D, r.t0, r.grid_t, r.grid_h, r.grid_w, r.base, stream);
+    r.tab = tmp;
+    r.tab_t_lo = r.t0;
+    r.tab_t_n = r.grid_t;
+  }
+  if (!rc) {
+    if (D == 64)
+      rc = launch_impl<64, kStagesK64, kStagesV64, true>(q, B, n_q, H, segs, n_segs, scale, o, lse, &r, stream);
+    else  // two K stages leave room for the tables (and run as fast as three)
+      rc = launch_impl<128, 2, kStagesV128, true>(q, B, n_q, H, segs, n_segs, scale, o, lse, &r, stream);
+  }
+  if (tmp) {
+    const cudaError_t e = cudaFreeAsync(tmp, stream);
+    if (!rc && e != cudaSuccess) rc = cuda_fail(e, "cudaFreeAsync(RoPE table)");
+  }
+  return rc;
 }
 
 }  // namespace savgb

@@ -51,6 +51,10 @@ struct chunk_stream {
   __nv_bfloat16_raw* anc_k[2];
   __nv_bfloat16_raw* anc_v[2];
   __nv_bfloat16_raw* v_buf;  // projected v of a block step (qkv_block); its bf16 x shares `o`
+  // the RoPE of q runs inside the attention kernel when its cos/sin table (t
+  // in [0, F) and the whole grid, built once here) fits in shared memory
+  bool qrope;
+  void* qrope_tab;
   int64_t ichunk_index;
   int cur;             // boundary slot in use
   int64_t bnd_in_use;  // 0 on chunk 0
@@ -134,7 +138,9 @@ int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stre
   const int64_t tok_b = round_up(s->n_tok * tok_bytes, 256);
   const int64_t anc_b = c.interp_chunks ? round_up(2 * fr * tok_bytes, 256) : 0;
   const int64_t vbuf_b = c.qkv_block ? tok_b : 0;
-  s->arena_bytes = 2 * ref_b + 4 * bnd_b + 3 * tok_b + 4 * anc_b + vbuf_b;
+  s->qrope = qrope_fits(c.D, c.F, c.grid_h, c.grid_w);
+  const int64_t tab_b = s->qrope ? round_up(rope_q_table_bytes(c.D, c.F, c.grid_h, c.grid_w), 256) : 0;
+  s->arena_bytes = 2 * ref_b + 4 * bnd_b + 3 * tok_b + 4 * anc_b + vbuf_b + tab_b;
   const char* cap = getenv("SAVGB_ARENA_LIMIT_BYTES");
   if (cap && *cap) {
     const long long lim = atoll(cap);
@@ -162,6 +168,13 @@ int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stre
     s->anc_v[i] = anc_b ? take(anc_b) : nullptr;
   }
   s->v_buf = vbuf_b ? take(vbuf_b) : nullptr;
+  s->qrope_tab = tab_b ? static_cast<void*>(take(tab_b)) : nullptr;
+  if (s->qrope &&
+      (rc = rope_q_table_build(s->qrope_tab, c.D, 0, c.F, c.grid_h, c.grid_w, c.rope_base, s->stream))) {
+    cudaFree(s->arena);
+    delete s;
+    return rc;
+  }
   s->ichunk_index = 0;
   s->cur = 0;
   s->bnd_in_use = 0;
@@ -206,11 +219,11 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
   const bool ev = s->have_events;
   s->have_events = false;
   if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[0], s->stream));
-  // one launch rotates q and k (rotating q inside the attention kernel
-  // measured slower: its start-up hand-off outweighs the saved HBM pass)
+  // k is rotated by its own pass; q inside the attention kernel (saving its
+  // HBM pass) when the stream's RoPE table fits, else in the same pass as k
   RopeArgs aq = rope_args(s, q, s->q_rot, per_b, per_b, c.F, 0);
   RopeArgs ak = rope_args(s, k, s->k_rot, per_b, per_b, c.F, 0);
-  int rc = launch_rope_pair(aq, ak, s->stream);
+  int rc = s->qrope ? launch_rope(ak, s->stream) : launch_rope_pair(aq, ak, s->stream);
   if (rc) return rc;
   if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[1], s->stream));
   AttnSeg segs[3] = {
@@ -218,8 +231,17 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
       {s->bnd_k[s->cur], s->bnd_v[s->cur], s->bnd_in_use},
       {s->k_rot, v, s->n_tok},
   };
-  rc = launch_attention(s->q_rot, c.B, s->n_tok, c.H, c.D, segs, 3, c.softmax_scale, s->o, nullptr,
-                        s->stream);
+  if (s->qrope) {
+    QRope r{c.F, c.grid_h, c.grid_w, 0, c.rope_base};
+    r.tab = s->qrope_tab;
+    r.tab_t_lo = 0;
+    r.tab_t_n = c.F;
+    rc = launch_attention_qrope(q, c.B, s->n_tok, c.H, c.D, segs, 3, c.softmax_scale, r, s->o, nullptr,
+                                s->stream);
+  } else {
+    rc = launch_attention(s->q_rot, c.B, s->n_tok, c.H, c.D, segs, 3, c.softmax_scale, s->o, nullptr,
+                          s->stream);
+  }
   if (rc) return rc;
   if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[2], s->stream));
   rc = launch_out_proj_euler(s->o, w_o, bias, x, c.B * s->n_tok, (int)s->hid, (int)s->hid, dt,
@@ -290,7 +312,7 @@ int chunk_stream_istep(chunk_stream_t* s, const void* q, const void* k, const vo
   const int64_t per_b = n_int * s->hid;
   RopeArgs aq = rope_args(s, q, s->q_rot, per_b, per_b, c.F - 2, 1);
   RopeArgs ak = rope_args(s, k, s->k_rot, per_b, per_b, c.F - 2, 1);
-  int rc = launch_rope_pair(aq, ak, s->stream);
+  int rc = s->qrope ? launch_rope(ak, s->stream) : launch_rope_pair(aq, ak, s->stream);
   if (rc) return rc;
   const int sl = (int)(s->ichunk_index & 1);
   AttnSeg segs[3] = {
@@ -298,7 +320,16 @@ int chunk_stream_istep(chunk_stream_t* s, const void* q, const void* k, const vo
       {s->anc_k[sl], s->anc_v[sl], 2 * fr},
       {s->k_rot, v, n_int},
   };
-  rc = launch_attention(s->q_rot, c.B, n_int, c.H, c.D, segs, 3, c.softmax_scale, s->o, nullptr, s->stream);
+  if (s->qrope) {
+    // the interior frames sit at t = 1 .. F-2 of the stream's table
+    QRope r{c.F - 2, c.grid_h, c.grid_w, 1, c.rope_base};
+    r.tab = s->qrope_tab;
+    r.tab_t_lo = 0;
+    r.tab_t_n = c.F;
+    rc = launch_attention_qrope(q, c.B, n_int, c.H, c.D, segs, 3, c.softmax_scale, r, s->o, nullptr, s->stream);
+  } else {
+    rc = launch_attention(s->q_rot, c.B, n_int, c.H, c.D, segs, 3, c.softmax_scale, s->o, nullptr, s->stream);
+  }
   if (rc) return rc;
   return launch_out_proj_euler(s->o, w_o, bias, x, c.B * n_int, (int)s->hid, (int)s->hid, dt, nullptr,
                                s->stream);
@@ -418,6 +449,13 @@ int chunk_stream_info(const chunk_stream_t* s, int64_t* chunk_index, int64_t* bo
   if (arena_bytes) *arena_bytes = s->arena_bytes;
   if (boundary_k) *boundary_k = s->bnd_in_use ? s->bnd_k[s->cur] : nullptr;
   if (boundary_v) *boundary_v = s->bnd_in_use ? s->bnd_v[s->cur] : nullptr;
+  return SAVGB_OK;
+}
+
+int chunk_stream_fused_q_rope(const chunk_stream_t* s, int* fused) {
+  clear_error();
+  if (!s || !fused) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_fused_q_rope: null argument");
+  *fused = s->qrope ? 1 : 0;
   return SAVGB_OK;
 }
 

@@ -97,8 +97,19 @@ int launch_attention(const void* q, int B, int64_t n_q, int H, int D, const Attn
 struct QRope {
   int grid_t, grid_h, grid_w, t0;
   double base;
+  // a cos/sin table from rope_q_table_build covering t in [tab_t_lo,
+  // tab_t_lo + tab_t_n); null: launch_attention_qrope builds one per call
+  const void* tab = nullptr;
+  int tab_t_lo = 0, tab_t_n = 0;
 };
 int validate_qrope(const QRope& r, int64_t n_q, int D);
+// The fused kernel's cos/sin table in global memory: [t rows | h | w] for
+// n_t time values from t_lo and the whole h x w grid (bytes, a multiple of 16).
+int64_t rope_q_table_bytes(int D, int n_t, int grid_h, int grid_w);
+int rope_q_table_build(void* tab, int D, int t_lo, int n_t, int grid_h, int grid_w, double base,
+                       cudaStream_t stream);
+// Whether the fused kernel's shared-memory copy of the table fits.
+bool qrope_fits(int D, int grid_t, int grid_h, int grid_w);
 int launch_attention_qrope(const void* q, int B, int64_t n_q, int H, int D, const AttnSeg* segs,
                            int n_segs, float scale, const QRope& rope, void* o, float* lse,
                            cudaStream_t stream);

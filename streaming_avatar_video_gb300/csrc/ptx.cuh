@@ -150,6 +150,14 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
 // Prefetches `bytes` (a multiple of 16) of global memory at a 16-byte aligned
 // address into L2.
 // Tensor-map store of a 2D tile from shared memory (bulk-group completion).
+// Untiled bulk copy global -> shared, completing on `bar` (complete_tx);
+// both addresses 16-byte aligned and `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1)

@@ -32,7 +32,7 @@ EXPORTS = (
     "chunk_stream_end_chunk", "chunk_stream_set_step_events", "chunk_stream_sync", "chunk_stream_info", "chunk_stream_export_state",
     "chunk_stream_import_state", "chunk_stream_destroy", "chunk_step_noalloc",
     "chunk_stream_istep", "chunk_stream_end_ichunk", "chunk_stream_ichunk_index", "chunk_attention_qrope",
-    "qkv_rope_project", "chunk_stream_block_step",
+    "qkv_rope_project", "chunk_stream_block_step", "chunk_stream_fused_q_rope",
 )
 
 
@@ -92,6 +92,7 @@ def lib() -> ctypes.CDLL:
         "chunk_stream_ichunk_index": (c_int, [c_vp, ctypes.POINTER(c_i64)]),
         "chunk_stream_set_step_events": (c_int, [c_vp, ctypes.POINTER(c_vp)]),
         "chunk_stream_sync": (c_int, [c_vp]),
+        "chunk_stream_fused_q_rope": (c_int, [c_vp, ctypes.POINTER(c_int)]),
         "chunk_stream_info": (c_int, [c_vp, ctypes.POINTER(c_i64), ctypes.POINTER(c_i64), ctypes.POINTER(c_i64),
                                       ctypes.POINTER(c_vp), ctypes.POINTER(c_vp)]),
         "chunk_stream_export_state": (c_int, [c_vp, c_vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]),
@@ -375,6 +376,14 @@ class ChunkStream:
 
     def sync(self) -> None:
         _check(lib().chunk_stream_sync(self.handle))
+
+    @property
+    def fused_q_rope(self) -> bool:
+        """True when the steps rotate q inside the attention kernel (the RoPE
+        pass then rotates k only)."""
+        f = ctypes.c_int()
+        _check(lib().chunk_stream_fused_q_rope(self.handle, ctypes.byref(f)))
+        return bool(f.value)
 
     def info(self) -> dict:
         ci, bt, ab = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()

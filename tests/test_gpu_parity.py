@@ -231,15 +231,35 @@ def run_stream_oracle(w, seed, chunks, steps=None):
 def test_stream_tiny(S):
     w = I.WORKLOADS["tiny"]
     cs, xs, _ = run_stream_gpu(S, w, 0, 1)
+    assert cs.fused_q_rope  # the stream's RoPE table fits: q is rotated inside the attention kernel
     want, _ = run_stream_oracle(w, 0, 1)
     assert_close(f64(xs[0]), want[0], what="tiny x")
     cs.close()
+
+
+def test_stream_wide_grid_unfused(S):
+    """A 2 x 400 frame grid: the RoPE table of its w axis (67 KB) does not fit
+    next to the attention operands, so the stream rotates q and k in one pass
+    before the plain attention kernel, and the stand-alone fused call refuses
+    the grid.  Two chunks x 2 steps against the oracle."""
+    w = I.Workload("wide", B=1, H=2, D=128, F=2, grid_h=2, grid_w=400, ref_frames=1, boundary_frames=1,
+                   ref_t=-1, steps=2, shift=1.0)
+    cs, xs, _ = run_stream_gpu(S, w, 5, 2)
+    assert not cs.fused_q_rope
+    want, _ = run_stream_oracle(w, 5, 2)
+    for c in range(2):
+        assert_close(f64(xs[c]), want[c], what=f"wide-grid chunk {c} x")
+    cs.close()
+    q = torch.zeros(1, w.n_q, w.H, w.D, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(S.SavgbError):
+        S.chunk_attention_qrope(q, (w.F, w.grid_h, w.grid_w), [(q, q)])
 
 
 def test_stream_small_pair(S):
     """Two chunks x 4 steps; chunk 1 attends over the boundary rolled from chunk 0."""
     w = I.WORKLOADS["small"]
     cs, xs, bnds = run_stream_gpu(S, w, 0, 2)
+    assert cs.fused_q_rope
     want, wbnds = run_stream_oracle(w, 0, 2)
     for c in range(2):
         assert_close(f64(xs[c]), want[c], what=f"small chunk {c} x")
