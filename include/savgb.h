@@ -129,10 +129,17 @@ int chunk_attention(const void* q, int B, int64_t n_q, int H, int D, const savgb
  * rope3d_apply reading: D/2 pairs split [t | h | w], pair j of an axis with P
  * pairs turning at base^(-j/P)).  Each block rotates its query tiles in
  * shared memory after loading them, which removes one read and one write of
- * q from HBM (on GB300 the block's start-up hand-off costs more than that
- * pass; chunk_stream_step keeps the separate rope3d pass).  Keys must already
- * be rotated.  Other arguments and errors as
+ * q from HBM.  The cos/sin table ([t rows | h | w] x pairs, fp32) is built on
+ * `stream` by a small kernel into a stream-ordered temporary
+ * (cudaMallocAsync / cudaFreeAsync, a few KB to tens of KB) and copied into
+ * each block's shared memory; chunk streams build theirs once at create.
+ * Keys must already be rotated.  Other arguments and errors as
  * chunk_attention; n_q must equal grid_t*grid_h*grid_w.
+ * SAVGB_ERR_UNSUPPORTED when a block's part of the table, 8 * (r*Pt +
+ * grid_h*Ph + grid_w*Pw) bytes with (Pt, Ph, Pw) the pairs per axis and r <=
+ * 255/(grid_h*grid_w) + 2 the time rows one 256-query block spans, exceeds
+ * the shared memory left beside the operands: 34560 bytes at D = 128 (a
+ * grid_h + grid_w of about 200), 67328 at D = 64.
  * ("The underlying model architecture": chunked latent video, reference and
  * boundary tokens as context.) */
 int chunk_attention_qrope(const void* q, int B, int64_t n_q, int H, int D, int grid_t, int grid_h,
