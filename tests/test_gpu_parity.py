@@ -603,6 +603,7 @@ def test_interp_state_and_resume(S):
     (64, 1, 2, 4, 4, 0, [16, 0]),            # tiny chunk
     (128, 2, 3, 7, 9, 1, [63, 200, 0]),      # ragged: 189 queries, B = 2, t0 = 1
     (128, 1, 8, 30, 52, 0, [1560, 3120]),    # base-DiT chunk (sampled rows)
+    (128, 1, 2, 4, 150, -3, [600, 0]),       # t0 < 0; a 26 KB table, near the shared-memory limit
 ])
 def test_attention_qrope_parity(S, D, B, gt, gh, gw, t0, segs):
     """Unrotated queries, rotated inside the kernel, against the oracle's
