@@ -299,7 +299,11 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
         },
         "latent_frames_per_s": round(frames_per_s, 1),
         "pct_of_bf16_peak": {"nominal_2250": round(100 * attn_tflops / NOMINAL_BF16_TFLOPS, 1),
-                             f"{pk_kind}_sustained": round(100 * attn_tflops / peak, 1)},
+                             f"{pk_kind}_sustained": round(100 * attn_tflops / peak, 1),
+                             f"{pk_kind}_burst": round(100 * attn_tflops / pk["bf16_tflops"], 1)},
+        # one exp per score: B*H*Nq*Nkv per attention launch
+        "softmax_exps": {"per_step": w.B * w.H * w.n_q * w.n_kv,
+                         "per_s": round(w.B * w.H * w.n_q * w.n_kv / (attn_ms * 1e-3), 1)},
         "kernels_timed_region": {"steps": args.steps, "ms_per_step": round(ms_step_instr, 4),
                                  "what": "a second K-step region with CUDA events around each stage of every step"},
         "kernels_ms": {("rope3d_k" if fused else "rope3d_qk"): round(rope_ms, 4),
@@ -309,6 +313,8 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
             "chunk_attention_tflops": round(attn_tflops, 1),
             "out_proj_euler_tflops": round(wo_flops / (wo_ms * 1e-3) / 1e12, 1),
             "rope3d_gbs": round(rope_bytes / (rope_ms * 1e-3) / 1e9, 1),
+            "rope3d_pct_of_hbm": {"nominal_8000": round(100 * rope_bytes / (rope_ms * 1e-3) / 8e12, 1),
+                                  f"{pk_kind}_copy": round(100 * rope_bytes / (rope_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 1)},
         },
         "roofline": {
             "kernel": ("chunk_attention_qrope (attn_fwd_kernel<128, 2, 2, true>: RoPE of q fused)" if fused
