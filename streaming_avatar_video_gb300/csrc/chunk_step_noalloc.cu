@@ -6,8 +6,9 @@
 // device synchronisation cudaMalloc/cudaFree may imply) is not allowed once
 // the session runs.  Those callers cannot create a chunk_stream handle, whose
 // arena is allocated at create.  This entry point runs the same step as
-// chunk_stream_step (RoPE of q and k, attention over the caller's context
-// segments plus the chunk, W_o with the Euler update) and keeps its
+// chunk_stream_step in its unfused form (RoPE of q and k in one launch,
+// attention over the caller's context segments plus the chunk, W_o with the
+// Euler update) and keeps its
 // intermediates - rotated q, rotated k and the attention output - in one
 // file-scope __device__ array of a fixed size instead.
 //

@@ -13,9 +13,13 @@
 //
 // The handle owns one device arena allocated at create and never grown:
 //   ref_k (rotated once) | ref_v | boundary k/v x 2 slots | q_rot | k_rot | o
-// A step enqueues, on the handle's stream: RoPE of q and k (one launch),
-// attention over [reference | boundary | chunk], then the W_o GEMM with the
-// Euler update fused into its epilogue.  The last step of a chunk also rotates
+//   | (interpolation anchors, block-step v) | cos/sin table of the q RoPE
+// A step enqueues, on the handle's stream: RoPE of k, attention over
+// [reference | boundary | chunk] with the RoPE of q applied inside the kernel
+// from the table built at create (or, when that table does not fit in the
+// kernel's shared memory, RoPE of q and k in one launch and the plain
+// attention), then the W_o GEMM with the Euler update fused into its
+// epilogue.  The last step of a chunk also rotates
 // the tail frames of its k into the spare boundary slot (t = -T_b .. -1) and
 // copies the tail of v; end_chunk swaps the slots.
 #include <cuda_bf16.h>
