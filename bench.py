@@ -47,8 +47,8 @@ METRIC = "chunk-attention TFLOP/s (% of bf16 tensor peak); latent frames/s per d
 # change of them reports null.
 ATTN_TRAFFIC = {
     # profiles/chunk_attention_base.md: the fused-RoPE kernel the stream runs at base,
-    # 289.085 MB read + 60.695 MB written
-    "8615deccde31ab04c77232ddc39a589aa894d94ed6a9ffe661175cc58cefef55": {"base": 349779968},
+    # 292.563 MB read + 61.584 MB written
+    "50a452a0f0b15e25abaf6529d2f8809bd093968a78d1e76f757daf1658ad9a68": {"base": 354147072},
 }
 
 

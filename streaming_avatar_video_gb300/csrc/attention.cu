@@ -13,7 +13,8 @@
 //               elected lane issues the copies.
 //   warp 1      allocates 512 TMEM columns and runs the MMA issue loop; one
 //               elected lane issues every tcgen05.mma.
-//   warp 3      idle (it completes the first warpgroup).
+//   warp 3      checks that each key tile's V and the next K have landed and
+//               adds one arrival to the P barrier of tile 0.
 //   warps 4-7   softmax of query tile 0, warps 8-11 of query tile 1; thread =
 //               one query row (TMEM lane), so row max and sum need no shuffle.
 // Registers: the block launches with 168 per thread; the first warpgroup
@@ -25,8 +26,10 @@
 // works on one tile's QK^T / PV while the other tile's softmax runs.
 // tcgen05.mma issue is nearly synchronous with execution (the unit holds
 // about one instruction ahead), so every clock the issuing thread spends
-// between MMAs idles the tensor core: the issue loop has three wait points
-// per key tile (V and K together, P of tile 0, P of tile 1) and no other work.
+// between MMAs idles the tensor core: the issue loop has two wait points per
+// key tile (P of tile 0, P of tile 1) and no other work.  A satisfied
+// mbarrier try_wait still costs it ~60 clocks, so the check that V(j) and
+// K(j+1) have landed is made by warp 3, which arrives on P of tile 0 too.
 // The running max is updated lazily (only when it grows by more than 2^8 in
 // probability), and O is rescaled in TMEM by the softmax warps when it is.
 // At the end each softmax warp normalises its 32 rows of O into the Q tile's
@@ -235,7 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       dev::mbar_init(&bars[L::kSFull + x], 1);
-      dev::mbar_init(&bars[L::kP + x], 4);  // one elected lane per softmax warp
+      // one elected lane per softmax warp; for tile 0 also warp 3 (V and K landed)
+      dev::mbar_init(&bars[L::kP + x], x == 0 ? 5 : 4);
       dev::mbar_init(&bars[L::kODone + x], 1);
     }
     dev::mbar_init(&bars[L::kDrain], 1);
@@ -326,6 +330,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (is_k) dev::mbar_wait(&bars[L::kQFull], 0, &never);
       for (int t = (issued > stages ? issued - stages : 0); t < issued; ++t)
         dev::mbar_wait(&full[t % stages], (t / stages) & 1, &never);
+    } else if (warp == 3) {
+      // ------------------------------------------------ V/K landing checks
+      // For every key tile j: V(j) and K(j+1) have landed, then one arrival
+      // on P of tile 0, so the MMA issuer's wait on that P covers them (a
+      // satisfied try_wait costs the issuer ~60 clocks).  The next arrival
+      // waits until this phase has completed, so it never counts towards it.
+      const bool elected = dev::elect_one();
+      for (int j = 0; j < n; ++j) {
+        const bool kv = j + 1 < n ? dev::mbar_wait2(&bars[L::kVFull + j % VS], (j / VS) & 1,
+                                                    &bars[L::kKFull + (j + 1) % KS], ((j + 1) / KS) & 1, abort)
+                                  : dev::mbar_wait(&bars[L::kVFull + j % VS], (j / VS) & 1, abort);
+        if (!__all_sync(0xffffffffu, kv)) {
+          if (elected) give_up(p, abort, 9);
+          break;
+        }
+        if (elected) dev::mbar_arrive(&bars[L::kP + 0]);
+        if (!__all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kP + 0], j & 1, abort))) break;
+      }
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
       // The whole warp runs the loop, so its state is warp-uniform; one
@@ -376,15 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int j = 0; j < n; ++j) {
           const int vst = j % VS;
-          const uint32_t vuse = j / VS;
           const bool more = j + 1 < n;
           const int kst1 = (j + 1) % KS;
-          const uint32_t kuse1 = (j + 1) / KS;
-          // V(j) and K(j+1) in one wait (both landed long before in steady state)
-          const bool kv_ok = more ? dev::mbar_wait2(&bars[L::kVFull + vst], vuse & 1, &bars[L::kKFull + kst1],
-                                                    kuse1 & 1, abort)
-                                  : dev::mbar_wait(&bars[L::kVFull + vst], vuse & 1, abort);
-          if (!__all_sync(0xffffffffu, kv_ok && dev::mbar_wait(&bars[L::kP + 0], j & 1, abort))) {
+          // P of tile 0 also means V(j) and K(j+1) have landed (warp 3)
+          if (!__all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kP + 0], j & 1, abort))) {
             if (leader) give_up(p, abort, 4);
             break;
           }
