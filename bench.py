@@ -47,8 +47,8 @@ METRIC = "chunk-attention TFLOP/s (% of bf16 tensor peak); latent frames/s per d
 # change of them reports null.
 ATTN_TRAFFIC = {
     # profiles/chunk_attention_base.md: the fused-RoPE kernel the stream runs at base,
-    # 292.563 MB read + 61.584 MB written
-    "50a452a0f0b15e25abaf6529d2f8809bd093968a78d1e76f757daf1658ad9a68": {"base": 354147072},
+    # 290.597 MB read + 60.385 MB written
+    "92e93434f32a6d12f42dadd0deb916e6575e7e211e02375ce46c309441fe0f1c": {"base": 350981888},
 }
 
 
@@ -317,8 +317,8 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
                                   f"{pk_kind}_copy": round(100 * rope_bytes / (rope_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 1)},
         },
         "roofline": {
-            "kernel": ("chunk_attention_qrope (attn_fwd_kernel<128, 2, 2, true>: RoPE of q fused)" if fused
-                       else "chunk_attention (attn_fwd_kernel<128, 3, 2, false>)"),
+            "kernel": ("chunk_attention_qrope (attn_fwd_kernel<128, 2, 2, true, false>: RoPE of q fused)" if fused
+                       else "chunk_attention (attn_fwd_kernel<128, 3, 2, false, false>)"),
             "bound": "tensor",
             "achieved": round(attn_tflops, 1),
             "peak": peak,

@@ -32,6 +32,10 @@
 // K(j+1) have landed is made by warp 3, which arrives on P of tile 0 too.
 // The running max is updated lazily (only when it grows by more than 2^8 in
 // probability), and O is rescaled in TMEM by the softmax warps when it is.
+// The probabilities come from one packed bf16x2 exp2 per two scores (their
+// exponents rounded to bf16), which yields the bf16 P operand directly; the
+// row sums add those same bf16 values in fp32.  When the log-sum-exp output is
+// asked for, an instantiation with fp32 exponentials and exact sums runs.
 // At the end each softmax warp normalises its 32 rows of O into the Q tile's
 // shared memory (free by then) and writes them with tensor-map stores.
 // Every wait is bounded; on a timeout the block records it in the device
@@ -208,7 +212,11 @@ __device__ __forceinline__ void rope_q_row(uint8_t* sQ, int tile_bytes, const fl
   }
 }
 
-template <int D, int KS, int VS, bool ROPE_Q>
+// EXACT_L: the row sums come from fp32 probabilities (one MUFU operation per
+// score), as the log-sum-exp output needs; otherwise from the bf16 ones of
+// the packed exponential (one operation per two scores), whose rounding
+// leaves the sum ~0.3 % low on average but matches the P the PV product uses.
+template <int D, int KS, int VS, bool ROPE_Q, bool EXACT_L>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ AttnParams p) {
   using L = Layout<D, KS, VS>;
@@ -534,10 +542,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 32; ++i) {
           float y0, y1;
           dev::ffma2(y0, y1, s[half * 64 + 2 * i], s[half * 64 + 2 * i + 1], sl2, nm);
-          const float p0 = dev::ex2_approx(y0);
-          const float p1 = dev::ex2_approx(y1);
-          dev::fadd2(l0, l1, p0, p1);
-          pk[i] = dev::pack_bf16x2(p0, p1);
+          if constexpr (EXACT_L) {
+            const float p0 = dev::ex2_approx(y0);
+            const float p1 = dev::ex2_approx(y1);
+            dev::fadd2(l0, l1, p0, p1);
+            pk[i] = dev::pack_bf16x2(p0, p1);
+          } else {
+            // p = 2^(s*scale - m) for two scores in one MUFU operation on the
+            // exponents rounded to bf16; the result is already P's MMA
+            // operand, and the row sum adds exactly those bf16 values in fp32
+            pk[i] = dev::ex2_bf16x2(dev::pack_bf16x2(y0, y1));
+            dev::add_bf16x2_to_f32(l0, l1, pk[i]);
+          }
         }
         dev::tmem_st32(tS + half * 32, pk);
       }
@@ -609,31 +625,35 @@ int make_token_map(CUtensorMap* m, const void* ptr, int B, int64_t N, int H, int
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// Sets a kernel's shared-memory limit and checks its register count against
+// the setmaxnreg split, once per device.
+template <typename Kernel>
+int prepare_kernel(Kernel kernel, bool* done) {
+  int dev_id = 0;
+  SAVGB_CUDA(cudaGetDevice(&dev_id));
+  if (done[dev_id & 63]) return SAVGB_OK;
+  SAVGB_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
+  cudaFuncAttributes fa;
+  SAVGB_CUDA(cudaFuncGetAttributes(&fa, kernel));
+  if (fa.numRegs * kThreads < kRegPoolNeeded)
+    return fail(SAVGB_ERR_UNSUPPORTED,
+                "chunk_attention: kernel built with %d registers/thread; its register split needs %d",
+                fa.numRegs, (kRegPoolNeeded + kThreads - 1) / kThreads);
+  done[dev_id & 63] = true;
+  return SAVGB_OK;
+}
+
 template <int D, int KS, int VS, bool ROPE_Q>
 int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, int n_segs,
                 float scale, void* o, float* lse, const QRope* rope, cudaStream_t stream) {
   using L = Layout<D, KS, VS>;
-  static bool attr_done[64] = {false};
-  int dev_id = 0;
-  SAVGB_CUDA(cudaGetDevice(&dev_id));
-  if (!attr_done[dev_id & 63]) {
-    SAVGB_CUDA(cudaFuncSetAttribute(attn_fwd_kernel<D, KS, VS, ROPE_Q>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    227 * 1024));
-    attr_done[dev_id & 63] = true;
-  }
-  static int regs_checked[64] = {0};
-  if (!regs_checked[dev_id & 63]) {
-    cudaFuncAttributes fa;
-    SAVGB_CUDA(cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, KS, VS, ROPE_Q>));
-    if (fa.numRegs * kThreads < kRegPoolNeeded)
-      return fail(SAVGB_ERR_UNSUPPORTED,
-                  "chunk_attention: kernel built with %d registers/thread; its register split needs %d",
-                  fa.numRegs, (kRegPoolNeeded + kThreads - 1) / kThreads);
-    regs_checked[dev_id & 63] = 1;
-  }
-  AttnMaps maps;
-  int rc = make_token_map(&maps.q, q, B, n_q, H, D);
+  // the log-sum-exp output takes the instantiation with exact row sums
+  static bool ready[2][64] = {};
+  auto kernel = lse ? attn_fwd_kernel<D, KS, VS, ROPE_Q, true> : attn_fwd_kernel<D, KS, VS, ROPE_Q, false>;
+  int rc = prepare_kernel(kernel, ready[lse ? 1 : 0]);
   if (rc) return rc;
+  AttnMaps maps;
+  if ((rc = make_token_map(&maps.q, q, B, n_q, H, D))) return rc;
   if ((rc = make_token_map(&maps.o, o, B, n_q, H, D, 32))) return rc;
   AttnParams p{};
   p.n_q = (int)n_q;
@@ -675,7 +695,7 @@ int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, i
   }
   if ((rc = error_word(&p.err))) return rc;
   dim3 grid((unsigned)((n_q + kBlockQ - 1) / kBlockQ), (unsigned)H, (unsigned)B);
-  SAVGB_CUDA(launch_dependent(attn_fwd_kernel<D, KS, VS, ROPE_Q>, grid, dim3(kThreads), dyn_smem, stream, maps, p));
+  SAVGB_CUDA(launch_dependent(kernel, grid, dim3(kThreads), dyn_smem, stream, maps, p));
   SAVGB_CUDA(cudaGetLastError());
   return SAVGB_OK;
 }

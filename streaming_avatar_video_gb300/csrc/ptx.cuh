@@ -428,6 +428,21 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 2^x of both bf16 halves of a bf16x2 word, one MUFU operation for the pair.
+__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// (a0, a1) += (low, high) bf16 halves of h, widened exactly, added in fp32.
+__device__ __forceinline__ void add_bf16x2_to_f32(float& a0, float& a1, uint32_t h) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(h));
+}
+
 // Packed fp32 pairs (sm_100+): one instruction for two lanes of work.
 // (y0, y1) = (x0 * a + c0, x1 * a + c1)
 __device__ __forceinline__ void ffma2(float& y0, float& y1, float x0, float x1, float a, float c) {
