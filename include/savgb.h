@@ -117,8 +117,12 @@ typedef struct {
  *   scale    softmax scale; <= 0 selects 1/sqrt(D).
  *   o        bf16 [B][n_q][H][D] output (must not alias q or any k/v).
  *   lse      optional fp32 [B][H][n_q]: natural-log sum of exp(scale*q.k).
- * D must be 64 or 128.  bf16 tensor-core products, fp32 accumulation and
- * softmax; probabilities rounded to bf16 for the PV product.
+ * D must be 64 or 128.  bf16 tensor-core products, fp32 accumulation; the
+ * probabilities are bf16 (the PV operand), from one packed bf16 exp2 per two
+ * scores with their exponents rounded to bf16, and the row sums add those
+ * bf16 values in fp32.  With lse non-NULL the kernel instead takes fp32
+ * exponentials and exact fp32 row sums (the packed form's sums run ~0.3 %
+ * low, which cancels in O but not in lse); that form is a few percent slower.
  * ------------------------------------------------------------------------ */
 int chunk_attention(const void* q, int B, int64_t n_q, int H, int D, const savgb_kv_segment* segs,
                     int n_segs, float scale, void* o, float* lse, void* stream);
