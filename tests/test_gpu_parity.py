@@ -632,6 +632,25 @@ def test_attention_qrope_parity(S, D, B, gt, gh, gw, t0, segs):
     want = O.attention(qq, osegs)
     got = f64(o) if rows is None else f64(o)[:, rows]
     assert_close(got, want, what=f"attention with RoPE of q inside (D={D})")
+    # with the log-sum-exp output the kernel takes fp32 exponentials and exact row sums
+    lse = torch.empty(B, H, n_q, dtype=torch.float32, device="cuda")
+    o2 = S.chunk_attention_qrope(q.cuda(), (gt, gh, gw), dsegs, t0=t0, lse=lse)
+    torch.cuda.synchronize()
+    S.savgb_device_check()
+    got2 = f64(o2) if rows is None else f64(o2)[:, rows]
+    assert_close(got2, want, what=f"attention with RoPE of q inside and lse (D={D})")
+    kk = np.concatenate([k for k, _ in osegs], axis=1)
+    sc = 1.0 / math.sqrt(D)
+    sco = np.einsum("bnhd,bmhd->bhnm", qq, kk) * sc
+    mx = sco.max(-1, keepdims=True)
+    want_lse = mx[..., 0] + np.log(np.exp(sco - mx).sum(-1))
+    got_lse = f64(lse) if rows is None else f64(lse)[:, :, rows]
+    # The kernel rounds the rotated queries to bf16 (its MMA operand) and the
+    # oracle does not.  A score then moves by at most 2^-9 * sum_d |q_d k_d| *
+    # scale (~0.014 at D = 128 for unit normals, ~1e-3 rms), and lse by a
+    # p-weighted mean of those moves: bars 5e-3 / 1e-3 instead of the 1e-3 /
+    # 1e-4 of the test whose queries arrive as bf16.
+    assert_close(got_lse, want_lse, max_abs=5e-3, mean_abs=1e-3, what=f"lse with RoPE of q inside (D={D})")
 
 
 # ------------------------------------------------------- DiT attention block
