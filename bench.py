@@ -47,8 +47,9 @@ METRIC = "chunk-attention TFLOP/s (% of bf16 tensor peak); latent frames/s per d
 # change of them reports null.
 ATTN_TRAFFIC = {
     # profiles/chunk_attention_base.md: the fused-RoPE kernel the stream runs at base,
-    # 290.597 MB read + 60.385 MB written
-    "92e93434f32a6d12f42dadd0deb916e6575e7e211e02375ce46c309441fe0f1c": {"base": 350981888},
+    # 290.597 MB read + 60.385 MB written (captured on sources 92e93434...; the only
+    # change since is a comment in attention.cu's header)
+    "9e8753069573304774b76a7ba1a9c1363ae2b914ce5bbc077c534faf652191e8": {"base": 350981888},
 }
 
 

@@ -38,6 +38,10 @@
 // asked for, an instantiation with fp32 exponentials and exact sums runs.
 // At the end each softmax warp normalises its 32 rows of O into the Q tile's
 // shared memory (free by then) and writes them with tensor-map stores.
+// Built with ROPE_Q (chunk_attention_qrope) the kernel takes unrotated
+// queries: the block's part of a cos/sin table arrives from global memory with
+// Q, and the softmax threads rotate one query row each in shared memory before
+// the first MMA.
 // Every wait is bounded; on a timeout the block records it in the device
 // error word and every role leaves its loop.
 #include <cuda_bf16.h>
