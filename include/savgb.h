@@ -344,9 +344,12 @@ int chunk_stream_destroy(chunk_stream_t* s);
  * [B][n][H][D].  q, k, v: bf16 [B][N][H][D], N = F*grid_h*grid_w; w_o bf16
  * [H*D][H*D]; bias optional fp32 [H*D]; x fp32 [B*N][H*D], updated in place.
  *
- * The step's intermediates (rotated q, rotated k, attention output: 3 x
- * B*N*H*D bf16, each rounded up to 256 bytes) live in one file-scope device
- * array of SAVGB_NOALLOC_SCRATCH_BYTES, which every device that loads the
+ * Like the stream, the step rotates q inside the attention kernel when that
+ * kernel's cos/sin table fits in its shared memory (rebuilt by every call),
+ * else q and k in one RoPE pass.  Its intermediates (rotated k, the attention
+ * output: 2 x B*N*H*D bf16, plus the table or rotated q, each rounded up to
+ * 256 bytes) live in one file-scope device array of
+ * SAVGB_NOALLOC_SCRATCH_BYTES, which every device that loads the
  * library holds until the process exits.  Larger steps are rejected with
  * SAVGB_ERR_INVALID_ARG.  The array's address is looked up on the first call
  * made on each device; make that call before any stream capture.  All calls

@@ -6,11 +6,13 @@
 // device synchronisation cudaMalloc/cudaFree may imply) is not allowed once
 // the session runs.  Those callers cannot create a chunk_stream handle, whose
 // arena is allocated at create.  This entry point runs the same step as
-// chunk_stream_step in its unfused form (RoPE of q and k in one launch,
-// attention over the caller's context segments plus the chunk, W_o with the
-// Euler update) and keeps its
-// intermediates - rotated q, rotated k and the attention output - in one
-// file-scope __device__ array of a fixed size instead.
+// chunk_stream_step (RoPE of k, attention over the caller's context segments
+// plus the chunk with the RoPE of q inside the kernel, W_o with the Euler
+// update; or, when the kernel's cos/sin table does not fit, RoPE of q and k
+// in one launch and the plain attention) and keeps its intermediates -
+// rotated k, the attention output and the table, or rotated q in its place -
+// in one file-scope __device__ array of a fixed size instead.  The table is
+// rebuilt by every call.
 //
 // The array exists once per device that loads this library and is held until
 // the process exits.  Its device address is looked up once per device (with
@@ -71,11 +73,15 @@ extern "C" int chunk_step_noalloc(const void* q, const void* k, const void* v,
   const int64_t n = (int64_t)F * grid_h * grid_w;
   const int64_t hid = (int64_t)H * D;
   const int64_t tensor_bytes = round256((int64_t)B * n * hid * 2);
-  const int64_t need = 3 * tensor_bytes;
-  if ((double)B * n * hid * 2 * 3 > (double)kScratchBytes || need > (int64_t)kScratchBytes)
+  // the fused form keeps the q RoPE table where the unfused one keeps rotated q
+  const bool fused = (D == 64 || D == 128) && grid_h <= 4096 && grid_w <= 4096 && qrope_fits(D, F, grid_h, grid_w);
+  const int64_t third = fused ? round256(rope_q_table_bytes(D, F, grid_h, grid_w)) : tensor_bytes;
+  const int64_t need = 2 * tensor_bytes + third;
+  if ((double)B * n * hid * 2 * 2 > (double)kScratchBytes || need > (int64_t)kScratchBytes)
     return fail(SAVGB_ERR_INVALID_ARG,
-                "chunk_step_noalloc: the step needs %lld bytes of scratch (3 x B*N*H*D bf16), more than "
-                "the fixed %zu bytes; use a chunk_stream handle for larger chunks",
+                "chunk_step_noalloc: the step needs %lld bytes of scratch (rotated k, attention output and the "
+                "q RoPE table or rotated q), more than the fixed %zu bytes; use a chunk_stream handle for "
+                "larger chunks",
                 (long long)need, kScratchBytes);
   if (hid > (1 << 24) || hid % 16) return fail(SAVGB_ERR_INVALID_ARG, "chunk_step_noalloc: H*D must be a multiple of 16");
   // shapes and pointers of the three launches, checked before any launch
@@ -97,15 +103,26 @@ extern "C" int chunk_step_noalloc(const void* q, const void* k, const void* v,
   void* base = nullptr;
   if ((rc = scratch_address(&base))) return rc;
   unsigned char* p = static_cast<unsigned char*>(base);
-  void* q_rot = p;
-  void* k_rot = p + tensor_bytes;
-  void* o = p + 2 * tensor_bytes;
+  void* k_rot = p;
+  void* o = p + tensor_bytes;
+  void* third_buf = p + 2 * tensor_bytes;  // the table (fused) or rotated q
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  aq.out = q_rot;
   ak.out = k_rot;
-  if ((rc = launch_rope_pair(aq, ak, st))) return rc;
   segs[n_context].k = k_rot;
-  if ((rc = launch_attention(q_rot, B, n, H, D, segs, n_context + 1, softmax_scale, o, nullptr, st)))
-    return rc;
+  if (fused) {
+    if ((rc = rope_q_table_build(third_buf, D, 0, F, grid_h, grid_w, rope_base, st))) return rc;
+    if ((rc = launch_rope(ak, st))) return rc;
+    QRope r{F, grid_h, grid_w, 0, rope_base};
+    r.tab = third_buf;
+    r.tab_t_lo = 0;
+    r.tab_t_n = F;
+    if ((rc = launch_attention_qrope(q, B, n, H, D, segs, n_context + 1, softmax_scale, r, o, nullptr, st)))
+      return rc;
+  } else {
+    aq.out = third_buf;
+    if ((rc = launch_rope_pair(aq, ak, st))) return rc;
+    if ((rc = launch_attention(third_buf, B, n, H, D, segs, n_context + 1, softmax_scale, o, nullptr, st)))
+      return rc;
+  }
   return launch_out_proj_euler(o, w_o, bias, x, (int64_t)B * n, (int)hid, (int)hid, dt, nullptr, st);
 }

@@ -29,7 +29,10 @@ def S():
     I.WORKLOADS["small"],
     I.Workload("d128", B=2, H=4, D=128, F=3, grid_h=8, grid_w=12, ref_frames=1, boundary_frames=1,
                steps=4, shift=3.0),
-], ids=["small", "d128"])
+    # a 2 x 400 grid: the q RoPE table does not fit the attention kernel, so both take the unfused form
+    I.Workload("wide", B=1, H=2, D=128, F=2, grid_h=2, grid_w=400, ref_frames=1, boundary_frames=1,
+               steps=2, shift=1.0),
+], ids=["small", "d128", "wide"])
 def test_noalloc_step_matches_stream_step(S, w):
     seed = 17
     rk, rv = I.reference_kv(w, seed)
@@ -67,7 +70,7 @@ def test_noalloc_step_matches_stream_step(S, w):
 
 
 def test_noalloc_rejects_steps_beyond_scratch(S):
-    # a base-DiT-sized chunk needs 3 x 12480 x 3072 x 2 bytes, beyond the fixed array
+    # a base-DiT-sized chunk needs 2 x 12480 x 3072 x 2 bytes and the RoPE table, beyond the fixed array
     w = I.WORKLOADS["base"]
     q = torch.zeros((1, 16, 24, 128), dtype=torch.bfloat16, device="cuda")  # pointers only
     wo = torch.zeros((w.hid, w.hid), dtype=torch.bfloat16, device="cuda")
