@@ -47,9 +47,8 @@ METRIC = "chunk-attention TFLOP/s (% of bf16 tensor peak); latent frames/s per d
 # change of them reports null.
 ATTN_TRAFFIC = {
     # profiles/chunk_attention_base.md: the fused-RoPE kernel the stream runs at base,
-    # 290.597 MB read + 60.385 MB written (captured on sources 92e93434...; the only
-    # change since is a comment in attention.cu's header)
-    "9e8753069573304774b76a7ba1a9c1363ae2b914ce5bbc077c534faf652191e8": {"base": 350981888},
+    # 289.926 MB read + 60.824 MB written
+    "7f4a80268126f06fc44d736eed0ecd60a517d71b2c6d9f8e8790771c06cc8607": {"base": 350749952},
 }
 
 

@@ -74,7 +74,7 @@ def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = N
         with concurrent.futures.ThreadPoolExecutor(max_workers=n) as ex:
             logs = list(ex.map(compile_one, todo))
     if todo or force or _stale(LIB_PATH, objs):
-        cmd = [nvcc, *ARCH, "-shared", "-o", LIB_PATH, *objs, "-lrt"]
+        cmd = [nvcc, *ARCH, "-shared", "-o", LIB_PATH, *objs, "-lrt", "-ldl"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

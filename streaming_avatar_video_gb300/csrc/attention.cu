@@ -834,6 +834,7 @@ extern "C" int chunk_attention(const void* q, int B, int64_t n_q, int H, int D,
                                const savgb_kv_segment* segs, int n_segs, float scale, void* o,
                                float* lse, void* stream) {
   using namespace savgb;
+  savgb::ApiRange api_range_("savgb:chunk_attention");
   clear_error();
   AttnSeg s[3] = {};
   if (segs && n_segs >= 1 && n_segs <= 3)
@@ -848,6 +849,7 @@ extern "C" int chunk_attention_qrope(const void* q, int B, int64_t n_q, int H, i
                                      int grid_w, int t0, double base, const savgb_kv_segment* segs, int n_segs,
                                      float scale, void* o, float* lse, void* stream) {
   using namespace savgb;
+  savgb::ApiRange api_range_("savgb:chunk_attention_qrope");
   clear_error();
   AttnSeg sg[3] = {};
   if (segs && n_segs >= 1 && n_segs <= 3)

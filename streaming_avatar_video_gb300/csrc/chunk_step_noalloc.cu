@@ -63,6 +63,7 @@ extern "C" int chunk_step_noalloc(const void* q, const void* k, const void* v,
                                   int grid_h, int grid_w, double rope_base, float softmax_scale,
                                   void* stream) {
   using namespace savgb;
+  savgb::ApiRange api_range_("savgb:chunk_step_noalloc");
   clear_error();
   if (!q || !k || !v || !w_o || !x) return fail(SAVGB_ERR_INVALID_ARG, "chunk_step_noalloc: null argument");
   if (n_context < 0 || n_context > 2 || (n_context > 0 && !context))

@@ -114,6 +114,7 @@ RopeArgs rope_args(const chunk_stream* s, const void* in, void* out, int64_t in_
 extern "C" {
 
 int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stream_t** out) {
+  savgb::ApiRange api_range_("savgb:chunk_stream_create");
   clear_error();
   if (!out) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_create: null out");
   *out = nullptr;
@@ -190,6 +191,7 @@ int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stre
 }
 
 int chunk_stream_set_reference(chunk_stream_t* s, const void* k_ref, const void* v_ref) {
+  savgb::ApiRange api_range_("savgb:chunk_stream_set_reference");
   clear_error();
   if (!s || !k_ref || !v_ref) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_set_reference: null argument");
   if (!aligned16(k_ref) || !aligned16(v_ref)) return fail(SAVGB_ERR_ALIGNMENT, "chunk_stream_set_reference: pointers must be 16-byte aligned");
@@ -210,6 +212,7 @@ int chunk_stream_set_reference(chunk_stream_t* s, const void* k_ref, const void*
 
 int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const void* v,
                       const void* w_o, const float* bias, float* x, float dt, int is_last_step) {
+  savgb::ApiRange api_range_("savgb:chunk_stream_step");
   clear_error();
   if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_step: null handle");
   if (!s->ref_set) return fail(SAVGB_ERR_STATE, "chunk_stream_step: set_reference has not been called");
@@ -293,6 +296,7 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
 
 int chunk_stream_istep(chunk_stream_t* s, const void* q, const void* k, const void* v,
                        const void* w_o, const float* bias, float* x, float dt) {
+  savgb::ApiRange api_range_("savgb:chunk_stream_istep");
   clear_error();
   if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_istep: null handle");
   const chunk_stream_config& c = s->cfg;
@@ -358,6 +362,7 @@ int chunk_stream_ichunk_index(const chunk_stream_t* s, int64_t* index) {
 
 int chunk_stream_block_step(chunk_stream_t* s, const void* w_qkv, const void* w_o, const float* bias,
                             float* x, float dt, int is_last_step) {
+  savgb::ApiRange api_range_("savgb:chunk_stream_block_step");
   clear_error();
   if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_block_step: null handle");
   const chunk_stream_config& c = s->cfg;
@@ -410,6 +415,7 @@ int chunk_stream_block_step(chunk_stream_t* s, const void* w_qkv, const void* w_
 }
 
 int chunk_stream_end_chunk(chunk_stream_t* s) {
+  savgb::ApiRange api_range_("savgb:chunk_stream_end_chunk");
   clear_error();
   if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_end_chunk: null handle");
   if (!s->captured)
@@ -439,6 +445,7 @@ int chunk_stream_set_step_events(chunk_stream_t* s, void* const* events) {
 }
 
 int chunk_stream_sync(chunk_stream_t* s) {
+  savgb::ApiRange api_range_("savgb:chunk_stream_sync");
   clear_error();
   if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_sync: null handle");
   return savgb_device_check(s->stream);
@@ -464,6 +471,7 @@ int chunk_stream_fused_q_rope(const chunk_stream_t* s, int* fused) {
 }
 
 int chunk_stream_export_state(chunk_stream_t* s, void* buf, size_t cap, size_t* size_out) {
+  savgb::ApiRange api_range_("savgb:chunk_stream_export_state");
   clear_error();
   if (!s || !size_out) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_export_state: null argument");
   const int64_t fr = (int64_t)s->cfg.grid_h * s->cfg.grid_w;
@@ -501,6 +509,7 @@ int chunk_stream_export_state(chunk_stream_t* s, void* buf, size_t cap, size_t* 
 }
 
 int chunk_stream_import_state(chunk_stream_t* s, const void* buf, size_t size) {
+  savgb::ApiRange api_range_("savgb:chunk_stream_import_state");
   clear_error();
   if (!s || !buf) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_import_state: null argument");
   if (size < sizeof(StateHeader)) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_import_state: truncated state");
@@ -539,6 +548,7 @@ int chunk_stream_import_state(chunk_stream_t* s, const void* buf, size_t size) {
 }
 
 int chunk_stream_destroy(chunk_stream_t* s) {
+  savgb::ApiRange api_range_("savgb:chunk_stream_destroy");
   clear_error();
   if (!s) return SAVGB_OK;
   cudaError_t e1 = cudaStreamSynchronize(s->stream);

@@ -1,6 +1,7 @@
 // Host-side helpers shared by the library's translation units.
 #pragma once
 
+#include <nvtx3/nvToolsExt.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -13,6 +14,15 @@ namespace savgb {
 int fail(int code, const char* fmt, ...);
 // Clears the thread-local message (called at the start of every entry point).
 void clear_error();
+
+// A named NVTX range around one C-ABI call, for profilers (ncu --nvtx
+// filters kernels by it); with no tool attached it costs a few nanoseconds.
+struct ApiRange {
+  explicit ApiRange(const char* name) { nvtxRangePushA(name); }
+  ~ApiRange() { nvtxRangePop(); }
+  ApiRange(const ApiRange&) = delete;
+  ApiRange& operator=(const ApiRange&) = delete;
+};
 // Maps a CUDA runtime error to SAVGB_ERR_CUDA / SAVGB_ERR_OOM with a message.
 int cuda_fail(cudaError_t e, const char* what);
 

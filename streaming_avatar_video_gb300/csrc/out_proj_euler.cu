@@ -613,6 +613,7 @@ extern "C" int out_proj_euler_step(const void* o, const void* w_o, const float* 
                                    int64_t M, int hid_in, int hid_out, float dt, float* v_out,
                                    void* stream) {
   using namespace savgb;
+  savgb::ApiRange api_range_("savgb:out_proj_euler_step");
   clear_error();
   int rc = validate_out_proj(o, w_o, bias, x, M, hid_in, hid_out, v_out);
   if (rc) return rc;

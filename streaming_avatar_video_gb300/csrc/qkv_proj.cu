@@ -254,6 +254,7 @@ extern "C" int qkv_rope_project(const void* x_bf16, const void* w_qkv, void* q, 
                                 int64_t n_tokens, int H, int D, int grid_t, int grid_h, int grid_w, int t0,
                                 double base, void* stream) {
   using namespace savgb;
+  savgb::ApiRange api_range_("savgb:qkv_rope_project");
   clear_error();
   QkvArgs a{x_bf16, w_qkv, q, k, v, nullptr, 0, B, n_tokens, H, D, grid_t, grid_h, grid_w, t0, base};
   int rc = validate_qkv(a);

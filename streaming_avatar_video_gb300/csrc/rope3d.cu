@@ -285,6 +285,7 @@ extern "C" int rope3d_apply(const void* in, void* out, int B, int64_t n_tokens, 
                             int grid_t, int grid_h, int grid_w, int t0, double base,
                             void* stream) {
   using namespace savgb;
+  savgb::ApiRange api_range_("savgb:rope3d_apply");
   clear_error();
   RopeArgs a{in, out, B, n_tokens, H, D, grid_t, grid_h, grid_w, t0, base,
              n_tokens * H * D, n_tokens * H * D};

@@ -152,6 +152,7 @@ const char* savgb_last_error(void) { return g_msg; }
 int savgb_version(void) { return 100; }
 
 int savgb_device_check(void* stream) {
+  savgb::ApiRange api_range_("savgb:savgb_device_check");
   clear_error();
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
@@ -170,6 +171,7 @@ int savgb_device_check(void* stream) {
 }
 
 int savgb_watchdog_selftest(uint64_t limit_ns, void* stream) {
+  savgb::ApiRange api_range_("savgb:savgb_watchdog_selftest");
   clear_error();
   int rc = check_device(nullptr);
   if (rc) return rc;
