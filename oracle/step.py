@@ -334,18 +334,27 @@ def block_step(x, w_qkv, ref_k_rot, ref_v, bnd_k_rot, bnd_v, w_o, dt, grid, H, D
 
 
 def run_stream_block(w, ref_k, ref_v, w_qkv, w_o, x0_per_chunk, dts, chunks, scale=None, bias=None):
-    """A stream of chunks through block_step, the boundary rolled from each
-    chunk's final-step projected k, v.  Returns the final x of every chunk."""
+    """A stream of chunks through block_step: reference K rotated once (its
+    frames ending at t = ref_t), each chunk run over the grid ``dts`` against
+    [reference | boundary | chunk], and the boundary of the next chunk taken
+    from the projected k, v of the chunk's final step (boundary_from_chunk).
+
+    Reading of "The underlying model architecture" (later chunks use boundary
+    data from the previous segments) with the block's own projection: the
+    carried tokens are the last frames' keys and values as the block computed
+    them at the chunk's last denoising step.
+    Returns (final x of every chunk, boundary (k_rot, v) used by every chunk)."""
     ref_k_rot = rope3d(ref_k, w.ref_frames, w.grid_h, w.grid_w, w.ref_t - w.ref_frames + 1, w.rope_base)
     empty = np.zeros((w.B, 0, w.H, w.D))
     bnd = (empty, empty)
-    xs = []
+    xs, bnds = [], []
     for c in range(chunks):
         x = x0_per_chunk(c)
+        bnds.append(bnd)
         for dt in dts:
             x, k, v = block_step(x, w_qkv, ref_k_rot, ref_v, bnd[0], bnd[1], w_o, dt,
                                  (w.F, w.grid_h, w.grid_w), w.H, w.D, w.rope_base, scale, bias)
         xs.append(x)
         if w.boundary_frames > 0:
             bnd = boundary_from_chunk(k, v, w.frame_tokens, w.boundary_frames, w.grid_h, w.grid_w, w.rope_base)
-    return xs
+    return xs, bnds

@@ -698,7 +698,7 @@ def test_stream_block_steps(S):
         xs.append(x.cpu())
     cs.sync()
     cs.close()
-    want = O.run_stream_block(w, f64(rk), f64(rv), f64(wqkv), f64(wo),
+    want, _ = O.run_stream_block(w, f64(rk), f64(rv), f64(wqkv), f64(wo),
                               lambda c: I.normal_f32((w.B * w.n_q, w.hid), 1.0, seed, I.KIND_X, c).astype(np.float64),
                               O.time_grid(w.steps, w.shift), 2)
     for c in range(2):

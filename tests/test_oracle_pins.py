@@ -560,3 +560,124 @@ def test_block_step_is_projection_then_chunk_step():
     x2, _ = O.chunk_step(q2, k2, v2, rk, rv, empty, empty, wo, x, 0.3, (F, gh, gw))
     assert np.allclose(x1, x2, atol=1e-12)
     assert np.allclose(k, k2, atol=1e-12) and np.allclose(v, v2, atol=1e-12)
+
+
+# ------------------------------------------ block stream (rolled boundary) ----
+
+def _block_stream_case(seed=31):
+    from streaming_avatar_video_gb300.inputs import Workload
+    w = Workload("tb", B=1, H=2, D=8, F=2, grid_h=2, grid_w=2, ref_frames=1, boundary_frames=1,
+                 steps=2, shift=1.0, chunks=3)
+    rng = np.random.default_rng(seed)
+    rk, rv = rng.standard_normal((1, w.n_ref, w.H, w.D)), rng.standard_normal((1, w.n_ref, w.H, w.D))
+    wq = rng.standard_normal((3 * w.hid, w.hid)) / math.sqrt(w.hid)
+    wo = rng.standard_normal((w.hid, w.hid)) / math.sqrt(w.hid)
+    bias = rng.standard_normal(w.hid) / 4
+    x0 = {c: rng.standard_normal((w.B * w.n_q, w.hid)) for c in range(3)}
+    return w, rk, rv, wq, wo, bias, x0, [0.375, 0.625]
+
+
+def _brute_block_stream(w, rk, rv, wq, wo, bias, x0, dts, chunks, base=10000.0):
+    """The block stream written as literal loops: the state is projected to
+    q, k, v by a triple loop, every head vector rotated pair by pair, attention
+    by explicit sums over [reference | boundary | chunk], W_o by a triple loop
+    and the Euler update element by element.  The boundary of chunk c+1 is the
+    last frame of chunk c's keys and values as projected at its final step, the
+    keys rotated to t = -1."""
+    H, D, hid = w.H, w.D, w.hid
+    ref_rot = _brute.rope_block(rk, w.ref_frames, w.grid_h, w.grid_w, w.ref_t - w.ref_frames + 1, base)[0]
+    ref_v = [[list(map(float, hv)) for hv in tok] for tok in rv[0]]
+    bnd_k, bnd_v = [], []
+    xs, used = [], []
+    for c in range(chunks):
+        used.append((bnd_k, bnd_v))
+        x = [list(map(float, r)) for r in x0[c]]
+        for dt in dts:
+            qkv = _brute.linear(x, wq.tolist())
+            split = lambda i: [[r[i * hid + hh * D: i * hid + (hh + 1) * D] for hh in range(H)] for r in qkv]  # noqa: E731
+            q, k, v = split(0), split(1), split(2)
+            qr = _brute.rope_block([q], w.F, w.grid_h, w.grid_w, 0, base)[0]
+            kr = _brute.rope_block([k], w.F, w.grid_h, w.grid_w, 0, base)[0]
+            o = _brute.attend(qr, ref_rot + bnd_k + kr, ref_v + bnd_v + v, 1.0 / math.sqrt(D))
+            vel = _brute.linear([[e for hv in tok for e in hv] for tok in o], wo.tolist(), bias.tolist())
+            x = [[x[i][j] + dt * vel[i][j] for j in range(hid)] for i in range(len(x))]
+        xs.append(np.array(x))
+        tail = w.n_q - w.n_b
+        bnd_k = _brute.rope_block([k[tail:]], w.boundary_frames, w.grid_h, w.grid_w, -w.boundary_frames, base)[0]
+        bnd_v = [[list(hv) for hv in tok] for tok in v[tail:]]
+    return xs, used
+
+
+def pin_stream_block(run=O.run_stream_block):
+    w, rk, rv, wq, wo, bias, x0, dts = _block_stream_case()
+    xs, bnds = run(w, rk, rv, wq, wo, lambda c: x0[c], np.array(dts), 3, None, bias)
+    want_x, want_b = _brute_block_stream(w, rk, rv, wq, wo, bias, x0, dts, 3)
+    assert len(xs) == 3 and len(bnds) == 3
+    assert bnds[0][0].shape[1] == 0
+    for c in range(3):
+        assert np.allclose(xs[c], want_x[c], atol=1e-12), f"chunk {c} x"
+        if c > 0:
+            assert np.allclose(bnds[c][0][0], np.array(want_b[c][0]), atol=1e-12), f"chunk {c} boundary k"
+            assert np.allclose(bnds[c][1][0], np.array(want_b[c][1]), atol=1e-12), f"chunk {c} boundary v"
+
+
+def test_stream_block_equals_brute_force():
+    pin_stream_block()
+
+
+def test_stream_block_boundary_is_last_step_tail():
+    """Chunk c+1's boundary is the tail of chunk c's final-step projection:
+    the k, v that block_step returns for the last dt, k rotated to -T_b..-1."""
+    w, rk, rv, wq, wo, bias, x0, dts = _block_stream_case(seed=32)
+    xs, bnds = O.run_stream_block(w, rk, rv, wq, wo, lambda c: x0[c], np.array(dts), 2, None, bias)
+    rk_rot = O.rope3d(rk, 1, w.grid_h, w.grid_w, -1)
+    empty = np.zeros((1, 0, w.H, w.D))
+    x = x0[0]
+    x, k0, v0 = O.block_step(x, wq, rk_rot, rv, empty, empty, wo, dts[0], (w.F, w.grid_h, w.grid_w), w.H, w.D,
+                             bias=bias)
+    x, k1, v1 = O.block_step(x, wq, rk_rot, rv, empty, empty, wo, dts[1], (w.F, w.grid_h, w.grid_w), w.H, w.D,
+                             bias=bias)
+    assert np.allclose(xs[0], x, atol=1e-13)
+    tail = w.n_q - w.n_b
+    assert np.allclose(bnds[1][0], O.rope3d(k1[:, tail:], 1, w.grid_h, w.grid_w, -1), atol=1e-14)
+    assert np.array_equal(bnds[1][1], v1[:, tail:])
+    # the first step's projection differs, so a roll from it would be caught
+    assert not np.allclose(k0[:, tail:], k1[:, tail:], atol=1e-3)
+
+
+def _planted_block_stream(first_step_boundary=False, ref_t_shift=0):
+    def run(w, ref_k, ref_v, w_qkv, w_o, x0_per_chunk, dts, chunks, scale=None, bias=None):
+        ref_k_rot = O.rope3d(ref_k, w.ref_frames, w.grid_h, w.grid_w,
+                             w.ref_t - w.ref_frames + 1 + ref_t_shift, w.rope_base)
+        empty = np.zeros((w.B, 0, w.H, w.D))
+        bnd = (empty, empty)
+        xs, bnds = [], []
+        for c in range(chunks):
+            x = x0_per_chunk(c)
+            bnds.append(bnd)
+            kv = None
+            for dt in dts:
+                x, k, v = O.block_step(x, w_qkv, ref_k_rot, ref_v, bnd[0], bnd[1], w_o, dt,
+                                       (w.F, w.grid_h, w.grid_w), w.H, w.D, w.rope_base, scale, bias)
+                if kv is None or not first_step_boundary:
+                    kv = (k, v)
+            xs.append(x)
+            bnd = O.boundary_from_chunk(kv[0], kv[1], w.frame_tokens, w.boundary_frames, w.grid_h, w.grid_w,
+                                        w.rope_base)
+        return xs, bnds
+    return run
+
+
+def test_planted_block_stream_first_step_boundary():
+    # the boundary rolled from the chunk's first step instead of its last
+    _expect_pin_failure(pin_stream_block, _planted_block_stream(first_step_boundary=True))
+
+
+def test_planted_block_stream_reference_time():
+    # the reference rotated at t = 0 instead of t = -1
+    _expect_pin_failure(pin_stream_block, _planted_block_stream(ref_t_shift=1))
+
+
+def test_planted_block_stream_control():
+    # the planted copy with no mistake passes the pin (the two above fail for their mistake alone)
+    pin_stream_block(_planted_block_stream())
