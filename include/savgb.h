@@ -102,6 +102,8 @@ typedef struct {
   const void* v;
   int64_t n_tokens;
 } savgb_kv_segment;
+/* The same segment under the name the problem statement's interface uses. */
+typedef savgb_kv_segment kv_segment_t;
 
 /* --------------------------------------------------------------------------
  * chunk_attention - queries of the current chunk attend over the
@@ -149,6 +151,17 @@ int chunk_attention(const void* q, int B, int64_t n_q, int H, int D, const savgb
 int chunk_attention_qrope(const void* q, int B, int64_t n_q, int H, int D, int grid_t, int grid_h,
                           int grid_w, int t0, double base, const savgb_kv_segment* segs, int n_segs,
                           float scale, void* o, float* lse, void* stream);
+
+/* chunk_attention_qrope_fits - host query, no device work: *fits = 1 when
+ * the block's part of the cos/sin table for a grid_t x grid_h x grid_w query
+ * grid fits in the attention kernel's shared memory (the limit stated for
+ * chunk_attention_qrope), else 0; *fits = 0 for a head_dim other than 64 or
+ * 128.  The same test picks the RoPE form of chunk_stream_step and
+ * chunk_step_noalloc: q rotated inside the attention kernel when it fits,
+ * one RoPE pass over q and k otherwise.  SAVGB_ERR_INVALID_ARG for a grid
+ * size below 1 or a NULL fits.  (A library facility; the pages have no
+ * counterpart.) */
+int chunk_attention_qrope_fits(int D, int grid_t, int grid_h, int grid_w, int* fits);
 
 /* --------------------------------------------------------------------------
  * out_proj_euler_step - output projection of the attention, taken as the
@@ -224,6 +237,8 @@ typedef struct {
   int interp_chunks;   /* nonzero: keep the anchors of interpolation chunks (needs F >= 3) */
   int qkv_block;       /* nonzero: reserve room for chunk_stream_block_step */
 } chunk_stream_config;
+/* The same config under the name the problem statement's interface uses. */
+typedef chunk_stream_config chunk_stream_config_t;
 
 typedef struct chunk_stream chunk_stream_t;
 

@@ -860,3 +860,14 @@ extern "C" int chunk_attention_qrope(const void* q, int B, int64_t n_q, int H, i
   if ((rc = validate_qrope(r, n_q, D))) return rc;
   return launch_attention_qrope(q, B, n_q, H, D, sg, n_segs, scale, r, o, lse, static_cast<cudaStream_t>(stream));
 }
+
+extern "C" int chunk_attention_qrope_fits(int D, int grid_t, int grid_h, int grid_w, int* fits) {
+  using namespace savgb;
+  clear_error();
+  if (!fits) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope_fits: null output");
+  *fits = 0;
+  if (grid_t < 1 || grid_h < 1 || grid_w < 1)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope_fits: grid sizes must be >= 1");
+  *fits = (grid_h <= 4096 && grid_w <= 4096 && qrope_fits(D, grid_t, grid_h, grid_w)) ? 1 : 0;
+  return SAVGB_OK;
+}

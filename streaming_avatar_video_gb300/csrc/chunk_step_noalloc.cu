@@ -52,8 +52,6 @@ int scratch_address(void** out) {
   return SAVGB_OK;
 }
 
-int64_t round256(int64_t v) { return (v + 255) / 256 * 256; }
-
 }  // namespace
 }  // namespace savgb
 
@@ -68,23 +66,31 @@ extern "C" int chunk_step_noalloc(const void* q, const void* k, const void* v,
   if (!q || !k || !v || !w_o || !x) return fail(SAVGB_ERR_INVALID_ARG, "chunk_step_noalloc: null argument");
   if (n_context < 0 || n_context > 2 || (n_context > 0 && !context))
     return fail(SAVGB_ERR_INVALID_ARG, "chunk_step_noalloc: 0 to 2 context segments");
-  if (B < 1 || H < 1 || F < 1 || grid_h < 1 || grid_w < 1)
-    return fail(SAVGB_ERR_INVALID_ARG, "chunk_step_noalloc: B, H, F, grid_h, grid_w must be >= 1");
+  if (B < 1 || B > 65535 || H < 1 || H > 65535 || F < 1 || grid_h < 1 || grid_w < 1)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_step_noalloc: B, H in [1, 65535]; F, grid_h, grid_w >= 1");
+  if (F > 4096 || grid_h > 4096 || grid_w > 4096)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_step_noalloc: F, grid_h and grid_w must be <= 4096");
+  if (D != 64 && D != 128) return fail(SAVGB_ERR_UNSUPPORTED, "chunk_step_noalloc: head_dim %d (64 or 128)", D);
   if (!std::isfinite(dt)) return fail(SAVGB_ERR_INVALID_ARG, "chunk_step_noalloc: dt must be finite");
+  // every size below is bounded now: n <= 2^36, hid <= 2^24, B < 2^16
   const int64_t n = (int64_t)F * grid_h * grid_w;
   const int64_t hid = (int64_t)H * D;
-  const int64_t tensor_bytes = round256((int64_t)B * n * hid * 2);
-  // the fused form keeps the q RoPE table where the unfused one keeps rotated q
-  const bool fused = (D == 64 || D == 128) && grid_h <= 4096 && grid_w <= 4096 && qrope_fits(D, F, grid_h, grid_w);
-  const int64_t third = fused ? round256(rope_q_table_bytes(D, F, grid_h, grid_w)) : tensor_bytes;
-  const int64_t need = 2 * tensor_bytes + third;
-  if ((double)B * n * hid * 2 * 2 > (double)kScratchBytes || need > (int64_t)kScratchBytes)
+  if (hid > (1 << 24) || hid % 16)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_step_noalloc: H*D = %lld must be a multiple of 16 and at most 2^24",
+                (long long)hid);
+  // the fused form keeps the q RoPE table where the unfused one keeps rotated q;
+  // the sizes are summed in double, which is exact here and cannot overflow
+  const bool fused = qrope_fits(D, F, grid_h, grid_w);
+  const double tensor_d = std::ceil((double)B * (double)n * (double)hid * 2.0 / 256.0) * 256.0;
+  const double third_d = fused ? std::ceil((double)rope_q_table_bytes(D, F, grid_h, grid_w) / 256.0) * 256.0 : tensor_d;
+  const double need = 2.0 * tensor_d + third_d;
+  if (need > (double)kScratchBytes)
     return fail(SAVGB_ERR_INVALID_ARG,
-                "chunk_step_noalloc: the step needs %lld bytes of scratch (rotated k, attention output and the "
+                "chunk_step_noalloc: the step needs %.0f bytes of scratch (rotated k, attention output and the "
                 "q RoPE table or rotated q), more than the fixed %zu bytes; use a chunk_stream handle for "
                 "larger chunks",
-                (long long)need, kScratchBytes);
-  if (hid > (1 << 24) || hid % 16) return fail(SAVGB_ERR_INVALID_ARG, "chunk_step_noalloc: H*D must be a multiple of 16");
+                need, kScratchBytes);
+  const int64_t tensor_bytes = (int64_t)tensor_d;
   // shapes and pointers of the three launches, checked before any launch
   RopeArgs aq{q, (void*)16, B, n, H, D, F, grid_h, grid_w, 0, rope_base, n * hid, n * hid};
   RopeArgs ak = aq;

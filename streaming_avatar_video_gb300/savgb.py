@@ -32,7 +32,7 @@ EXPORTS = (
     "chunk_stream_end_chunk", "chunk_stream_set_step_events", "chunk_stream_sync", "chunk_stream_info", "chunk_stream_export_state",
     "chunk_stream_import_state", "chunk_stream_destroy", "chunk_step_noalloc",
     "chunk_stream_istep", "chunk_stream_end_ichunk", "chunk_stream_ichunk_index", "chunk_attention_qrope",
-    "qkv_rope_project", "chunk_stream_block_step", "chunk_stream_fused_q_rope",
+    "qkv_rope_project", "chunk_stream_block_step", "chunk_stream_fused_q_rope", "chunk_attention_qrope_fits",
 )
 
 
@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
         "chunk_stream_set_step_events": (c_int, [c_vp, ctypes.POINTER(c_vp)]),
         "chunk_stream_sync": (c_int, [c_vp]),
         "chunk_stream_fused_q_rope": (c_int, [c_vp, ctypes.POINTER(c_int)]),
+        "chunk_attention_qrope_fits": (c_int, [c_int, c_int, c_int, c_int, ctypes.POINTER(c_int)]),
         "chunk_stream_info": (c_int, [c_vp, ctypes.POINTER(c_i64), ctypes.POINTER(c_i64), ctypes.POINTER(c_i64),
                                       ctypes.POINTER(c_vp), ctypes.POINTER(c_vp)]),
         "chunk_stream_export_state": (c_int, [c_vp, c_vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]),
@@ -191,6 +192,8 @@ def chunk_attention(q: torch.Tensor, segments: Sequence[Tuple[torch.Tensor, torc
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", torch.bfloat16, 4)
+    if out.shape != q.shape:
+        raise ValueError("out must have the shape of q")
     if lse is not None:
         _need(lse, "lse", torch.float32)
         if lse.numel() != B * H * Nq:
@@ -207,6 +210,9 @@ def chunk_attention_qrope(q: torch.Tensor, grid, segments: Sequence[Tuple[torch.
     the kernel; grid = (grid_t, grid_h, grid_w) of the queries."""
     _need(q, "q", torch.bfloat16, 4)
     B, Nq, H, D = q.shape
+    gt, gh, gw = (int(g) for g in grid)
+    if min(gt, gh, gw) < 1 or Nq != gt * gh * gw:
+        raise ValueError(f"q has {Nq} tokens, the grid {gt}x{gh}x{gw} holds {gt * gh * gw}")
     if not 1 <= len(segments) <= 3:
         raise ValueError("1 to 3 segments")
     segs = (KVSegment * 3)()
@@ -215,16 +221,33 @@ def chunk_attention_qrope(q: torch.Tensor, grid, segments: Sequence[Tuple[torch.
         if n > 0:
             _need(k, f"segments[{i}].k", torch.bfloat16, 4)
             _need(v, f"segments[{i}].v", torch.bfloat16, 4)
+            if k.shape != (B, n, H, D) or v.shape != k.shape:
+                raise ValueError(f"segment {i} must be [B][n][H][D] like q")
             segs[i] = KVSegment(k.data_ptr(), v.data_ptr(), n)
         else:
             segs[i] = KVSegment(None, None, 0)
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", torch.bfloat16, 4)
-    gt, gh, gw = grid
+    if out.shape != q.shape:
+        raise ValueError("out must have the shape of q")
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+        if lse.numel() != B * H * Nq:
+            raise ValueError("lse must hold B*H*n_q floats")
     _check(lib().chunk_attention_qrope(q.data_ptr(), B, Nq, H, D, gt, gh, gw, t0, float(base), segs, len(segments),
                                        float(scale), out.data_ptr(), _ptr(lse), _stream(stream)))
     return out
+
+
+def chunk_attention_qrope_fits(D: int, grid) -> bool:
+    """Host query: whether the RoPE of q can run inside the attention kernel
+    for this query grid (grid_t, grid_h, grid_w), the test that picks the
+    RoPE form of the stream steps and of chunk_step_noalloc."""
+    f = ctypes.c_int()
+    gt, gh, gw = grid
+    _check(lib().chunk_attention_qrope_fits(int(D), int(gt), int(gh), int(gw), ctypes.byref(f)))
+    return bool(f.value)
 
 
 def qkv_rope_project(x_bf16: torch.Tensor, w_qkv: torch.Tensor, grid, H: int, D: int, t0: int = 0,
@@ -313,6 +336,8 @@ class ChunkStream:
             raise ValueError("w_o must be [hid][hid] and x [B*N][hid]")
         if bias is not None:
             _need(bias, "bias", torch.float32, 1)
+            if bias.numel() != hid:
+                raise ValueError("bias must hold hid floats")
         _check(lib().chunk_stream_step(self.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(), w_o.data_ptr(),
                                        _ptr(bias), x.data_ptr(), float(dt), int(bool(is_last_step))))
 
@@ -329,8 +354,13 @@ class ChunkStream:
                 raise ValueError(f"{name} must be {shp}")
         _need(w_o, "w_o", torch.bfloat16, 2)
         _need(x, "x", torch.float32)
+        hid = c.H * c.D
+        if tuple(w_o.shape) != (hid, hid) or x.numel() != shp[0] * shp[1] * hid:
+            raise ValueError("w_o must be [hid][hid] and x [B*(F-2)*h*w][hid]")
         if bias is not None:
             _need(bias, "bias", torch.float32, 1)
+            if bias.numel() != hid:
+                raise ValueError("bias must hold hid floats")
         _check(lib().chunk_stream_istep(self.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(), w_o.data_ptr(),
                                         _ptr(bias), x.data_ptr(), float(dt)))
 
@@ -348,6 +378,8 @@ class ChunkStream:
             raise ValueError("x must be [B*N][hid]")
         if bias is not None:
             _need(bias, "bias", torch.float32, 1)
+            if bias.numel() != hid:
+                raise ValueError("bias must hold hid floats")
         _check(lib().chunk_stream_block_step(self.handle, w_qkv.data_ptr(), w_o.data_ptr(), _ptr(bias), x.data_ptr(),
                                              float(dt), int(bool(is_last_step))))
 
@@ -451,18 +483,29 @@ def chunk_step_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     B, N, H, D = q.shape
     if k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must have one shape")
+    F, gh, gw = (int(g) for g in grid)
+    if min(F, gh, gw) < 1 or N != F * gh * gw:
+        raise ValueError(f"q has {N} tokens, the grid {F}x{gh}x{gw} holds {F * gh * gw}")
+    hid = H * D
     if len(context) > 2:
         raise ValueError("0 to 2 context segments")
     segs = (KVSegment * 2)()
     for i, (ck, cv) in enumerate(context):
         _need(ck, f"context[{i}].k", torch.bfloat16, 4)
         _need(cv, f"context[{i}].v", torch.bfloat16, 4)
+        if ck.shape[0] != B or tuple(ck.shape[2:]) != (H, D) or cv.shape != ck.shape:
+            raise ValueError(f"context[{i}] k and v must both be [B][n][H][D] = [{B}][n][{H}][{D}]")
         segs[i] = KVSegment(ck.data_ptr(), cv.data_ptr(), ck.shape[1])
     _need(w_o, "w_o", torch.bfloat16, 2)
+    if tuple(w_o.shape) != (hid, hid):
+        raise ValueError(f"w_o must be [{hid}][{hid}]")
     _need(x, "x", torch.float32)
+    if x.numel() != B * N * hid:
+        raise ValueError(f"x must hold B*N*H*D = {B * N * hid} floats")
     if bias is not None:
         _need(bias, "bias", torch.float32, 1)
-    F, gh, gw = grid
+        if bias.numel() != hid:
+            raise ValueError(f"bias must hold {hid} floats")
     _check(lib().chunk_step_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), segs, len(context), w_o.data_ptr(),
                                     _ptr(bias), x.data_ptr(), float(dt), B, H, D, F, gh, gw, float(rope_base),
                                     float(softmax_scale), _stream(stream)))

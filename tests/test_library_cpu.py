@@ -99,3 +99,38 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(savgb, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         savgb.lib()
+
+
+def test_qrope_fits_query(S):
+    """The host query that picks the RoPE form: every configured grid fits,
+    a 2 x 400 grid (table past the shared-memory limit) does not, another
+    head_dim never does, and a grid size below 1 is refused."""
+    for D, grid in [(64, (2, 4, 4)), (64, (4, 16, 16)), (128, (8, 30, 52)), (128, (8, 60, 104)), (128, (3, 8, 12))]:
+        assert S.chunk_attention_qrope_fits(D, grid), (D, grid)
+    assert not S.chunk_attention_qrope_fits(128, (2, 2, 400))
+    assert not S.chunk_attention_qrope_fits(96, (2, 4, 4))
+    with pytest.raises(S.SavgbError):
+        S.chunk_attention_qrope_fits(128, (0, 4, 4))
+    assert S.lib().chunk_attention_qrope_fits(128, 1, 1, 1, None) == -1
+
+
+def test_noalloc_validates_before_any_device_call(S):
+    """chunk_step_noalloc refuses, on the host, a step beyond its fixed
+    scratch array (naming the array's size, also for sizes whose product
+    would overflow), out-of-range counts, an unsupported head_dim and a
+    non-finite dt."""
+    L = S.lib()
+    c_vp = ctypes.c_void_p
+    p = c_vp(256)
+    # base-DiT chunk: 2 x 12480 x 3072 x 2 bytes alone exceed the array
+    assert L.chunk_step_noalloc(p, p, p, None, 0, p, None, p, 0.1, 1, 24, 128, 8, 30, 52, 1e4, 0.0, None) == -1
+    msg = L.savgb_last_error().decode()
+    assert "scratch" in msg and str(S.NOALLOC_SCRATCH_BYTES) in msg
+    # sizes whose product would overflow 64-bit arithmetic are refused the same way
+    assert L.chunk_step_noalloc(p, p, p, None, 0, p, None, p, 0.1, 65535, 65535, 128, 4096, 4096, 4096, 1e4, 0.0,
+                                None) == -1
+    # heads beyond the launch grid's limit
+    assert L.chunk_step_noalloc(p, p, p, None, 0, p, None, p, 0.1, 1, 65536, 128, 1, 1, 1, 1e4, 0.0, None) == -1
+    assert L.chunk_step_noalloc(p, p, p, None, 0, p, None, p, 0.1, 1, 2, 96, 1, 4, 4, 1e4, 0.0, None) == -2
+    assert L.chunk_step_noalloc(p, p, p, None, 3, p, None, p, 0.1, 1, 2, 64, 1, 4, 4, 1e4, 0.0, None) == -1
+    assert L.chunk_step_noalloc(p, p, p, None, 0, p, None, p, float("nan"), 1, 2, 64, 1, 4, 4, 1e4, 0.0, None) == -1
