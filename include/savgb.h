@@ -138,7 +138,8 @@ int chunk_attention(const void* q, int B, int64_t n_q, int H, int D, const savgb
  * q from HBM.  The cos/sin table ([t rows | h | w] x pairs, fp32) is built on
  * `stream` by a small kernel into a stream-ordered temporary
  * (cudaMallocAsync / cudaFreeAsync, a few KB to tens of KB) and copied into
- * each block's shared memory; chunk streams build theirs once at create.
+ * each block's shared memory; chunk streams build theirs once at create, and
+ * chunk_attention_qrope_with_table (below) takes one the caller built.
  * Keys must already be rotated.  Other arguments and errors as
  * chunk_attention; n_q must equal grid_t*grid_h*grid_w.
  * SAVGB_ERR_UNSUPPORTED when a block's part of the table, 8 * (r*Pt +
@@ -151,6 +152,29 @@ int chunk_attention(const void* q, int B, int64_t n_q, int H, int D, const savgb
 int chunk_attention_qrope(const void* q, int B, int64_t n_q, int H, int D, int grid_t, int grid_h,
                           int grid_w, int t0, double base, const savgb_kv_segment* segs, int n_segs,
                           float scale, void* o, float* lse, void* stream);
+
+/* chunk_attention_qrope with a caller-built cos/sin table, for callers that
+ * run the stand-alone fused call in a loop and want no allocation per call.
+ *   chunk_attention_qrope_table_bytes: host query, *bytes = the table's size
+ *     for a grid_t x grid_h x grid_w query grid at head_dim D (64 or 128;
+ *     grid sizes in [1, 4096]).  No device work.
+ *   chunk_attention_qrope_build_table: fills `table` (caller-owned device
+ *     memory of at least that many bytes, 16-byte aligned) on `stream` for
+ *     time values t0 .. t0+grid_t-1 and the whole grid_h x grid_w grid at
+ *     rotary base `base` (one small kernel).
+ *   chunk_attention_qrope_with_table: chunk_attention_qrope that reads such a
+ *     table instead of building one; D, the grid and t0 must be those the
+ *     table was built for (the table carries the base).  The table must stay
+ *     unchanged until the call's kernel has run (stream order).  Other
+ *     arguments, errors and limits as chunk_attention_qrope.
+ * (Library facilities over the same computation; the pages have no
+ * counterpart.) */
+int chunk_attention_qrope_table_bytes(int D, int grid_t, int grid_h, int grid_w, int64_t* bytes);
+int chunk_attention_qrope_build_table(void* table, int D, int grid_t, int grid_h, int grid_w, int t0, double base,
+                                      void* stream);
+int chunk_attention_qrope_with_table(const void* q, int B, int64_t n_q, int H, int D, int grid_t, int grid_h,
+                                     int grid_w, int t0, const void* table, const savgb_kv_segment* segs,
+                                     int n_segs, float scale, void* o, float* lse, void* stream);
 
 /* chunk_attention_qrope_fits - host query, no device work: *fits = 1 when
  * the block's part of the cos/sin table for a grid_t x grid_h x grid_w query

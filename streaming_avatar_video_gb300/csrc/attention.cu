@@ -871,3 +871,53 @@ extern "C" int chunk_attention_qrope_fits(int D, int grid_t, int grid_h, int gri
   *fits = (grid_h <= 4096 && grid_w <= 4096 && qrope_fits(D, grid_t, grid_h, grid_w)) ? 1 : 0;
   return SAVGB_OK;
 }
+
+extern "C" int chunk_attention_qrope_table_bytes(int D, int grid_t, int grid_h, int grid_w, int64_t* bytes) {
+  using namespace savgb;
+  clear_error();
+  if (!bytes) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope_table_bytes: null output");
+  *bytes = 0;
+  if (D != 64 && D != 128) return fail(SAVGB_ERR_UNSUPPORTED, "chunk_attention_qrope_table_bytes: head_dim %d", D);
+  if (grid_t < 1 || grid_h < 1 || grid_w < 1 || grid_t > 4096 || grid_h > 4096 || grid_w > 4096)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope_table_bytes: grid sizes must be in [1, 4096]");
+  *bytes = rope_q_table_bytes(D, grid_t, grid_h, grid_w);
+  return SAVGB_OK;
+}
+
+extern "C" int chunk_attention_qrope_build_table(void* table, int D, int grid_t, int grid_h, int grid_w, int t0,
+                                                 double base, void* stream) {
+  using namespace savgb;
+  savgb::ApiRange api_range_("savgb:chunk_attention_qrope_build_table");
+  clear_error();
+  if (!table) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope_build_table: null table");
+  if (!aligned16(table)) return fail(SAVGB_ERR_ALIGNMENT, "chunk_attention_qrope_build_table: table not 16-byte aligned");
+  if (D != 64 && D != 128) return fail(SAVGB_ERR_UNSUPPORTED, "chunk_attention_qrope_build_table: head_dim %d", D);
+  const QRope r{grid_t, grid_h, grid_w, t0, base};
+  int rc = validate_qrope(r, (int64_t)grid_t * grid_h * grid_w, D);
+  if (rc) return rc;
+  if (grid_t > 4096) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope_build_table: grid_t > 4096");
+  if ((rc = check_device(nullptr))) return rc;
+  return rope_q_table_build(table, D, t0, grid_t, grid_h, grid_w, base, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int chunk_attention_qrope_with_table(const void* q, int B, int64_t n_q, int H, int D, int grid_t,
+                                                int grid_h, int grid_w, int t0, const void* table,
+                                                const savgb_kv_segment* segs, int n_segs, float scale, void* o,
+                                                float* lse, void* stream) {
+  using namespace savgb;
+  savgb::ApiRange api_range_("savgb:chunk_attention_qrope_with_table");
+  clear_error();
+  if (!table) return fail(SAVGB_ERR_INVALID_ARG, "chunk_attention_qrope_with_table: null table");
+  AttnSeg sg[3] = {};
+  if (segs && n_segs >= 1 && n_segs <= 3)
+    for (int i = 0; i < n_segs; ++i) sg[i] = AttnSeg{segs[i].k, segs[i].v, segs[i].n_tokens};
+  int rc = validate_attention(q, B, n_q, H, D, segs ? sg : nullptr, n_segs, o);
+  if (rc) return rc;
+  // the table holds the angles, so the base only has to pass validation here
+  QRope r{grid_t, grid_h, grid_w, t0, 1.0};
+  r.tab = table;
+  r.tab_t_lo = t0;
+  r.tab_t_n = grid_t;
+  if ((rc = validate_qrope(r, n_q, D))) return rc;
+  return launch_attention_qrope(q, B, n_q, H, D, sg, n_segs, scale, r, o, lse, static_cast<cudaStream_t>(stream));
+}

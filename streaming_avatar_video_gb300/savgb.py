@@ -33,6 +33,7 @@ EXPORTS = (
     "chunk_stream_import_state", "chunk_stream_destroy", "chunk_step_noalloc",
     "chunk_stream_istep", "chunk_stream_end_ichunk", "chunk_stream_ichunk_index", "chunk_attention_qrope",
     "qkv_rope_project", "chunk_stream_block_step", "chunk_stream_fused_q_rope", "chunk_attention_qrope_fits",
+    "chunk_attention_qrope_table_bytes", "chunk_attention_qrope_build_table", "chunk_attention_qrope_with_table",
 )
 
 
@@ -94,6 +95,10 @@ def lib() -> ctypes.CDLL:
         "chunk_stream_sync": (c_int, [c_vp]),
         "chunk_stream_fused_q_rope": (c_int, [c_vp, ctypes.POINTER(c_int)]),
         "chunk_attention_qrope_fits": (c_int, [c_int, c_int, c_int, c_int, ctypes.POINTER(c_int)]),
+        "chunk_attention_qrope_table_bytes": (c_int, [c_int, c_int, c_int, c_int, ctypes.POINTER(c_i64)]),
+        "chunk_attention_qrope_build_table": (c_int, [c_vp, c_int, c_int, c_int, c_int, c_int, c_d, c_vp]),
+        "chunk_attention_qrope_with_table": (c_int, [c_vp, c_int, c_i64, c_int, c_int, c_int, c_int, c_int, c_int,
+                                                     c_vp, ctypes.POINTER(KVSegment), c_int, c_f, c_vp, c_vp, c_vp]),
         "chunk_stream_info": (c_int, [c_vp, ctypes.POINTER(c_i64), ctypes.POINTER(c_i64), ctypes.POINTER(c_i64),
                                       ctypes.POINTER(c_vp), ctypes.POINTER(c_vp)]),
         "chunk_stream_export_state": (c_int, [c_vp, c_vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]),
@@ -237,6 +242,64 @@ def chunk_attention_qrope(q: torch.Tensor, grid, segments: Sequence[Tuple[torch.
             raise ValueError("lse must hold B*H*n_q floats")
     _check(lib().chunk_attention_qrope(q.data_ptr(), B, Nq, H, D, gt, gh, gw, t0, float(base), segs, len(segments),
                                        float(scale), out.data_ptr(), _ptr(lse), _stream(stream)))
+    return out
+
+
+def chunk_attention_qrope_table(D: int, grid, t0: int = 0, base: float = 10000.0, stream=None) -> torch.Tensor:
+    """A cos/sin table for chunk_attention_qrope_with_table, built on the
+    device for the query grid (grid_t, grid_h, grid_w) starting at time t0
+    (the tensor is allocated here, by torch, once; the library allocates
+    nothing)."""
+    gt, gh, gw = (int(g) for g in grid)
+    n = ctypes.c_int64()
+    _check(lib().chunk_attention_qrope_table_bytes(int(D), gt, gh, gw, ctypes.byref(n)))
+    tab = torch.empty(n.value, dtype=torch.uint8, device="cuda")
+    _check(lib().chunk_attention_qrope_build_table(tab.data_ptr(), int(D), gt, gh, gw, int(t0), float(base),
+                                                   _stream(stream)))
+    return tab
+
+
+def chunk_attention_qrope_with_table(q: torch.Tensor, grid, table: torch.Tensor,
+                                     segments: Sequence[Tuple[torch.Tensor, torch.Tensor]], t0: int = 0,
+                                     out: Optional[torch.Tensor] = None, scale: float = 0.0,
+                                     lse: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """chunk_attention_qrope reading a table from chunk_attention_qrope_table
+    (same D, grid and t0) instead of building one per call."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(table, "table", torch.uint8, 1)
+    B, Nq, H, D = q.shape
+    gt, gh, gw = (int(g) for g in grid)
+    if min(gt, gh, gw) < 1 or Nq != gt * gh * gw:
+        raise ValueError(f"q has {Nq} tokens, the grid {gt}x{gh}x{gw} holds {gt * gh * gw}")
+    n = ctypes.c_int64()
+    _check(lib().chunk_attention_qrope_table_bytes(D, gt, gh, gw, ctypes.byref(n)))
+    if table.numel() < n.value:
+        raise ValueError(f"table holds {table.numel()} bytes, the grid needs {n.value}")
+    if not 1 <= len(segments) <= 3:
+        raise ValueError("1 to 3 segments")
+    segs = (KVSegment * 3)()
+    for i, (k, v) in enumerate(segments):
+        nk = k.shape[1] if k.dim() == 4 else 0
+        if nk > 0:
+            _need(k, f"segments[{i}].k", torch.bfloat16, 4)
+            _need(v, f"segments[{i}].v", torch.bfloat16, 4)
+            if k.shape != (B, nk, H, D) or v.shape != k.shape:
+                raise ValueError(f"segment {i} must be [B][n][H][D] like q")
+            segs[i] = KVSegment(k.data_ptr(), v.data_ptr(), nk)
+        else:
+            segs[i] = KVSegment(None, None, 0)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 4)
+    if out.shape != q.shape:
+        raise ValueError("out must have the shape of q")
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+        if lse.numel() != B * H * Nq:
+            raise ValueError("lse must hold B*H*n_q floats")
+    _check(lib().chunk_attention_qrope_with_table(q.data_ptr(), B, Nq, H, D, gt, gh, gw, int(t0), table.data_ptr(),
+                                                  segs, len(segments), float(scale), out.data_ptr(), _ptr(lse),
+                                                  _stream(stream)))
     return out
 
 

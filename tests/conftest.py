@@ -24,3 +24,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Achieved errors of the full-size parity checks (those that also assert
+    the margin below the bars), as a table at the end of the run."""
+    try:
+        from tests import _util
+    except Exception:  # pragma: no cover
+        return
+    if not _util.RECORD:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", f"parity margins (bars max-abs {_util.MAX_ABS:g} / mean-abs {_util.MEAN_ABS:g}; "
+                      f"full-size checks held to {_util.MARGIN:.0%} of them)")
+    for what, mx, mn, bmx, bmn in _util.RECORD:
+        tr.write_line(f"{what}: max-abs {mx:.2e} ({mx / bmx:.1%} of bar), mean-abs {mn:.2e} ({mn / bmn:.1%} of bar)")

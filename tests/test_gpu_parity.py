@@ -77,7 +77,7 @@ def test_rope3d_identity_at_origin(S):
 
 # -------------------------------------------------------------- attention
 
-def attn_case(S, B, H, D, n_q, seg_lens, seed, scale=0.0, rows=None, lse=False, q_scale=1.0):
+def attn_case(S, B, H, D, n_q, seg_lens, seed, scale=0.0, rows=None, lse=False, q_scale=1.0, margin=False):
     q = bf16((B, n_q, H, D), seed, I.KIND_Q, std=q_scale)
     segs = [(bf16((B, n, H, D), seed, I.KIND_K, chunk=i), bf16((B, n, H, D), seed, I.KIND_V, chunk=i))
             for i, n in enumerate(seg_lens)]
@@ -91,7 +91,7 @@ def attn_case(S, B, H, D, n_q, seg_lens, seed, scale=0.0, rows=None, lse=False, 
     qq = f64(q) if rows is None else f64(q)[:, rows]
     want = O.attention(qq, [(f64(k), f64(v)) for k, v in segs], sc)
     got = f64(o) if rows is None else f64(o)[:, rows]
-    assert_close(got, want, what=f"attention B{B} H{H} D{D} nq{n_q} segs{seg_lens}")
+    assert_close(got, want, what=f"attention B{B} H{H} D{D} nq{n_q} segs{seg_lens}", margin=margin)
     if lse:
         kk = np.concatenate([f64(k) for k, _ in segs], axis=1)
         s = np.einsum("bnhd,bmhd->bhnm", qq, kk) * sc
@@ -142,7 +142,7 @@ def test_attention_full_size_sampled_rows(S, name):
     rng = np.random.default_rng(0)
     rows = np.unique(np.concatenate([rng.choice(w.n_q, 40, replace=False),
                                      [0, 127, 128, 255, w.n_q - 129, w.n_q - 65, w.n_q - 1]]))
-    attn_case(S, w.B, w.H, w.D, w.n_q, [w.n_ref, w.n_b, w.n_q], 21, rows=rows)
+    attn_case(S, w.B, w.H, w.D, w.n_q, [w.n_ref, w.n_b, w.n_q], 21, rows=rows, margin=True)
 
 
 # ------------------------------------------------------- W_o + Euler update
@@ -418,7 +418,7 @@ def test_stream_step_full_size_sampled_rows(S, name):
     k_rot = O.rope3d(f64(st1.k), w.F, w.grid_h, w.grid_w, 0, w.rope_base)
     o = O.attention(q_rot, [(rk_rot, f64(rv)), (bk_rot, bv), (k_rot, f64(st1.v))])
     want = O.euler_update(f64(x0)[rows], O.out_proj(o.reshape(len(rows), w.hid), f64(wo)), dt)
-    assert_close(f64(got)[rows], want, what=f"{name} step x (sampled rows)")
+    assert_close(f64(got)[rows], want, what=f"{name} step x (sampled rows)", margin=True)
 
 
 def _stream_sampled_rows(S, w, seed, chunk_dts, rows, check_chunks):
@@ -456,7 +456,8 @@ def _stream_sampled_rows(S, w, seed, chunk_dts, rows, check_chunks):
         if c in check_chunks:
             got = x.cpu()
             for b in range(w.B):
-                assert_close(f64(got)[x_rows_of[b]], want[b], what=f"{w.name} chunk {c} session {b} x (sampled rows)")
+                assert_close(f64(got)[x_rows_of[b]], want[b], what=f"{w.name} chunk {c} session {b} x (sampled rows)",
+                             margin=True)
         bnd = O.boundary_from_chunk(f64(last_kv[0]), f64(last_kv[1]), w.frame_tokens, w.boundary_frames,
                                     w.grid_h, w.grid_w, w.rope_base)
     cs.close()
@@ -631,7 +632,13 @@ def test_attention_qrope_parity(S, D, B, gt, gh, gw, t0, segs):
     qq = q_rot if rows is None else q_rot[:, rows]
     want = O.attention(qq, osegs)
     got = f64(o) if rows is None else f64(o)[:, rows]
-    assert_close(got, want, what=f"attention with RoPE of q inside (D={D})")
+    assert_close(got, want, what=f"attention with RoPE of q inside (D={D}, grid {gt}x{gh}x{gw})", margin=n_q > 512)
+    # the same kernel reading a table the caller built once: bit-identical output
+    tab = S.chunk_attention_qrope_table(D, (gt, gh, gw), t0)
+    o_tab = S.chunk_attention_qrope_with_table(q.cuda(), (gt, gh, gw), tab, dsegs, t0=t0)
+    torch.cuda.synchronize()
+    S.savgb_device_check()
+    assert torch.equal(o_tab, o)
     # with the log-sum-exp output the kernel takes fp32 exponentials and exact row sums
     lse = torch.empty(B, H, n_q, dtype=torch.float32, device="cuda")
     o2 = S.chunk_attention_qrope(q.cuda(), (gt, gh, gw), dsegs, t0=t0, lse=lse)
