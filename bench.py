@@ -84,58 +84,128 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock, power draw and clock-event (throttle) reasons sampled during
+    a timed region.  Read-only NVML queries through ctypes every 5 ms on a
+    thread of this process, so that even a region of a few tens of
+    milliseconds gets samples under load; nvidia-smi -lms 25 when the NVML
+    library cannot be loaded.  Nothing here changes a setting of the GPU."""
 
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
+    def __init__(self, device: int, period_s: float = 0.005):
+        self.device = device
+        self.period = period_s
+        self.samples = []  # (sm MHz, power W, reasons bitmask)
+        self.sm_max = None
+        self.source = None
+        self._nvml = None
+        self._h = None
+        self._proc = None
+
+    def _open_nvml(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return False
+            h = ctypes.c_void_p()
+            ok = False
+            props = torch.cuda.get_device_properties(self.device)
+            if all(hasattr(props, a) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+                bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+                ok = lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) == 0
+            if not ok:
+                ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.device), ctypes.byref(h)) == 0
+            if not ok:
+                return False
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+                self.sm_max = float(mx.value)
+            self._reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._nvml, self._h = lib, h
+            return True
+        except Exception:
+            return False
+
+    def _poll(self):
+        import ctypes
+        lib, h = self._nvml, self._h
+        mhz, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
+                lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+                self._reasons(h, ctypes.byref(rs))
+                self.samples.append((float(mhz.value), mw.value / 1000.0, int(rs.value)))
+            self._stop.wait(self.period)
 
     def __enter__(self):
+        import threading
+        if self._open_nvml():
+            self.source = "nvml"
+            self._stop = threading.Event()
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+            return self
+        self.source = "nvidia-smi"
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
-            self.proc = None
+            self._proc = None
         time.sleep(0.25)
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            time.sleep(0.15)
-            self.proc.terminate()
+        if self.source == "nvml":
+            self._stop.set()
+            self._thread.join(timeout=1.0)
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self._nvml.nvmlShutdown()
             except Exception:
-                self.proc.kill()
-                out = ""
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
-
-    def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+                pass
+            return
+        if self._proc is None:
+            return
+        time.sleep(0.15)
+        self._proc.terminate()
+        try:
+            out, _ = self._proc.communicate(timeout=5)
+        except Exception:
+            self._proc.kill()
+            out = ""
+        names = {5: 0x8, 6: 0x40, 7: 0x20, 8: 0x4}
+        for ln in out.splitlines():
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                sm, mx, pw = float(f[1]), float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for name, val in zip(names, f[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+            bits = 0
+            for i, b in names.items():
+                if f[i].lower() == "active":
+                    bits |= b
+            self.samples.append((sm, pw, bits))
+            self.sm_max = mx
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.sm_max, "reasons": [], "samples": 0, "source": self.source}
+        bits = 0
+        for _, _, b in self.samples:
+            bits |= b
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples), "sm_max_mhz": self.sm_max,
+                "reasons": sorted(n for b, n in self.REASONS.items() if bits & b),
+                "power_w_median": round(statistics.median(s[1] for s in self.samples), 1),
+                "samples": len(self.samples), "source": self.source}
 
 
 def dist_setup(backend: str = "nccl"):
@@ -483,18 +553,20 @@ def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world):
     torch.cuda.synchronize()
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    base = 3
-    for i in range(base, base + n):
-        step(i, upload_next=True)
-    stream.wait_event(out_done[0])
-    b.record(stream)
-    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        a.record(stream)
+        base = 3
+        for i in range(base, base + n):
+            step(i, upload_next=True)
+        stream.wait_event(out_done[0])
+        b.record(stream)
+        torch.cuda.synchronize()
     ms = max_over_ranks(world, a.elapsed_time(b)) / n
     h2d = sum(t.numel() * t.element_size() for t in sets[0])
     d2h = x.numel() * x.element_size()
     return {"value": round(whole_job_rate(world, w.attn_flops(True), ms) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "clocks": clk.summary(),
             "api": "ChunkStream.step (C ABI chunk_stream_step) with pinned host q/k/v in and x out; uploads of "
                    "the next step and read-back of the previous one overlap the step on two copy streams"}
 

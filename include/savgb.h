@@ -73,6 +73,29 @@ int savgb_device_check(void* stream);
  * failure reporting without faulting or hanging the GPU. */
 int savgb_watchdog_selftest(uint64_t limit_ns, void* stream);
 
+/* Diagnostic with no counterpart on the pages: arms a one-shot fault in the
+ * next launch of one of the library's kernels, so that a test can run that
+ * kernel's own give-up path without faulting or hanging the GPU.
+ *   SAVGB_FAULT_ATTENTION_K_TILE  the attention kernel (any of its entry
+ *       points, the chunk-stream steps included): in the block of batch 0,
+ *       head 0, first query block, the key producer skips the copy of key
+ *       tile `index` (and the arrival that goes with it);
+ *   SAVGB_FAULT_WO_PAIR_RELAY  the W_o CTA-pair kernel (out_proj_euler_step
+ *       with no v_out and hid_out % 256 == 0, and the stream steps): the odd
+ *       CTA of the first cluster skips its "stage full" relay of k-block
+ *       iteration `index`.  Other W_o launches leave the arm in place.
+ * Every bounded wait of that launch gives up after limit_ns nanoseconds
+ * (0 < limit_ns <= 1e10) instead of 2 s; the kernel records the timeout in
+ * the device error word, waits (bounded) for its own copies and MMAs in
+ * flight, frees its tensor memory and returns, and the next
+ * savgb_device_check() returns SAVGB_ERR_TIMEOUT.  That launch's outputs are
+ * undefined.  The arm is process-wide and taken by the next launch of that
+ * kernel from any thread; index < 0 disarms.  SAVGB_ERR_INVALID_ARG for an
+ * unknown kind or a limit out of range. */
+#define SAVGB_FAULT_ATTENTION_K_TILE 1
+#define SAVGB_FAULT_WO_PAIR_RELAY 2
+int savgb_arm_wait_fault(int kind, int index, uint64_t limit_ns);
+
 /* --------------------------------------------------------------------------
  * rope3d_apply - 3D (t, h, w) rotary position embedding.
  *

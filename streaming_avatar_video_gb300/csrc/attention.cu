@@ -98,6 +98,10 @@ struct AttnParams {
   int tab_t_rows;      // time rows one block's 256 queries can span
   int tab_h_sec;       // entries of the h section (padded to 16 bytes)
   int tab_hw_entries;  // entries of the h and w sections
+  // failure-path test hook (savgb_arm_wait_fault): key tile whose copy the K
+  // producer of block (0, 0, 0) skips (-1: none), and the limit of every wait
+  int fault_tile;
+  uint64_t wait_limit_ns;
 };
 
 template <int D, int KS, int VS>
@@ -292,6 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* ring = smem + (is_k ? L::kK : L::kV);
       uint64_t* full = &bars[is_k ? L::kKFull : L::kVFull];
       uint64_t* empty = &bars[is_k ? L::kKEmpty : L::kVEmpty];
+      // test hook: block (0, 0, 0) leaves one key tile uncopied (fault_tile < 0: never)
+      const int skip = (is_k && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) ? p.fault_tile : -1;
       if (is_k && elected) {
         uint8_t* sQ = smem + L::kQ;
         if constexpr (ROPE_Q) {
@@ -322,11 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_of(p, j, seg, row0, valid);
         const int st = j % stages;
         const uint32_t use = j / stages;
-        if (j >= stages && !__all_sync(0xffffffffu, dev::mbar_wait(&empty[st], (use - 1) & 1, abort))) {
+        if (j >= stages && !__all_sync(0xffffffffu, dev::mbar_wait(&empty[st], (use - 1) & 1, abort, p.wait_limit_ns))) {
           if (elected) give_up(p, abort, is_k ? 1 : 2);
           break;
         }
-        if (elected) {
+        if (elected && j != skip) {
           dev::mbar_arrive_expect_tx(&full[st], L::kTileBytes);
           #pragma unroll
           for (int c = 0; c < D / 64; ++c)
@@ -339,9 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // drain: every issued copy has landed before the block may exit
       volatile int never = 0;
-      if (is_k) dev::mbar_wait(&bars[L::kQFull], 0, &never);
+      if (is_k) dev::mbar_wait(&bars[L::kQFull], 0, &never, p.wait_limit_ns);
       for (int t = (issued > stages ? issued - stages : 0); t < issued; ++t)
-        dev::mbar_wait(&full[t % stages], (t / stages) & 1, &never);
+        dev::mbar_wait(&full[t % stages], (t / stages) & 1, &never, p.wait_limit_ns);
     } else if (warp == 3) {
       // ------------------------------------------------ V/K landing checks
       // For every key tile j: V(j) and K(j+1) have landed, then one arrival
@@ -351,14 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool elected = dev::elect_one();
       for (int j = 0; j < n; ++j) {
         const bool kv = j + 1 < n ? dev::mbar_wait2(&bars[L::kVFull + j % VS], (j / VS) & 1,
-                                                    &bars[L::kKFull + (j + 1) % KS], ((j + 1) / KS) & 1, abort)
-                                  : dev::mbar_wait(&bars[L::kVFull + j % VS], (j / VS) & 1, abort);
+                                                    &bars[L::kKFull + (j + 1) % KS], ((j + 1) / KS) & 1, abort, p.wait_limit_ns)
+                                  : dev::mbar_wait(&bars[L::kVFull + j % VS], (j / VS) & 1, abort, p.wait_limit_ns);
         if (!__all_sync(0xffffffffu, kv)) {
           if (elected) give_up(p, abort, 9);
           break;
         }
         if (elected) dev::mbar_arrive(&bars[L::kP + 0]);
-        if (!__all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kP + 0], j & 1, abort))) break;
+        if (!__all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kP + 0], j & 1, abort, p.wait_limit_ns))) break;
       }
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
@@ -396,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           dev::mma_ts(d, tmem + x * 128 + kk * 8, b0 + static_cast<uint32_t>(kk * (2048 >> 4)), idesc_o,
                       (acc || kk > 0) ? 1u : 0u);
       };
-      const bool ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[ROPE_Q ? L::kQReady : L::kQFull], 0, abort) &&
-                                                  dev::mbar_wait(&bars[L::kKFull], 0, abort));
+      const bool ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[ROPE_Q ? L::kQReady : L::kQFull], 0, abort, p.wait_limit_ns) &&
+                                                  dev::mbar_wait(&bars[L::kKFull], 0, abort, p.wait_limit_ns));
       if (!ok && leader) give_up(p, abort, 3);
       if (ok) {
         dev::tc_fence_after();
@@ -413,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool more = j + 1 < n;
           const int kst1 = (j + 1) % KS;
           // P of tile 0 also means V(j) and K(j+1) have landed (warp 3)
-          if (!__all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kP + 0], j & 1, abort))) {
+          if (!__all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kP + 0], j & 1, abort, p.wait_limit_ns))) {
             if (leader) give_up(p, abort, 4);
             break;
           }
@@ -425,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               dev::mma_commit(&bars[L::kSFull + 0]);
             }
           }
-          if (!__all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kP + 1], j & 1, abort))) {
+          if (!__all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kP + 1], j & 1, abort, p.wait_limit_ns))) {
             if (leader) give_up(p, abort, 6);
             break;
           }
@@ -449,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) dev::mma_commit(&bars[L::kDrain]);
       __syncwarp();
       volatile int never = 0;
-      dev::mbar_wait(&bars[L::kDrain], 0, &never);
+      dev::mbar_wait(&bars[L::kDrain], 0, &never, p.wait_limit_ns);
     }
   } else {
     dev::setmaxnreg_inc<kRegsHigh>();
@@ -458,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the table arrived with Q; one thread rotates one query row
       const float2* tab = reinterpret_cast<const float2*>(smem + L::kTab);
       const int r = (warp - 4) * 32 + lane;  // 0..255
-      const bool qok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kQFull], 0, abort));
+      const bool qok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kQFull], 0, abort, p.wait_limit_ns));
       if (qok) {
         if (q0 + r < p.n_q) rope_q_row<D>(smem + L::kQ, L::kTileBytes, tab, r, q0, p);
         // the rotated tiles are read by the tensor core (async proxy)
@@ -484,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int seg, row0, valid;
       tile_of(p, j, seg, row0, valid);
       // every lane polls the barrier; a vote keeps the warp on one path
-      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kSFull + x], j & 1, abort));
+      ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kSFull + x], j & 1, abort, p.wait_limit_ns));
       if (!ok) {
         give_up(p, abort, 7);
         break;
@@ -567,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) dev::mbar_arrive(&bars[L::kP + x]);
       l += l0 + l1;
     }
-    if (ok) ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kODone + x], 0, abort));
+    if (ok) ok = __all_sync(0xffffffffu, dev::mbar_wait(&bars[L::kODone + x], 0, abort, p.wait_limit_ns));
     if (ok) {
       dev::tc_fence_after();
       const int q = q0 + x * 128 + row;
@@ -698,6 +704,13 @@ int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, i
     dyn_smem = std::max<int>(dyn_smem, L::kTab + 1024 + (int)tab);
   }
   if ((rc = error_word(&p.err))) return rc;
+  p.fault_tile = -1;
+  p.wait_limit_ns = dev::kWaitLimitNs;
+  ArmedFault fault;
+  if (take_fault(SAVGB_FAULT_ATTENTION_K_TILE, &fault)) {
+    p.fault_tile = fault.index;
+    p.wait_limit_ns = fault.limit_ns;
+  }
   dim3 grid((unsigned)((n_q + kBlockQ - 1) / kBlockQ), (unsigned)H, (unsigned)B);
   SAVGB_CUDA(launch_dependent(kernel, grid, dim3(kThreads), dyn_smem, stream, maps, p));
   SAVGB_CUDA(cudaGetLastError());

@@ -49,6 +49,15 @@ enum : unsigned int {
 };
 int error_word(DeviceErrorWord** out);
 
+// One-shot fault armed by savgb_arm_wait_fault (a failure-path test hook):
+// the next launch of the kernel of `kind` takes it and disarms it.  The
+// kernel then skips one arrival at `index` and bounds its waits by limit_ns.
+struct ArmedFault {
+  int index;
+  uint64_t limit_ns;
+};
+bool take_fault(int kind, ArmedFault* out);
+
 // Current device must be an sm_103 part (GB300); returns SAVGB_ERR_UNSUPPORTED
 // otherwise.  Caches the SM count.
 int check_device(int* sm_count);

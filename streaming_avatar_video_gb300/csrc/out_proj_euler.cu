@@ -40,6 +40,11 @@ struct WoParams {
   float* x;
   float* v_out;
   DeviceErrorWord* err;
+  // failure-path test hook of the CTA-pair kernel (savgb_arm_wait_fault):
+  // k-block iteration whose relay the odd CTA of cluster 0 skips (-1: none),
+  // and the limit of every wait of that kernel
+  int fault_iter;
+  uint64_t wait_limit_ns;
 };
 
 constexpr int kXChunk = 32;                   // columns of x per staged chunk
@@ -301,7 +306,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         for (int kb = 0; kb < kb_count; ++kb, ++it) {
           const int st = static_cast<int>(it % kStages);
           const uint32_t use = it / kStages;
-          if (use > 0 && !dev::mbar_wait(&bars[kEmpty + st], (use - 1) & 1, abort)) {
+          if (use > 0 && !dev::mbar_wait(&bars[kEmpty + st], (use - 1) & 1, abort, p.wait_limit_ns)) {
             give_up(p, abort, 11);
             ok = false;
             break;
@@ -316,8 +321,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       volatile int never = 0;
       const uint32_t first = it > static_cast<uint32_t>(kStages) ? it - kStages : 0;
       for (uint32_t t = first; t < it; ++t) {
-        if (leader) dev::mbar_wait_cluster(&bars[kFull + t % kStages], (t / kStages) & 1, &never);
-        else dev::mbar_wait(&bars[kFull + t % kStages], (t / kStages) & 1, &never);
+        if (leader) dev::mbar_wait_cluster(&bars[kFull + t % kStages], (t / kStages) & 1, &never, p.wait_limit_ns);
+        else dev::mbar_wait(&bars[kFull + t % kStages], (t / kStages) & 1, &never, p.wait_limit_ns);
       }
     }
   } else if (warp == 1) {
@@ -335,7 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         const int buf = tile_i & 1;
         const uint32_t buse = static_cast<uint32_t>(tile_i >> 1);
         if (buse > 0 &&
-            !__all_sync(0xffffffffu, dev::mbar_wait_cluster(&bars[kAccEmpty + buf], (buse - 1) & 1, abort))) {
+            !__all_sync(0xffffffffu, dev::mbar_wait_cluster(&bars[kAccEmpty + buf], (buse - 1) & 1, abort, p.wait_limit_ns))) {
           if (issuer) give_up(p, abort, 12);
           break;
         }
@@ -343,7 +348,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         const uint32_t d = tmem + static_cast<uint32_t>(buf * 256);
         for (int kb = 0; kb < kb_count; ++kb, ++it) {
           const int st = static_cast<int>(it % kStages);
-          if (!__all_sync(0xffffffffu, dev::mbar_wait(&bars[kFull + st], (it / kStages) & 1, abort))) {
+          if (!__all_sync(0xffffffffu, dev::mbar_wait(&bars[kFull + st], (it / kStages) & 1, abort, p.wait_limit_ns))) {
             if (issuer) give_up(p, abort, 13);
             ok = false;
             break;
@@ -365,18 +370,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       if (issuer) dev::mma_commit_pair(&bars[kDrain], 1);
       __syncwarp();
       volatile int never = 0;
-      dev::mbar_wait(&bars[kDrain], 0, &never);
+      dev::mbar_wait(&bars[kDrain], 0, &never, p.wait_limit_ns);
     }
   } else if (warp == 2) {
     if (lane == 0 && !leader) {
       // ----------------------------------------------- relay (odd CTA only)
       const uint32_t full0 = dev::mapa_shared(&bars[kFull], 0);
+      // test hook: the first cluster leaves one relay out (fault_iter < 0: never)
+      const int64_t skip = cluster == 0 ? p.fault_iter : -1;
       uint32_t it = 0;
       bool ok = true;
       for (int t = cluster; t < n_tiles && ok; t += n_clusters) {
         for (int kb = 0; kb < kb_count; ++kb, ++it) {
           const int st = static_cast<int>(it % kStages);
-          if (!dev::mbar_wait(&bars[kFull + st], (it / kStages) & 1, abort)) {
+          if (!dev::mbar_wait(&bars[kFull + st], (it / kStages) & 1, abort, p.wait_limit_ns)) {
             give_up(p, abort, 14);
             ok = false;
             break;
@@ -384,7 +391,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           // relaxed: the TMA completion just observed already placed the
           // data; a release arrive at cluster scope held this thread ~0.8 us
           // per stage and throttled the whole pipeline to half speed
-          dev::mbar_arrive_cluster_relaxed(full0 + static_cast<uint32_t>(st * 8));
+          if (static_cast<int64_t>(it) != skip) dev::mbar_arrive_cluster_relaxed(full0 + static_cast<uint32_t>(st * 8));
         }
       }
     }
@@ -411,7 +418,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         if (m < p.M && ncols > 0) dev::prefetch_l2(p.x + static_cast<int64_t>(m) * p.N + ncol0, ncols * 4);
       }
       // every lane polls; a vote keeps the warp on one path
-      if (!__all_sync(0xffffffffu, dev::mbar_wait_cluster(&bars[kAccFull + buf], (tile_i >> 1) & 1, abort))) {
+      if (!__all_sync(0xffffffffu, dev::mbar_wait_cluster(&bars[kAccFull + buf], (tile_i >> 1) & 1, abort, p.wait_limit_ns))) {
         give_up(p, abort, 15);
         break;
       }
@@ -428,7 +435,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         const int bi = cc % kPairXBufs;
         uint32_t acc[32];
         dev::tmem_ld32(t_lane + static_cast<uint32_t>(buf * 256 + ch * 128 + cc * kXChunk), acc);
-        const bool xg = __all_sync(0xffffffffu, dev::mbar_wait(&xbar[bi], xwaits[bi] & 1, abort));
+        const bool xg = __all_sync(0xffffffffu, dev::mbar_wait(&xbar[bi], xwaits[bi] & 1, abort, p.wait_limit_ns));
         ++xwaits[bi];
         if (!xg) {
           give_up(p, abort, 16);
@@ -517,7 +524,7 @@ int launch_bn(const void* o, const void* w, const float* bias, float* x, int64_t
   const uint32_t bx[2] = {kXChunk, 32};
   rc = encode_tiled(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, x, dx, sx, bx, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
-  WoParams p{(int)M, N, K, dt, bias, x, v_out, nullptr};
+  WoParams p{(int)M, N, K, dt, bias, x, v_out, nullptr, -1, dev::kWaitLimitNs};
   if ((rc = error_word(&p.err))) return rc;
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + gemm::kBM - 1) / gemm::kBM));
   SAVGB_CUDA(launch_dependent(wo_euler_kernel<BN>, grid, dim3(gemm::kThreads), L::kDynSmem, stream, ma, mb, mx, p));
@@ -566,8 +573,13 @@ int launch_pair(const void* o, const void* w, const float* bias, float* x, int64
   const uint32_t bx[2] = {kXChunk, 32};
   rc = encode_tiled(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, x, dx, sx, bx, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
-  WoParams p{(int)M, N, K, dt, bias, x, nullptr, nullptr};
+  WoParams p{(int)M, N, K, dt, bias, x, nullptr, nullptr, -1, dev::kWaitLimitNs};
   if ((rc = error_word(&p.err))) return rc;
+  ArmedFault fault;
+  if (take_fault(SAVGB_FAULT_WO_PAIR_RELAY, &fault)) {
+    p.fault_iter = fault.index;
+    p.wait_limit_ns = fault.limit_ns;
+  }
   const int n_tiles_n = N / 256;
   const int n_tiles = (int)((M + 255) / 256) * n_tiles_n;
   // one wave of pairs: as many clusters as can be resident at once

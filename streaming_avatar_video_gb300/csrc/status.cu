@@ -28,6 +28,20 @@ std::mutex g_mu;
 
 void clear_error() { g_msg[0] = 0; }
 
+namespace {
+std::mutex g_fault_mu;
+int g_fault_kind = 0;
+ArmedFault g_fault{-1, 0};
+}  // namespace
+
+bool take_fault(int kind, ArmedFault* out) {
+  std::lock_guard<std::mutex> lk(g_fault_mu);
+  if (g_fault_kind != kind) return false;
+  *out = g_fault;
+  g_fault_kind = 0;
+  return true;
+}
+
 int fail(int code, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -181,6 +195,22 @@ int savgb_watchdog_selftest(uint64_t limit_ns, void* stream) {
   if ((rc = error_word(&err))) return rc;
   watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, limit_ns);
   SAVGB_CUDA(cudaGetLastError());
+  return SAVGB_OK;
+}
+
+int savgb_arm_wait_fault(int kind, int index, uint64_t limit_ns) {
+  clear_error();
+  if (kind != SAVGB_FAULT_ATTENTION_K_TILE && kind != SAVGB_FAULT_WO_PAIR_RELAY)
+    return fail(SAVGB_ERR_INVALID_ARG, "savgb_arm_wait_fault: unknown kind %d", kind);
+  std::lock_guard<std::mutex> lk(g_fault_mu);
+  if (index < 0) {
+    if (g_fault_kind == kind) g_fault_kind = 0;
+    return SAVGB_OK;
+  }
+  if (limit_ns == 0 || limit_ns > 10000000000ull)
+    return fail(SAVGB_ERR_INVALID_ARG, "savgb_arm_wait_fault: limit_ns must be in (0, 1e10]");
+  g_fault_kind = kind;
+  g_fault = ArmedFault{index, limit_ns};
   return SAVGB_OK;
 }
 

@@ -27,7 +27,7 @@ STATUS = {
 # every entry point of include/savgb.h
 EXPORTS = (
     "savgb_status_string", "savgb_last_error", "savgb_version", "savgb_device_check",
-    "savgb_watchdog_selftest", "rope3d_apply", "chunk_attention", "out_proj_euler_step",
+    "savgb_watchdog_selftest", "savgb_arm_wait_fault", "rope3d_apply", "chunk_attention", "out_proj_euler_step",
     "flow_time_grid", "chunk_stream_create", "chunk_stream_set_reference", "chunk_stream_step",
     "chunk_stream_end_chunk", "chunk_stream_set_step_events", "chunk_stream_sync", "chunk_stream_info", "chunk_stream_export_state",
     "chunk_stream_import_state", "chunk_stream_destroy", "chunk_step_noalloc",
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
         "savgb_version": (c_int, []),
         "savgb_device_check": (c_int, [c_vp]),
         "savgb_watchdog_selftest": (c_int, [ctypes.c_uint64, c_vp]),
+        "savgb_arm_wait_fault": (c_int, [c_int, c_int, ctypes.c_uint64]),
         "rope3d_apply": (c_int, [c_vp, c_vp, c_int, c_i64, c_int, c_int, c_int, c_int, c_int, c_int, c_d, c_vp]),
         "chunk_attention": (c_int, [c_vp, c_int, c_i64, c_int, c_int, ctypes.POINTER(KVSegment), c_int, c_f,
                                     c_vp, c_vp, c_vp]),
@@ -158,6 +159,17 @@ def savgb_device_check(stream=None) -> None:
 
 def savgb_watchdog_selftest(limit_ns: int, stream=None) -> None:
     _check(lib().savgb_watchdog_selftest(int(limit_ns), _stream(stream)))
+
+
+FAULT_ATTENTION_K_TILE = 1
+FAULT_WO_PAIR_RELAY = 2
+
+
+def savgb_arm_wait_fault(kind: int, index: int, limit_ns: int = 20_000_000) -> None:
+    """Failure-path test hook: the next launch of the kernel of ``kind``
+    skips one arrival at ``index`` and gives up its waits after ``limit_ns``
+    (index < 0 disarms)."""
+    _check(lib().savgb_arm_wait_fault(int(kind), int(index), int(limit_ns)))
 
 
 # ------------------------------------------------------------------ kernels

@@ -383,6 +383,67 @@ def test_watchdog_timeout_is_reported(S):
     assert float((x * 2).sum()) == 8.0
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["plain", "rope-q-fused"])
+def test_attention_give_up_path(S, fused):
+    """The real attention kernel's give-up path: block (0, 0, 0)'s key
+    producer skips the copy of key tile 1, so the block's waits for it run
+    out after 20 ms.  The block records the timeout, drains its copies and
+    MMAs, frees its tensor memory and returns; the host reads
+    SAVGB_ERR_TIMEOUT, and the next launch, with no fault, passes parity."""
+    B, H, D, gt, gh, gw = 1, 2, 128, 3, 10, 10   # 300 queries: two query blocks per head
+    segs = [100, 37]                              # with the chunk: 1 + 1 + 3 key tiles
+    n_q = gt * gh * gw
+    q = bf16((B, n_q, H, D), 61, I.KIND_Q)
+    kc, vc = bf16((B, n_q, H, D), 61, I.KIND_K), bf16((B, n_q, H, D), 61, I.KIND_V)
+    ctx = [(bf16((B, n, H, D), 61, I.KIND_K, chunk=i + 1), bf16((B, n, H, D), 61, I.KIND_V, chunk=i + 1))
+           for i, n in enumerate(segs)]
+    dsegs = [(k.cuda(), v.cuda()) for k, v in ctx] + [(kc.cuda(), vc.cuda())]
+
+    def run():
+        if fused:
+            return S.chunk_attention_qrope(q.cuda(), (gt, gh, gw), dsegs)
+        return S.chunk_attention(q.cuda(), dsegs)
+
+    S.savgb_device_check()
+    S.savgb_arm_wait_fault(S.FAULT_ATTENTION_K_TILE, 1, 20_000_000)
+    run()
+    with pytest.raises(S.SavgbError) as e:
+        S.savgb_device_check()
+    assert e.value.status == -6 and "chunk_attention" in str(e.value)
+    S.savgb_device_check()  # cleared
+    o = run()               # the arm was taken: a normal launch
+    S.savgb_device_check()
+    q_ref = O.rope3d(f64(q), gt, gh, gw, 0) if fused else f64(q)
+    want = O.attention(q_ref, [(f64(k), f64(v)) for k, v in ctx] + [(f64(kc), f64(vc))])
+    assert_close(f64(o), want, what=f"attention after a give-up ({'fused' if fused else 'plain'})")
+
+
+def test_out_proj_pair_give_up_path(S):
+    """The W_o CTA-pair kernel's give-up path: the odd CTA of the first
+    cluster skips its relay of k-block iteration 3, so the even CTA's MMA
+    issuer gives up after 20 ms; both CTAs drain, reach the cluster barriers
+    and free their tensor memory.  SAVGB_ERR_TIMEOUT on the host, then a
+    normal launch passes parity."""
+    M, hid = 1024, 512   # 8 tiles of 256 x 256, 8 k-blocks each
+    o = bf16((M, hid), 62, I.KIND_Q, std=0.05)
+    wo = bf16((hid, hid), 62, I.KIND_WO, std=1.0 / math.sqrt(hid))
+    x0 = torch.from_numpy(I.normal_f32((M, hid), 1.0, 62, I.KIND_X))
+    dt = 0.125
+    S.savgb_device_check()
+    S.savgb_arm_wait_fault(S.FAULT_WO_PAIR_RELAY, 3, 20_000_000)
+    x = x0.cuda()
+    S.out_proj_euler_step(o.cuda(), wo.cuda(), x, dt)
+    with pytest.raises(S.SavgbError) as e:
+        S.savgb_device_check()
+    assert e.value.status == -6 and "out_proj_euler_step" in str(e.value)
+    S.savgb_device_check()  # cleared
+    x = x0.cuda()
+    S.out_proj_euler_step(o.cuda(), wo.cuda(), x, dt)
+    S.savgb_device_check()
+    want = O.euler_update(f64(x0), O.out_proj(f64(o), f64(wo)), dt)
+    assert_close(f64(x), want, max_abs=1e-4, mean_abs=1e-5, what="x after a give-up")
+
+
 @pytest.mark.parametrize("name", ["base", "sr1"])
 def test_stream_step_full_size_sampled_rows(S, name):
     """Two one-step chunks of a full-size workload through chunk_stream_step:

@@ -134,3 +134,15 @@ def test_noalloc_validates_before_any_device_call(S):
     assert L.chunk_step_noalloc(p, p, p, None, 0, p, None, p, 0.1, 1, 2, 96, 1, 4, 4, 1e4, 0.0, None) == -2
     assert L.chunk_step_noalloc(p, p, p, None, 3, p, None, p, 0.1, 1, 2, 64, 1, 4, 4, 1e4, 0.0, None) == -1
     assert L.chunk_step_noalloc(p, p, p, None, 0, p, None, p, float("nan"), 1, 2, 64, 1, 4, 4, 1e4, 0.0, None) == -1
+
+
+def test_arm_wait_fault_validates(S):
+    """The failure-path hook refuses unknown kinds and out-of-range limits;
+    a negative index disarms (no device work either way)."""
+    L = S.lib()
+    assert L.savgb_arm_wait_fault(0, 1, 1000) == -1
+    assert L.savgb_arm_wait_fault(3, 1, 1000) == -1
+    assert L.savgb_arm_wait_fault(S.FAULT_ATTENTION_K_TILE, 1, 0) == -1
+    assert L.savgb_arm_wait_fault(S.FAULT_ATTENTION_K_TILE, 1, 10_000_000_001) == -1
+    assert L.savgb_arm_wait_fault(S.FAULT_WO_PAIR_RELAY, 2, 5_000_000) == 0
+    assert L.savgb_arm_wait_fault(S.FAULT_WO_PAIR_RELAY, -1, 0) == 0  # disarmed
