@@ -48,9 +48,9 @@ METRIC = "chunk-attention TFLOP/s (% of bf16 tensor peak); latent frames/s per d
 # sources the capture was taken on (attention.cu, ptx.cuh, common.h); any later
 # change of them reports null.
 ATTN_TRAFFIC = {
-    # profiles/chunk_attention_base.md: the fused-RoPE kernel the stream runs at base,
-    # 289.926 MB read + 60.824 MB written
-    "7f4a80268126f06fc44d736eed0ecd60a517d71b2c6d9f8e8790771c06cc8607": {"base": 350749952},
+    # profiles/chunk_attention_base.md and profiles/chunk_attention_sr.md: the fused-RoPE kernel the stream
+    # runs; base 290.340 MB read + 60.136 MB written, SR 1.48 GB read + 295.68 MB written
+    "b276d2b26209180403689079af1542a65cc7a049031bd103eff0ff2a633eac54": {"base": 350476288, "sr": 1775680000},
 }
 
 
@@ -358,6 +358,7 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
     exp_forms = None
     if fused and not args.no_exp_forms:
         exp_forms = time_exp_forms(S, w, dsets, dev, stream, max(3, min(args.steps, 20)))
+    rope_loop_ms = time_rope_loop(S, w, dsets, stream, max(10, args.steps))
 
     # end-to-end through the public API with host buffers
     e2e = None
@@ -396,6 +397,12 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
             "chunk_attention_tflops": round(attn_tflops, 1),
             "out_proj_euler_tflops": round(wo_flops / (wo_ms * 1e-3) / 1e12, 1),
             "rope3d_gbs": round(rope_bytes / (rope_ms * 1e-3) / 1e9, 1),
+            # the k-only pass timed back to back (programmatic launch overlapping each launch's table build with
+            # the previous one's tail, as between the kernels of a step), not between events
+            "rope3d_k_loop": {"ms": round(rope_loop_ms, 4),
+                              "gbs": round(4 * w.B * w.n_q * w.hid / (rope_loop_ms * 1e-3) / 1e9, 1),
+                              f"pct_of_{pk_kind}_copy": round(100 * 4 * w.B * w.n_q * w.hid / (rope_loop_ms * 1e-3)
+                                                              / 1e9 / pk["hbm_gbs"], 1)},
             "rope3d_pct_of_hbm": {"nominal_8000": round(100 * rope_bytes / (rope_ms * 1e-3) / 8e12, 1),
                                   f"{pk_kind}_copy": round(100 * rope_bytes / (rope_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 1)},
         },
@@ -451,6 +458,24 @@ def clock_normalised(attn_flops, attn_ms, wo_flops, wo_ms, sm_mhz, sms):
 
     return {"sm_mhz_median": sm_mhz, "sms": sms, "chunk_attention": one(attn_flops, attn_ms),
             "out_proj_euler": one(wo_flops, wo_ms)}
+
+
+def time_rope_loop(S, w, dsets, stream, k):
+    """The RoPE pass of a stream step (k alone, chunk-local positions) as k
+    back-to-back launches between two events, alternating the two input sets
+    (each larger than L2) into one output; ms per launch."""
+    out = torch.empty_like(dsets[0][1])
+    grid = (w.F, w.grid_h, w.grid_w)
+    for i in range(3):
+        S.rope3d_apply(dsets[i & 1][1], out, *grid, 0, w.rope_base)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(k):
+        S.rope3d_apply(dsets[i & 1][1], out, *grid, 0, w.rope_base)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / k
 
 
 def time_exp_forms(S, w, dsets, dev, stream, k):
