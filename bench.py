@@ -271,7 +271,7 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
     x = I.state_x(w, seed).to(dev)
 
     cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
-                       w.rope_base)
+                       w.rope_base, host_io=not args.no_e2e)
     cs.set_reference(rk.to(dev), rv.to(dev))
     # prime: one chunk end so that every timed step attends over the boundary too
     q, k, v = dsets[0]
@@ -525,79 +525,47 @@ def time_exp_forms(S, w, dsets, dev, stream, k):
 
 
 def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world, i0=0):
-    """Same metric through ChunkStream.step with host buffers.  Every step
-    uploads that step's q, k, v from pinned host memory and reads the updated
-    state x back into pinned host memory, all inside the timed region.  The
-    copies run on two copy streams: step i+1's inputs are uploaded into the
-    other half of a double buffer while step i computes, and step i's x is
-    snapshotted on the device and read back while step i+1 computes."""
+    """Same metric through the C-ABI call with HOST buffers:
+    chunk_stream_step_host takes the step's q, k, v from pinned host memory
+    and reads the updated state x back into pinned host memory every step.
+    The library uploads each step's inputs into one of two device slots on a
+    copy stream while the previous step computes, and reads x back on a
+    second copy stream while the next step computes.  The timed region ends
+    once the last read-back has landed (join_copies, then an event)."""
     hsets = [tuple(t.pin_memory() for t in s) for s in sets]
-    dbuf = [tuple(torch.empty_like(t, device=dev) for t in sets[0]) for _ in range(2)]
-    x_stage = torch.empty_like(x)
     hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     n = max(3, min(args.steps, 60))
-    ev = lambda: torch.cuda.Event()  # noqa: E731
-    loaded = [ev(), ev()]
-    freed = [None, None]
-    out_done = [None]
 
-    def upload(i):
-        hq, hk, hv = hsets[i & 1]
-        with torch.cuda.stream(s_in):
-            if freed[i & 1] is not None:
-                s_in.wait_event(freed[i & 1])
-            for d, h in zip(dbuf[i & 1], (hq, hk, hv)):
-                d.copy_(h, non_blocking=True)
-            loaded[i & 1].record(s_in)
-
-    def step(i, upload_next=True):
-        if upload_next:
-            upload(i + 1)
+    def step(i):
         s_idx = (i0 + i) % w.steps
         last = s_idx == w.steps - 1
-        stream.wait_event(loaded[i & 1])
-        dq, dk, dv = dbuf[i & 1]
-        cs.step(dq, dk, dv, wo, x, dts[s_idx], last)
+        hq, hk, hv = hsets[i & 1]
+        cs.step_host(hq, hk, hv, wo, x, dts[s_idx], last, x_host=hx)
         if last:
             cs.end_chunk()
-        freed[i & 1] = ev()
-        freed[i & 1].record(stream)
-        if out_done[0] is not None:
-            stream.wait_event(out_done[0])  # the previous snapshot has left the device
-        x_stage.copy_(x, non_blocking=True)
-        staged = ev()
-        staged.record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(staged)
-            hx.copy_(x_stage, non_blocking=True)
-            done = ev()
-            done.record(s_out)
-        out_done[0] = done
 
-    upload(0)
     for i in range(3):
         step(i)
-    torch.cuda.synchronize()
+    cs.sync()
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
         a.record(stream)
-        base = 3
-        for i in range(base, base + n):
-            step(i, upload_next=True)
-        stream.wait_event(out_done[0])
+        for i in range(3, 3 + n):
+            step(i)
+        cs.join_copies()
         b.record(stream)
         torch.cuda.synchronize()
+    cs.sync()
     ms = max_over_ranks(world, a.elapsed_time(b)) / n
     h2d = sum(t.numel() * t.element_size() for t in sets[0])
     d2h = x.numel() * x.element_size()
     return {"value": round(whole_job_rate(world, w.attn_flops(True), ms) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "clocks": clk.summary(),
-            "api": "ChunkStream.step (C ABI chunk_stream_step) with pinned host q/k/v in and x out; uploads of "
-                   "the next step and read-back of the previous one overlap the step on two copy streams; "
-                   "measured right after the headline region"}, i0 + base + n
+            "api": "C ABI chunk_stream_step_host: pinned host q/k/v in, x read back to pinned host memory every "
+                   "step; the library overlaps the uploads and read-backs with the steps on two copy streams; "
+                   "measured right after the headline region"}, i0 + 3 + n
 
 
 def run_long(args, w: I.Workload, world: int, rank: int, local: int):

@@ -283,6 +283,7 @@ typedef struct {
   float softmax_scale; /* <= 0 selects 1/sqrt(D) */
   int interp_chunks;   /* nonzero: keep the anchors of interpolation chunks (needs F >= 3) */
   int qkv_block;       /* nonzero: reserve room for chunk_stream_block_step */
+  int host_io;         /* nonzero: reserve two device input slots for chunk_stream_step_host */
 } chunk_stream_config;
 /* The same config under the name the problem statement's interface uses. */
 typedef chunk_stream_config chunk_stream_config_t;
@@ -308,6 +309,37 @@ int chunk_stream_set_reference(chunk_stream_t* s, const void* k_ref, const void*
  * this step's k and v. */
 int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const void* v,
                       const void* w_o, const float* bias, float* x, float dt, int is_last_step);
+
+/* chunk_stream_step with the step's inputs in HOST memory and, optionally,
+ * the updated state read back to host memory: the whole step through one
+ * call, host to host, as a serving loop that receives each step's q, k, v
+ * from the host and hands the state back would run it.  Needs host_io in the
+ * config (the arena then holds two device input slots, 2 x 3 x B*N*H*D bf16).
+ *   q_host, k_host, v_host  bf16 [B][N][H][D] in host memory; page-locked
+ *       (cudaHostAlloc / cudaHostRegister) for the upload to overlap compute,
+ *       pageable memory also works but its copy blocks the calling thread.
+ *   x       fp32 [B*N][H*D] DEVICE state, updated in place (it stays resident).
+ *   x_host  optional fp32 [B*N][H*D] host buffer (page-locked to overlap):
+ *       receives x after this step.
+ * The call enqueues and returns.  The upload goes into input slot (call
+ * count mod 2) on an internal copy stream once the step that last used that
+ * slot has finished with it; the step runs on the handle's stream once its
+ * upload has landed; the read-back of x runs on a second internal copy stream
+ * after the step, straight from x (no staging copy): the W_o update of the
+ * next step of this stream waits for it.  So consecutive calls overlap the
+ * upload of step i+1 and the read-back of step i with the compute of step i+1.
+ * Host buffers passed to a call must stay valid and unchanged (inputs) or
+ * unread (x_host) until chunk_stream_sync() returns, or until the handle's
+ * stream has passed a chunk_stream_join_copies() enqueued after the call.
+ * Until then x may be written only by later steps of this stream.
+ * SAVGB_ERR_STATE without host_io.  Otherwise as chunk_stream_step. */
+int chunk_stream_step_host(chunk_stream_t* s, const void* q_host, const void* k_host, const void* v_host,
+                           const void* w_o, const float* bias, float* x, float dt, int is_last_step,
+                           float* x_host);
+/* Makes the handle's stream wait for every upload and read-back that
+ * chunk_stream_step_host has enqueued so far (work enqueued on the stream
+ * afterwards, an event for one, comes after them).  Returns at once. */
+int chunk_stream_join_copies(chunk_stream_t* s);
 
 /* --------------------------------------------------------------------------
  * Interpolation (I) chunks ("Boundary continuity and chunk consistency"):
@@ -361,7 +393,8 @@ int chunk_stream_end_chunk(chunk_stream_t* s);
  * kernels as they run inside a loop.) */
 int chunk_stream_set_step_events(chunk_stream_t* s, void* const* events);
 
-/* Synchronises the handle's stream and reports device-side errors. */
+/* Synchronises the handle's stream (and, with host_io, its copy streams) and
+ * reports device-side errors. */
 int chunk_stream_sync(chunk_stream_t* s);
 
 /* Read-only view of the state: chunk index, boundary tokens in use (0 on

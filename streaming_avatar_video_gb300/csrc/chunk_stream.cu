@@ -67,6 +67,15 @@ struct chunk_stream {
   int64_t chunk_index;
   cudaEvent_t step_events[4];  // recorded by the next step, then cleared
   bool have_events;
+  // host_io: two device input slots [q | k | v] filled from host memory on
+  // copy_in, the state read back on copy_out (chunk_stream_step_host)
+  __nv_bfloat16_raw* in_slot[2][3];
+  cudaStream_t copy_in, copy_out;
+  cudaEvent_t ev_loaded[2], ev_freed[2], ev_step_done, ev_out_done;
+  bool slot_used[2];
+  int next_slot;
+  bool out_pending;  // a read-back of x is in flight: the next W_o update waits for it
+  bool host_used;    // copies were enqueued since the last join / sync
 };
 
 namespace {
@@ -99,6 +108,44 @@ int validate_config(const chunk_stream_config* c) {
   if (hid % 16) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: H*D must be a multiple of 16");
   if (c->interp_chunks && c->F < 3)
     return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: interpolation chunks need F >= 3");
+  return SAVGB_OK;
+}
+
+// Copy streams and events of chunk_stream_step_host.
+int host_io_init(chunk_stream* s) {
+  SAVGB_CUDA(cudaStreamCreateWithFlags(&s->copy_in, cudaStreamNonBlocking));
+  SAVGB_CUDA(cudaStreamCreateWithFlags(&s->copy_out, cudaStreamNonBlocking));
+  for (int i = 0; i < 2; ++i) {
+    SAVGB_CUDA(cudaEventCreateWithFlags(&s->ev_loaded[i], cudaEventDisableTiming));
+    SAVGB_CUDA(cudaEventCreateWithFlags(&s->ev_freed[i], cudaEventDisableTiming));
+    s->slot_used[i] = false;
+  }
+  SAVGB_CUDA(cudaEventCreateWithFlags(&s->ev_step_done, cudaEventDisableTiming));
+  SAVGB_CUDA(cudaEventCreateWithFlags(&s->ev_out_done, cudaEventDisableTiming));
+  s->next_slot = 0;
+  s->out_pending = false;
+  s->host_used = false;
+  return SAVGB_OK;
+}
+
+void host_io_release(chunk_stream* s) {
+  if (s->copy_in) cudaStreamSynchronize(s->copy_in);
+  if (s->copy_out) cudaStreamSynchronize(s->copy_out);
+  for (int i = 0; i < 2; ++i) {
+    if (s->ev_loaded[i]) cudaEventDestroy(s->ev_loaded[i]);
+    if (s->ev_freed[i]) cudaEventDestroy(s->ev_freed[i]);
+  }
+  if (s->ev_step_done) cudaEventDestroy(s->ev_step_done);
+  if (s->ev_out_done) cudaEventDestroy(s->ev_out_done);
+  if (s->copy_in) cudaStreamDestroy(s->copy_in);
+  if (s->copy_out) cudaStreamDestroy(s->copy_out);
+}
+
+// Before a launch that writes x: a read-back of x still in flight must end first.
+int wait_readback(chunk_stream* s) {
+  if (!s->out_pending) return SAVGB_OK;
+  SAVGB_CUDA(cudaStreamWaitEvent(s->stream, s->ev_out_done, 0));
+  s->out_pending = false;
   return SAVGB_OK;
 }
 
@@ -145,7 +192,8 @@ int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stre
   const int64_t vbuf_b = c.qkv_block ? tok_b : 0;
   s->qrope = qrope_fits(c.D, c.F, c.grid_h, c.grid_w);
   const int64_t tab_b = s->qrope ? round_up(rope_q_table_bytes(c.D, c.F, c.grid_h, c.grid_w), 256) : 0;
-  s->arena_bytes = 2 * ref_b + 4 * bnd_b + 3 * tok_b + 4 * anc_b + vbuf_b + tab_b;
+  const int64_t in_b = c.host_io ? 6 * tok_b : 0;
+  s->arena_bytes = 2 * ref_b + 4 * bnd_b + 3 * tok_b + 4 * anc_b + vbuf_b + tab_b + in_b;
   const char* cap = getenv("SAVGB_ARENA_LIMIT_BYTES");
   if (cap && *cap) {
     const long long lim = atoll(cap);
@@ -174,8 +222,16 @@ int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stre
   }
   s->v_buf = vbuf_b ? take(vbuf_b) : nullptr;
   s->qrope_tab = tab_b ? static_cast<void*>(take(tab_b)) : nullptr;
+  for (int i = 0; i < 2; ++i)
+    for (int t = 0; t < 3; ++t) s->in_slot[i][t] = in_b ? take(tok_b) : nullptr;
   if (s->qrope &&
       (rc = rope_q_table_build(s->qrope_tab, c.D, 0, c.F, c.grid_h, c.grid_w, c.rope_base, s->stream))) {
+    cudaFree(s->arena);
+    delete s;
+    return rc;
+  }
+  if (c.host_io && (rc = host_io_init(s))) {
+    host_io_release(s);
     cudaFree(s->arena);
     delete s;
     return rc;
@@ -251,6 +307,7 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
   }
   if (rc) return rc;
   if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[2], s->stream));
+  if ((rc = wait_readback(s))) return rc;
   rc = launch_out_proj_euler(s->o, w_o, bias, x, c.B * s->n_tok, (int)s->hid, (int)s->hid, dt,
                              nullptr, s->stream);
   if (rc) return rc;
@@ -291,6 +348,56 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
                                    (size_t)fr_el * 2, (size_t)c.B, cudaMemcpyDeviceToDevice, s->stream));
     }
   }
+  return SAVGB_OK;
+}
+
+int chunk_stream_step_host(chunk_stream_t* s, const void* q_host, const void* k_host, const void* v_host,
+                           const void* w_o, const float* bias, float* x, float dt, int is_last_step,
+                           float* x_host) {
+  savgb::ApiRange api_range_("savgb:chunk_stream_step_host");
+  clear_error();
+  if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_step_host: null handle");
+  if (!s->cfg.host_io) return fail(SAVGB_ERR_STATE, "chunk_stream_step_host: the stream was created without host_io");
+  if (!s->ref_set) return fail(SAVGB_ERR_STATE, "chunk_stream_step_host: set_reference has not been called");
+  if (!q_host || !k_host || !v_host || !w_o || !x)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_step_host: null argument");
+  if (!std::isfinite(dt)) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_step_host: dt must be finite");
+  const int slot = s->next_slot;
+  const size_t bytes = (size_t)(s->cfg.B * s->n_tok * s->hid * 2);
+  // upload into the slot once the step that last read it has finished
+  if (s->slot_used[slot]) SAVGB_CUDA(cudaStreamWaitEvent(s->copy_in, s->ev_freed[slot], 0));
+  const void* src[3] = {q_host, k_host, v_host};
+  for (int t = 0; t < 3; ++t)
+    SAVGB_CUDA(cudaMemcpyAsync(s->in_slot[slot][t], src[t], bytes, cudaMemcpyHostToDevice, s->copy_in));
+  SAVGB_CUDA(cudaEventRecord(s->ev_loaded[slot], s->copy_in));
+  SAVGB_CUDA(cudaStreamWaitEvent(s->stream, s->ev_loaded[slot], 0));
+  s->host_used = true;
+  int rc = chunk_stream_step(s, s->in_slot[slot][0], s->in_slot[slot][1], s->in_slot[slot][2], w_o, bias, x, dt,
+                             is_last_step);
+  if (rc) return rc;
+  SAVGB_CUDA(cudaEventRecord(s->ev_freed[slot], s->stream));
+  s->slot_used[slot] = true;
+  s->next_slot = slot ^ 1;
+  if (x_host) {
+    // read x back straight from the state; the next W_o update waits for it
+    SAVGB_CUDA(cudaEventRecord(s->ev_step_done, s->stream));
+    SAVGB_CUDA(cudaStreamWaitEvent(s->copy_out, s->ev_step_done, 0));
+    SAVGB_CUDA(cudaMemcpyAsync(x_host, x, (size_t)(s->cfg.B * s->n_tok * s->hid * 4), cudaMemcpyDeviceToHost,
+                               s->copy_out));
+    SAVGB_CUDA(cudaEventRecord(s->ev_out_done, s->copy_out));
+    s->out_pending = true;
+  }
+  return SAVGB_OK;
+}
+
+int chunk_stream_join_copies(chunk_stream_t* s) {
+  clear_error();
+  if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_join_copies: null handle");
+  if (!s->cfg.host_io || !s->host_used) return SAVGB_OK;
+  // every upload is already ordered before its step on the stream; the last
+  // read-back (ev_out_done follows every earlier one on copy_out) is not
+  if (s->out_pending) SAVGB_CUDA(cudaStreamWaitEvent(s->stream, s->ev_out_done, 0));
+  s->out_pending = false;
   return SAVGB_OK;
 }
 
@@ -339,6 +446,7 @@ int chunk_stream_istep(chunk_stream_t* s, const void* q, const void* k, const vo
     rc = launch_attention(s->q_rot, c.B, n_int, c.H, c.D, segs, 3, c.softmax_scale, s->o, nullptr, s->stream);
   }
   if (rc) return rc;
+  if ((rc = wait_readback(s))) return rc;
   return launch_out_proj_euler(s->o, w_o, bias, x, c.B * n_int, (int)s->hid, (int)s->hid, dt, nullptr,
                                s->stream);
 }
@@ -377,7 +485,9 @@ int chunk_stream_block_step(chunk_stream_t* s, const void* w_qkv, const void* w_
   if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[0], s->stream));
   const int64_t M = (int64_t)c.B * s->n_tok;
   void* xb = s->o;  // the bf16 copy of x is consumed by the projection before attention writes o
-  int rc = launch_to_bf16(x, xb, M * s->hid, s->stream);
+  int rc = wait_readback(s);
+  if (rc) return rc;
+  rc = launch_to_bf16(x, xb, M * s->hid, s->stream);
   if (rc) return rc;
   const int nxt = s->cur ^ 1;
   const bool capture = is_last_step && s->n_bnd > 0;
@@ -448,6 +558,12 @@ int chunk_stream_sync(chunk_stream_t* s) {
   savgb::ApiRange api_range_("savgb:chunk_stream_sync");
   clear_error();
   if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_sync: null handle");
+  if (s->cfg.host_io) {
+    SAVGB_CUDA(cudaStreamSynchronize(s->copy_in));
+    SAVGB_CUDA(cudaStreamSynchronize(s->copy_out));
+    s->out_pending = false;
+    s->host_used = false;
+  }
   return savgb_device_check(s->stream);
 }
 
@@ -552,6 +668,7 @@ int chunk_stream_destroy(chunk_stream_t* s) {
   clear_error();
   if (!s) return SAVGB_OK;
   cudaError_t e1 = cudaStreamSynchronize(s->stream);
+  if (s->cfg.host_io) host_io_release(s);
   cudaError_t e2 = cudaFree(s->arena);
   delete s;
   if (e1 != cudaSuccess) return cuda_fail(e1, "chunk_stream_destroy: cudaStreamSynchronize");

@@ -34,6 +34,7 @@ EXPORTS = (
     "chunk_stream_istep", "chunk_stream_end_ichunk", "chunk_stream_ichunk_index", "chunk_attention_qrope",
     "qkv_rope_project", "chunk_stream_block_step", "chunk_stream_fused_q_rope", "chunk_attention_qrope_fits",
     "chunk_attention_qrope_table_bytes", "chunk_attention_qrope_build_table", "chunk_attention_qrope_with_table",
+    "chunk_stream_step_host", "chunk_stream_join_copies",
 )
 
 
@@ -52,7 +53,7 @@ class ChunkStreamConfig(ctypes.Structure):
                 ("grid_h", ctypes.c_int), ("grid_w", ctypes.c_int), ("ref_frames", ctypes.c_int),
                 ("boundary_frames", ctypes.c_int), ("ref_t", ctypes.c_int),
                 ("rope_base", ctypes.c_double), ("softmax_scale", ctypes.c_float),
-                ("interp_chunks", ctypes.c_int), ("qkv_block", ctypes.c_int)]
+                ("interp_chunks", ctypes.c_int), ("qkv_block", ctypes.c_int), ("host_io", ctypes.c_int)]
 
 
 _lib = None
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
         "chunk_stream_set_reference": (c_int, [c_vp, c_vp, c_vp]),
         "chunk_stream_step": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f, c_int]),
         "chunk_stream_end_chunk": (c_int, [c_vp]),
+        "chunk_stream_step_host": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f, c_int, c_vp]),
+        "chunk_stream_join_copies": (c_int, [c_vp]),
         "chunk_stream_istep": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f]),
         "chunk_stream_block_step": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_f, c_int]),
         "qkv_rope_project": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_i64, c_int, c_int, c_int, c_int, c_int,
@@ -144,6 +147,19 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: Optional[int] = 
         raise ValueError(f"{name} must be contiguous")
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def _need_host(t: torch.Tensor, name: str, dtype: torch.dtype, numel: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() != numel:
+        raise ValueError(f"{name} must hold {numel} elements, got {t.numel()}")
 
 
 # ------------------------------------------------------------------ status
@@ -379,10 +395,11 @@ class ChunkStream:
 
     def __init__(self, B: int, H: int, D: int, F: int, grid_h: int, grid_w: int, ref_frames: int = 1,
                  boundary_frames: int = 0, ref_t: int = -1, rope_base: float = 10000.0,
-                 softmax_scale: float = 0.0, stream=None, interp_chunks: bool = False, qkv_block: bool = False):
+                 softmax_scale: float = 0.0, stream=None, interp_chunks: bool = False, qkv_block: bool = False,
+                 host_io: bool = False):
         self.cfg = ChunkStreamConfig(B, H, D, F, grid_h, grid_w, ref_frames, boundary_frames, ref_t,
                                      float(rope_base), float(softmax_scale), int(bool(interp_chunks)),
-                                     int(bool(qkv_block)))
+                                     int(bool(qkv_block)), int(bool(host_io)))
         self.stream = _stream(stream)
         h = ctypes.c_void_p()
         _check(lib().chunk_stream_create(ctypes.byref(self.cfg), self.stream, ctypes.byref(h)))
@@ -418,6 +435,36 @@ class ChunkStream:
 
     def end_chunk(self) -> None:
         _check(lib().chunk_stream_end_chunk(self.handle))
+
+    def step_host(self, q_host, k_host, v_host, w_o, x, dt: float, is_last_step: bool, bias=None,
+                  x_host=None) -> None:
+        """chunk_stream_step with q, k, v in host memory (bf16 CPU tensors,
+        pinned for overlap) and, with x_host (fp32 CPU tensor), the updated
+        state read back; x stays on the device.  Needs host_io.  The host
+        tensors must stay untouched until sync() or a join_copies() that the
+        stream has passed."""
+        c = self.cfg
+        n = c.B * c.F * c.grid_h * c.grid_w * c.H * c.D
+        for name, t in (("q_host", q_host), ("k_host", k_host), ("v_host", v_host)):
+            _need_host(t, name, torch.bfloat16, n)
+        _need(w_o, "w_o", torch.bfloat16, 2)
+        _need(x, "x", torch.float32)
+        hid = c.H * c.D
+        if tuple(w_o.shape) != (hid, hid) or x.numel() != n:
+            raise ValueError("w_o must be [hid][hid] and x [B*N][hid]")
+        if bias is not None:
+            _need(bias, "bias", torch.float32, 1)
+            if bias.numel() != hid:
+                raise ValueError("bias must hold hid floats")
+        if x_host is not None:
+            _need_host(x_host, "x_host", torch.float32, n)
+        _check(lib().chunk_stream_step_host(self.handle, q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(),
+                                            w_o.data_ptr(), _ptr(bias), x.data_ptr(), float(dt),
+                                            int(bool(is_last_step)), _ptr(x_host)))
+
+    def join_copies(self) -> None:
+        """The stream waits for every upload and read-back enqueued so far."""
+        _check(lib().chunk_stream_join_copies(self.handle))
 
     def istep(self, q, k, v, w_o, x, dt: float, bias=None) -> None:
         """One step of the pending interpolation chunk (interior frames only)."""

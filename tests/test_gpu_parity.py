@@ -290,6 +290,77 @@ def test_stream_two_sessions_ragged_blocks(S):
         assert torch.equal(xs[c], xs2[c]), f"chunk {c}: rerun differs"
 
 
+def test_stream_host_io_matches_device_steps(S):
+    """chunk_stream_step_host (q, k, v from host memory, x read back every
+    step) against chunk_stream_step on the same inputs: every step's read-back
+    bit-identical to the device path's x after that step, the final state
+    against the oracle.  One step in the middle runs through the device call:
+    its W_o update must wait for the previous read-back, whose buffer must
+    still hold the earlier state.  Pageable input memory works too."""
+    w = I.WORKLOADS["small"]
+    seed = 9
+    rk, rv = I.reference_kv(w, seed)
+    wo = I.out_proj_weight(w, seed).cuda()
+    dts = S.flow_time_grid(w.steps, w.shift)
+    plan = [(c, s_) for c in range(2) for s_ in range(w.steps)]
+    device_call = (1, 2)                     # this step goes through chunk_stream_step
+    pageable = (0, 1)                        # this step's inputs are not page-locked
+    ins = {cs_: I.step_inputs(w, seed, *cs_) for cs_ in plan}
+
+    def make(host_io):
+        cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                           w.rope_base, host_io=host_io)
+        cs.set_reference(rk.cuda(), rv.cuda())
+        return cs
+
+    ref = make(False)
+    want = {}
+    x = I.state_x(w, seed).cuda()
+    for c, s_ in plan:
+        st = ins[(c, s_)]
+        ref.step(st.q.cuda(), st.k.cuda(), st.v.cuda(), wo, x, dts[s_], s_ == w.steps - 1)
+        want[(c, s_)] = x.cpu()
+        if s_ == w.steps - 1:
+            ref.end_chunk()
+    ref.sync()
+    ref.close()
+
+    hs = make(True)
+    x = I.state_x(w, seed).cuda()
+    back = {cs_: torch.empty((w.B * w.n_q, w.hid), dtype=torch.float32).pin_memory() for cs_ in plan}
+    # every host input stays alive until the sync below: the uploads read them asynchronously
+    host_in = {cs_: ((ins[cs_].q, ins[cs_].k, ins[cs_].v) if cs_ == pageable else
+                     tuple(t.pin_memory() for t in (ins[cs_].q, ins[cs_].k, ins[cs_].v))) for cs_ in plan}
+    dev_in = tuple(t.cuda() for t in (ins[device_call].q, ins[device_call].k, ins[device_call].v))
+    for c, s_ in plan:
+        last = s_ == w.steps - 1
+        if (c, s_) == device_call:
+            hs.step(*dev_in, wo, x, dts[s_], last)
+        else:
+            hs.step_host(*host_in[(c, s_)], wo, x, dts[s_], last, x_host=back[(c, s_)])
+        if last:
+            hs.end_chunk()
+    hs.sync()
+    for cs_ in plan:
+        if cs_ != device_call:
+            assert torch.equal(back[cs_], want[cs_]), f"read-back after chunk {cs_[0]} step {cs_[1]}"
+    assert torch.equal(x.cpu(), want[plan[-1]])
+    hs.close()
+    # the final state against the oracle
+    f = lambda t: t.double().numpy()  # noqa: E731
+    xs, _ = O.run_stream(w, f(rk), f(rv), f(wo.cpu()), lambda c: f(I.state_x(w, seed)) if c == 0 else None,
+                         lambda c, s_: tuple(f(t) for t in (ins[(c, s_)].q, ins[(c, s_)].k, ins[(c, s_)].v)),
+                         O.time_grid(w.steps, w.shift), chunks=1)
+    assert_close(f64(want[(0, w.steps - 1)]), xs[0], what="host-io stream chunk 0 x")
+    # without host_io the call is refused
+    plain = make(False)
+    st = ins[plan[0]]
+    with pytest.raises(S.SavgbError) as e:
+        plain.step_host(st.q, st.k, st.v, wo, x, 0.1, False)
+    assert e.value.status == -7
+    plain.close()
+
+
 def test_stream_export_import_resume(S):
     """Checkpoint after chunk 1, resume in a fresh handle: chunk 2 equals the
     uninterrupted run."""
