@@ -146,3 +146,24 @@ def test_arm_wait_fault_validates(S):
     assert L.savgb_arm_wait_fault(S.FAULT_ATTENTION_K_TILE, 1, 10_000_000_001) == -1
     assert L.savgb_arm_wait_fault(S.FAULT_WO_PAIR_RELAY, 2, 5_000_000) == 0
     assert L.savgb_arm_wait_fault(S.FAULT_WO_PAIR_RELAY, -1, 0) == 0  # disarmed
+
+
+def test_qrope_table_calls_validate(S):
+    """The caller-built table path: size query, null / misaligned tables,
+    and a grid the table does not cover are refused on the host."""
+    L = S.lib()
+    c_vp = ctypes.c_void_p
+    n = ctypes.c_int64()
+    assert L.chunk_attention_qrope_table_bytes(128, 8, 30, 52, ctypes.byref(n)) == 0
+    assert n.value == 8 * (8 * 22 + 30 * 21 + 52 * 21 + (30 * 21) % 2 + (52 * 21) % 2)  # [t | h | w], sections even
+    assert L.chunk_attention_qrope_table_bytes(96, 8, 30, 52, ctypes.byref(n)) == -2
+    assert L.chunk_attention_qrope_table_bytes(128, 0, 30, 52, ctypes.byref(n)) == -1
+    assert L.chunk_attention_qrope_build_table(None, 128, 2, 4, 4, 0, 1e4, None) == -1
+    assert L.chunk_attention_qrope_build_table(c_vp(24), 128, 2, 4, 4, 0, 1e4, None) == -3
+    assert L.chunk_attention_qrope_build_table(c_vp(32), 128, 2, 4, 4, 0, -1.0, None) == -1
+    segs = (S.KVSegment * 3)()
+    segs[0] = S.KVSegment(16, 32, 4)
+    assert L.chunk_attention_qrope_with_table(c_vp(16), 1, 32, 2, 128, 2, 4, 4, 0, None, segs, 1, 0.0, c_vp(16),
+                                              None, None) == -1
+    assert L.chunk_attention_qrope_with_table(c_vp(16), 1, 33, 2, 128, 2, 4, 4, 0, c_vp(64), segs, 1, 0.0,
+                                              c_vp(16), None, None) == -1  # n_q != grid
