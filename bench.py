@@ -547,6 +547,7 @@ def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world, i0=0):
     for i in range(3):
         step(i)
     cs.sync()
+    copies = time_copies_alone(hsets[0], hx, dev)
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
@@ -562,10 +563,35 @@ def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world, i0=0):
     d2h = x.numel() * x.element_size()
     return {"value": round(whole_job_rate(world, w.attn_flops(True), ms) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "clocks": clk.summary(),
+            "clocks": clk.summary(), "copies_alone": copies,
             "api": "C ABI chunk_stream_step_host: pinned host q/k/v in, x read back to pinned host memory every "
                    "step; the library overlaps the uploads and read-backs with the steps on two copy streams; "
                    "measured right after the headline region"}, i0 + 3 + n
+
+
+def time_copies_alone(h_inputs, hx, dev):
+    """The e2e loop's host copies with no compute running, on this machine: one
+    step's inputs host -> device and the state device -> host (pinned
+    buffers, torch copies into a scratch device buffer), median of 3.  When
+    they take longer than a step, the e2e loop is bound by the host side."""
+    d_in = [torch.empty_like(t, device=dev) for t in h_inputs]
+    d_x = torch.empty(hx.shape, dtype=hx.dtype, device=dev)
+    out = {}
+    for name, fn in (("h2d", lambda: [d.copy_(h, non_blocking=True) for d, h in zip(d_in, h_inputs)]),
+                     ("d2h", lambda: hx.copy_(d_x, non_blocking=True))):
+        ts = []
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        nbytes = sum(t.numel() * t.element_size() for t in h_inputs) if name == "h2d" else hx.numel() * hx.element_size()
+        out[name] = {"ms": round(ms, 3), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+    del d_in, d_x
+    return out
 
 
 def run_long(args, w: I.Workload, world: int, rank: int, local: int):
