@@ -13,11 +13,14 @@ in HBM before timing.  Each rank runs an independent replica (sessions are
 independent; no collective on the data path), so scaling is weak.
 
 The default run measures the SR-shaped chunk (the largest configuration that
-fits one GPU) as the headline line and the base-DiT chunk under the key
-"base".  Printed: one JSON line on rank 0.  value = dense attention TFLOP per
-step / device time per step (whole job); e2e = the same with, every step, the
-host -> device copy of the step's q, k, v from pinned memory and the device ->
-host read of the updated state x inside the timed region.  The reference arm
+fits one GPU) as the headline line, and the base-DiT chunk, the long
+session (4 sessions x 64 chunks), the interpolation-chunk step and the DiT
+attention-block step under the keys "base", "long", "ibase" and "block".
+Printed: one JSON line on rank 0.  value = dense attention TFLOP per step /
+device time per step (whole job); e2e = the same through the C-ABI call that
+takes host buffers: every step, the host -> device copy of the step's q, k, v
+from pinned memory and the device -> host read of the updated state x inside
+the timed region.  The reference arm
 (--impl reference) times the fp64 CPU oracle on bounded samples of the same
 workload and extrapolates each to a full step.
 """
@@ -973,11 +976,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="default",
                     choices=["default", "base", "sr", "sr1", "long", "ibase", "block", "small", "tiny"],
-                    help="default: the SR-shaped chunk as the headline, the base-DiT chunk nested under 'base'")
+                    help="default: the SR-shaped chunk as the headline; the base-DiT chunk, the long session, the "
+                         "interpolation chunk and the DiT block nested under their names")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-exp-forms", action="store_true", help="skip the packed / fp32 exponential comparison")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="default run: skip the nested long-session, interpolation-chunk and DiT-block workloads")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the oracle's timed sample")
     ap.add_argument("--chunks", type=int, default=64, help="chunks of the long-session run (--config long)")
     args = ap.parse_args()
@@ -1000,6 +1006,14 @@ def main():
     res = run_ours(args, w, world, rank, local)
     if args.config == "default":
         res["base"] = nested(run_ours(args, I.WORKLOADS["base"], world, rank, local))
+        if not args.no_extra_workloads:
+            # the other configurations, each with its own timed region and clocks
+            sub = ("value", "unit", "ms_per_step", "steps", "latent_frames_per_s", "sustained_latent_frames_per_s",
+                   "chunk_latency_ms", "memory", "block_tflops", "kernels_ms", "kernel_rates", "gpu_launches",
+                   "clocks", "config")
+            for name, fn in (("long", run_long), ("ibase", run_interp), ("block", run_block)):
+                r = fn(args, I.WORKLOADS["long" if name == "long" else "base"], world, rank, local)
+                res[name] = {k: r[k] for k in sub if k in r}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if rank == 0:
