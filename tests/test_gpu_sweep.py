@@ -1,0 +1,152 @@
+"""Seeded random-shape sweeps of every kernel entry point against the fp64
+oracle, every output element compared (bars of tests/_util.py).
+
+The shapes are drawn from a fixed seed so that each run checks the same
+cases: degenerate sizes (a single query, a single key, empty segments, one
+row of W_o), sizes one either side of the 128-row tiles and of the 256-row
+query blocks, odd head counts, both head sizes, both W_o kernels, and RoPE
+grids with negative start times."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from streaming_avatar_video_gb300 import inputs as I
+from tests._util import assert_close, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def S():
+    import __graft_entry__ as g
+    g.build()
+    from streaming_avatar_video_gb300 import savgb
+    torch.cuda.set_device(0)
+    return savgb
+
+
+def bf16(shape, seed, kind, std=1.0, chunk=0):
+    return I.normal_bf16(shape, std, seed, kind, chunk)
+
+
+_NQ = [1, 2, 127, 128, 129, 255, 256, 257, 383, 700]
+_NKV = [0, 1, 2, 63, 127, 128, 129, 300, 511]
+
+
+def _attention_cases(n=16, seed=2024):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        n_segs = int(rng.integers(1, 4))
+        segs = [int(rng.choice(_NKV)) for _ in range(n_segs)]
+        if sum(segs) == 0:
+            segs[-1] = int(rng.choice(_NKV[1:]))
+        cases.append(dict(B=int(rng.integers(1, 4)), H=int(rng.integers(1, 5)), D=int(rng.choice([64, 128])),
+                          n_q=int(rng.choice(_NQ)), segs=segs, scale=float(rng.choice([0.0, 0.05, 0.3])),
+                          lse=bool(i % 2), seed=100 + i))
+    # degenerate ones, always: one query over one key, one query over many, keys only in the last segment
+    cases += [dict(B=1, H=1, D=128, n_q=1, segs=[1], scale=0.0, lse=True, seed=150),
+              dict(B=2, H=3, D=64, n_q=1, segs=[511, 1, 0], scale=0.0, lse=True, seed=151),
+              dict(B=1, H=2, D=128, n_q=2, segs=[0, 0, 1], scale=0.0, lse=False, seed=152)]
+    return cases
+
+
+@pytest.mark.parametrize("c", _attention_cases(), ids=lambda c: f"B{c['B']}H{c['H']}D{c['D']}q{c['n_q']}kv{c['segs']}")
+def test_attention_sweep(S, c):
+    B, H, D, n_q, seed = c["B"], c["H"], c["D"], c["n_q"], c["seed"]
+    q = bf16((B, n_q, H, D), seed, I.KIND_Q)
+    segs = [(bf16((B, n, H, D), seed, I.KIND_K, chunk=j), bf16((B, n, H, D), seed, I.KIND_V, chunk=j))
+            for j, n in enumerate(c["segs"])]
+    lse = torch.empty((B, H, n_q), dtype=torch.float32, device="cuda") if c["lse"] else None
+    o = S.chunk_attention(q.cuda(), [(k.cuda(), v.cuda()) for k, v in segs], scale=c["scale"], lse=lse)
+    S.savgb_device_check()
+    sc = c["scale"] if c["scale"] > 0 else 1.0 / math.sqrt(D)
+    osegs = [(f64(k), f64(v)) for k, v in segs]
+    assert_close(f64(o), O.attention(f64(q), osegs, sc), what=f"attention {c}")
+    if lse is not None:
+        kk = np.concatenate([k for k, _ in osegs], axis=1)
+        s = np.einsum("bnhd,bmhd->bhnm", f64(q), kk) * sc
+        m = s.max(-1, keepdims=True)
+        assert_close(f64(lse), m[..., 0] + np.log(np.exp(s - m).sum(-1)), max_abs=1e-3, mean_abs=1e-4,
+                     what=f"lse {c}")
+
+
+def _qrope_cases(n=8, seed=7):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        out.append(dict(B=int(rng.integers(1, 3)), H=int(rng.integers(1, 4)), D=int(rng.choice([64, 128])),
+                        grid=(int(rng.integers(1, 5)), int(rng.integers(1, 21)), int(rng.integers(1, 41))),
+                        t0=int(rng.integers(-5, 6)), ctx=int(rng.choice([0, 1, 90, 257])), seed=200 + i))
+    return out
+
+
+@pytest.mark.parametrize("c", _qrope_cases(), ids=lambda c: f"B{c['B']}H{c['H']}D{c['D']}g{c['grid']}t{c['t0']}")
+def test_attention_qrope_sweep(S, c):
+    B, H, D, (gt, gh, gw), t0, seed = c["B"], c["H"], c["D"], c["grid"], c["t0"], c["seed"]
+    n_q = gt * gh * gw
+    assert S.chunk_attention_qrope_fits(D, (gt, gh, gw))
+    q = bf16((B, n_q, H, D), seed, I.KIND_Q)
+    k = bf16((B, n_q, H, D), seed, I.KIND_K)
+    v = bf16((B, n_q, H, D), seed, I.KIND_V)
+    kc = bf16((B, c["ctx"], H, D), seed, I.KIND_K, chunk=1)
+    vc = bf16((B, c["ctx"], H, D), seed, I.KIND_V, chunk=1)
+    # chunk keys rotated by the oracle and rounded to bf16 (the kernel takes rotated keys)
+    k_rot = torch.from_numpy(O.rope3d(f64(k), gt, gh, gw, t0)).to(torch.bfloat16)
+    dsegs = ([(kc.cuda(), vc.cuda())] if c["ctx"] else []) + [(k_rot.cuda(), v.cuda())]
+    o = S.chunk_attention_qrope(q.cuda(), (gt, gh, gw), dsegs, t0=t0)
+    S.savgb_device_check()
+    osegs = ([(f64(kc), f64(vc))] if c["ctx"] else []) + [(f64(k_rot), f64(v))]
+    assert_close(f64(o), O.attention(O.rope3d(f64(q), gt, gh, gw, t0), osegs), what=f"qrope attention {c}")
+
+
+def _wo_cases(n=12, seed=99):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        hid_out = int(rng.choice([16, 48, 256, 400, 512, 768, 1024]))
+        out.append(dict(M=int(rng.choice([1, 7, 128, 255, 256, 257, 700, 1500])),
+                        hid_in=int(rng.choice([8, 24, 64, 200, 512, 1000])), hid_out=hid_out,
+                        bias=bool(rng.integers(0, 2)), with_v=bool(rng.integers(0, 2)),
+                        dt=float(rng.choice([0.01, 0.125, -0.3])), seed=300 + i))
+    return out
+
+
+@pytest.mark.parametrize("c", _wo_cases(), ids=lambda c: f"M{c['M']}k{c['hid_in']}n{c['hid_out']}")
+def test_out_proj_euler_sweep(S, c):
+    M, K, N, seed = c["M"], c["hid_in"], c["hid_out"], c["seed"]
+    o = bf16((M, K), seed, I.KIND_Q)
+    w = bf16((N, K), seed, I.KIND_WO, std=1.0 / math.sqrt(K))
+    x0 = torch.from_numpy(I.normal_f32((M, N), 1.0, seed, I.KIND_X))
+    b = torch.from_numpy(I.normal_f32((N,), 0.1, seed, I.KIND_BIAS)) if c["bias"] else None
+    x = x0.cuda()
+    v = torch.empty((M, N), dtype=torch.float32, device="cuda") if c["with_v"] else None
+    S.out_proj_euler_step(o.cuda(), w.cuda(), x, c["dt"], bias=None if b is None else b.cuda(), v_out=v)
+    S.savgb_device_check()
+    want_v = O.out_proj(f64(o), f64(w), None if b is None else f64(b))
+    if v is not None:
+        assert_close(f64(v), want_v, what=f"velocity {c}")
+    assert_close(f64(x), O.euler_update(f64(x0), want_v, c["dt"]), max_abs=1e-4, mean_abs=1e-5, what=f"x {c}")
+
+
+def _rope_cases(n=10, seed=5):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        out.append(dict(B=int(rng.integers(1, 3)), H=int(rng.integers(1, 9)), D=int(8 * rng.integers(1, 33)),
+                        grid=(int(rng.integers(1, 5)), int(rng.integers(1, 13)), int(rng.integers(1, 17))),
+                        t0=int(rng.integers(-8, 9)), base=float(rng.choice([100.0, 10000.0, 1e6])), seed=400 + i))
+    return out
+
+
+@pytest.mark.parametrize("c", _rope_cases(), ids=lambda c: f"B{c['B']}H{c['H']}D{c['D']}g{c['grid']}")
+def test_rope3d_sweep(S, c):
+    B, H, D, (gt, gh, gw), seed = c["B"], c["H"], c["D"], c["grid"], c["seed"]
+    x = bf16((B, gt * gh * gw, H, D), seed, I.KIND_K)
+    out = torch.empty_like(x).cuda()
+    S.rope3d_apply(x.cuda(), out, gt, gh, gw, c["t0"], c["base"])
+    S.savgb_device_check()
+    assert_close(f64(out), O.rope3d(f64(x), gt, gh, gw, c["t0"], c["base"]), what=f"rope3d {c}")
