@@ -539,11 +539,13 @@ def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world, i0=0):
     hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     n = max(3, min(args.steps, 60))
 
-    def step(i):
+    def step(i, read_back=True, ev=None):
         s_idx = (i0 + i) % w.steps
         last = s_idx == w.steps - 1
         hq, hk, hv = hsets[i & 1]
-        cs.step_host(hq, hk, hv, wo, x, dts[s_idx], last, x_host=hx)
+        cs.step_host(hq, hk, hv, wo, x, dts[s_idx], last, x_host=hx if read_back else None)
+        if ev is not None:
+            ev.record(stream)
         if last:
             cs.end_chunk()
 
@@ -562,14 +564,38 @@ def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world, i0=0):
         torch.cuda.synchronize()
     cs.sync()
     ms = max_over_ranks(world, a.elapsed_time(b)) / n
+    # diagnostics, after the timed region: the same loop with the uploads only,
+    # and the period of every step of one more pass (events on the compute stream)
+    i_next = 3 + n
+    a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a2.record(stream)
+    for i in range(i_next, i_next + n):
+        step(i, read_back=False)
+    b2.record(stream)
+    torch.cuda.synchronize()
+    cs.sync()
+    i_next += n
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    evs[0].record(stream)
+    for j, i in enumerate(range(i_next, i_next + n)):
+        step(i, ev=evs[j + 1])
+    cs.join_copies()
+    torch.cuda.synchronize()
+    cs.sync()
+    i_next += n
+    periods = [round(evs[j].elapsed_time(evs[j + 1]), 3) for j in range(n)]
     h2d = sum(t.numel() * t.element_size() for t in sets[0])
     d2h = x.numel() * x.element_size()
     return {"value": round(whole_job_rate(world, w.attn_flops(True), ms) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "clocks": clk.summary(), "copies_alone": copies,
+            "diagnostics": {"uploads_only_ms_per_step": round(a2.elapsed_time(b2) / n, 4),
+                            "step_periods_ms": periods,
+                            "what": "after the timed region: the same loop without read-backs, and the period of "
+                                    "each step of one more pass (events on the compute stream)"},
             "api": "C ABI chunk_stream_step_host: pinned host q/k/v in, x read back to pinned host memory every "
                    "step; the library overlaps the uploads and read-backs with the steps on two copy streams; "
-                   "measured right after the headline region"}, i0 + 3 + n
+                   "measured right after the headline region"}, i0 + i_next
 
 
 def time_copies_alone(h_inputs, hx, dev):
