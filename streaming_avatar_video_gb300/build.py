@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(PKG, "libsavgb.so")
 
 SOURCES = ["status.cu", "rope3d.cu", "attention.cu", "out_proj_euler.cu", "chunk_stream.cu",
            "chunk_step_noalloc.cu", "qkv_proj.cu"]
-HEADERS = ["common.h", "ptx.cuh", "gemm_tc.cuh"]
+HEADERS = ["common.h", "ptx.cuh", "gemm_tc.cuh", "gemm_pair.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -27,6 +27,7 @@
 #include <algorithm>
 
 #include "common.h"
+#include "gemm_pair.cuh"
 #include "gemm_tc.cuh"
 #include "ptx.cuh"
 
@@ -206,210 +207,53 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
 }
 
 // ------------------------------------------------------------ CTA-pair kernel
-// Persistent CTA-pair GEMM: a cluster of two CTAs computes 256 x 256 tiles of
-// v with tcgen05.mma.cta_group::2 (M = 256: each CTA holds 128 rows of O and
-// 128 of the 256 rows of the W_o tile).  Each CTA keeps two 128 x 256 fp32
-// accumulators in TMEM, so the Euler epilogue of one tile (x through the
-// shared-memory chunk staging above) runs while the next tile's MMAs
-// accumulate into the other buffer, and the x read-modify-write traffic no
-// longer idles the tensor cores.
-//   warp 0      TMA producer of this CTA's A rows and B half (6-stage ring)
-//   warp 1      TMEM allocation (both CTAs); lane 0 of the even CTA issues
-//               every MMA and commits to both CTAs' barriers
-//   warp 2      (odd CTA) relays "stage full" to the even CTA's barrier
-//   warps 4-11  epilogue: warp -> 32 rows (its TMEM lane quadrant) x 128
-//               columns (one half of the tile)
+// Persistent CTA-pair GEMM (gemm_pair.cuh): a cluster of two CTAs computes
+// 256 x 256 tiles of v with tcgen05.mma.cta_group::2, and each CTA keeps two
+// 128 x 256 fp32 accumulators in TMEM, so the Euler epilogue of one tile (x
+// through the shared-memory chunk staging above) runs while the next tile's
+// MMAs accumulate into the other buffer, and the x read-modify-write traffic
+// no longer idles the tensor cores.  Epilogue: warps 4-11, warp -> 32 rows
+// (its TMEM lane quadrant) x 128 columns (one half of the tile).
 namespace pair {
-constexpr int kThreads = 384;
-constexpr int kBK = 64;
 constexpr int kStages = 6;
-constexpr int kABytes = 128 * kBK * 2;  // 16 KiB: this CTA's 128 rows of O
-constexpr int kBBytes = 128 * kBK * 2;  // 16 KiB: this CTA's 128 rows of the W_o tile
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kPairXBufs = 1;
-constexpr int kXStage = kStages * kStageBytes;
-constexpr int kBar = kXStage + 8 * kPairXBufs * kXChunkBytes;
-constexpr int kFull = 0, kEmpty = kStages, kAccFull = 2 * kStages, kAccEmpty = kAccFull + 2, kDrain = kAccEmpty + 2;
-constexpr int kXBar = kDrain + 1;
-constexpr int kNumBars = kXBar + 8 * kPairXBufs;
-constexpr int kMisc = kBar + kNumBars * 8;
-constexpr int kDynSmem = kMisc + 16 + 1024;
-static_assert(kDynSmem <= 227 * 1024, "shared memory budget");
-
-__device__ __forceinline__ void give_up(const WoParams& p, volatile int* abort, unsigned code) {
-  if (atomicExch(const_cast<int*>(abort), 1) == 0) {
-    atomicOr(&p.err->flags, kErrGemmWait);
-    atomicCAS(&p.err->where, 0u, code);
-  }
-}
+using L = gemm_pair::Layout<kStages, 8>;  // one x barrier per epilogue warp
+static_assert(kXChunkBytes == gemm_pair::kWarpStaging, "one x chunk per epilogue warp");
+static_assert(L::kDynSmem <= 227 * 1024, "shared memory budget");
 }  // namespace pair
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_pair::kThreads, 1)
     wo_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_x, const WoParams p, int n_tiles_n, int n_tiles) {
-  using namespace pair;
+  using L = pair::L;
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = dev::smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMisc);
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + kMisc + 4);
+  const gemm_pair::Ctx c = gemm_pair::setup<L>(smem_raw, &map_a, &map_b, &map_x);
+  const gemm_pair::Hook hk{p.err, kErrGemmWait, p.fault_iter, p.wait_limit_ns};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = dev::cluster_rank();
-  const bool leader = rank == 0;
-  const int cluster = static_cast<int>(blockIdx.x >> 1);
-  const int n_clusters = static_cast<int>(gridDim.x >> 1);
-  const int kb_count = (p.K + kBK - 1) / kBK;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      dev::mbar_init(&bars[kFull + s], leader ? 2 : 1);  // the even CTA's: its own load + the odd CTA's relay
-      dev::mbar_init(&bars[kEmpty + s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      dev::mbar_init(&bars[kAccFull + b], 1);
-      dev::mbar_init(&bars[kAccEmpty + b], 16);  // the 8 epilogue warps of both CTAs (even CTA's copy)
-    }
-    dev::mbar_init(&bars[kDrain], 1);
-    for (int i = 0; i < 8 * kPairXBufs; ++i) dev::mbar_init(&bars[kXBar + i], 1);
-    *abort = 0;
-    dev::fence_barrier_init();
-  }
-  if (warp == 0 && lane == 0) {
-    dev::tma_prefetch_desc(&map_a);
-    dev::tma_prefetch_desc(&map_b);
-    dev::tma_prefetch_desc(&map_x);
-  }
-  __syncthreads();
-  dev::cluster_sync();  // both CTAs' barriers exist before any remote arrive
-  if (warp == 1) {
-    dev::tmem_alloc_pair(tmem_slot, 512);
-    dev::tmem_relinquish_pair();
-  }
-  dev::tc_fence_before();
-  __syncthreads();
-  dev::cluster_sync();
-  dev::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const int kb_count = (p.K + gemm_pair::kBK - 1) / gemm_pair::kBK;
   dev::griddep_launch_dependents();
   dev::griddep_wait();  // the set-up above overlaps the previous kernel (the attention)
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = cluster; t < n_tiles && ok; t += n_clusters) {
-        const int m0 = (t / n_tiles_n) * 256 + static_cast<int>(rank) * 128;
-        const int nb = (t % n_tiles_n) * 256 + static_cast<int>(rank) * 128;
-        for (int kb = 0; kb < kb_count; ++kb, ++it) {
-          const int st = static_cast<int>(it % kStages);
-          const uint32_t use = it / kStages;
-          if (use > 0 && !dev::mbar_wait(&bars[kEmpty + st], (use - 1) & 1, abort, p.wait_limit_ns)) {
-            give_up(p, abort, 11);
-            ok = false;
-            break;
-          }
-          uint8_t* sa = smem + st * kStageBytes;
-          dev::mbar_arrive_expect_tx(&bars[kFull + st], kStageBytes);
-          dev::tma_load_2d(sa, &map_a, &bars[kFull + st], kb * kBK, m0);
-          dev::tma_load_2d(sa + kABytes, &map_b, &bars[kFull + st], kb * kBK, nb);
-        }
-      }
-      // every issued copy has landed in this CTA before it may exit
-      volatile int never = 0;
-      const uint32_t first = it > static_cast<uint32_t>(kStages) ? it - kStages : 0;
-      for (uint32_t t = first; t < it; ++t) {
-        if (leader) dev::mbar_wait_cluster(&bars[kFull + t % kStages], (t / kStages) & 1, &never, p.wait_limit_ns);
-        else dev::mbar_wait(&bars[kFull + t % kStages], (t / kStages) & 1, &never, p.wait_limit_ns);
-      }
-    }
+    if (lane == 0) gemm_pair::produce<L>(c, hk, &map_a, &map_b, n_tiles_n, n_tiles, kb_count);
   } else if (warp == 1) {
-    if (leader) {
-      // ---------------------------------------------------------- MMA issuer
-      // the whole warp runs the loop (warp-uniform state); one elected lane
-      // issues the MMAs and commits
-      const bool issuer = dev::elect_one();
-      constexpr uint32_t idesc = dev::idesc_bf16_f32(256, 256, false, false);
-      const uint64_t d0 = dev::sdesc_sw128(dev::smem_u32(smem), 16, 1024);
-      uint32_t it = 0;
-      int tile_i = 0;
-      bool ok = true;
-      for (int t = cluster; t < n_tiles && ok; t += n_clusters, ++tile_i) {
-        const int buf = tile_i & 1;
-        const uint32_t buse = static_cast<uint32_t>(tile_i >> 1);
-        if (buse > 0 &&
-            !__all_sync(0xffffffffu, dev::mbar_wait_cluster(&bars[kAccEmpty + buf], (buse - 1) & 1, abort, p.wait_limit_ns))) {
-          if (issuer) give_up(p, abort, 12);
-          break;
-        }
-        dev::tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>(buf * 256);
-        for (int kb = 0; kb < kb_count; ++kb, ++it) {
-          const int st = static_cast<int>(it % kStages);
-          if (!__all_sync(0xffffffffu, dev::mbar_wait(&bars[kFull + st], (it / kStages) & 1, abort, p.wait_limit_ns))) {
-            if (issuer) give_up(p, abort, 13);
-            ok = false;
-            break;
-          }
-          dev::tc_fence_after();
-          if (issuer) {
-            const uint64_t ds = d0 + static_cast<uint32_t>((st * kStageBytes) >> 4);
-            #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              const uint32_t koff = (k * 32) >> 4;
-              dev::mma_ss_pair(d, ds + koff, ds + ((kABytes >> 4) + koff), idesc, (kb > 0 || k > 0) ? 1u : 0u);
-            }
-            dev::mma_commit_pair(&bars[kEmpty + st], 3);
-          }
-        }
-        if (ok && issuer) dev::mma_commit_pair(&bars[kAccFull + buf], 3);
-      }
-      // every MMA has completed before TMEM is released
-      if (issuer) dev::mma_commit_pair(&bars[kDrain], 1);
-      __syncwarp();
-      volatile int never = 0;
-      dev::mbar_wait(&bars[kDrain], 0, &never, p.wait_limit_ns);
-    }
+    if (c.leader) gemm_pair::mma<L>(c, hk, n_tiles, kb_count);
   } else if (warp == 2) {
-    if (lane == 0 && !leader) {
-      // ----------------------------------------------- relay (odd CTA only)
-      const uint32_t full0 = dev::mapa_shared(&bars[kFull], 0);
-      // test hook: the first cluster leaves one relay out (fault_iter < 0: never)
-      const int64_t skip = cluster == 0 ? p.fault_iter : -1;
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = cluster; t < n_tiles && ok; t += n_clusters) {
-        for (int kb = 0; kb < kb_count; ++kb, ++it) {
-          const int st = static_cast<int>(it % kStages);
-          if (!dev::mbar_wait(&bars[kFull + st], (it / kStages) & 1, abort, p.wait_limit_ns)) {
-            give_up(p, abort, 14);
-            ok = false;
-            break;
-          }
-          // relaxed: the TMA completion just observed already placed the
-          // data; a release arrive at cluster scope held this thread ~0.8 us
-          // per stage and throttled the whole pipeline to half speed
-          if (static_cast<int64_t>(it) != skip) dev::mbar_arrive_cluster_relaxed(full0 + static_cast<uint32_t>(st * 8));
-        }
-      }
-    }
+    if (lane == 0 && !c.leader) gemm_pair::relay<L>(c, hk, n_tiles, kb_count);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 4;
     const int quad = warp & 3;
     const int ch = ew >> 2;
-    uint8_t* xb = smem + kXStage + ew * (kPairXBufs * kXChunkBytes);
-    uint64_t* xbar = &bars[kXBar + ew * kPairXBufs];
-    const uint32_t acc_empty0 = dev::mapa_shared(&bars[kAccEmpty], 0);
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    uint8_t* xb = c.smem + L::kStaging + ew * kXChunkBytes;
+    uint64_t* xbar = &c.bars[L::kExtraBar + ew];
+    const uint32_t t_lane = c.tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const float dt = p.dt;
-    uint32_t xwaits[kPairXBufs] = {};
+    uint32_t xwaits = 0;
     int tile_i = 0;
-    for (int t = cluster; t < n_tiles; t += n_clusters, ++tile_i) {
+    for (int t = c.cluster; t < n_tiles; t += c.n_clusters, ++tile_i) {
       const int buf = tile_i & 1;
-      const int row_base = (t / n_tiles_n) * 256 + static_cast<int>(rank) * 128 + quad * 32;
+      const int row_base = (t / n_tiles_n) * 256 + static_cast<int>(c.rank) * 128 + quad * 32;
       const int ncol0 = (t % n_tiles_n) * 256 + ch * 128;
       {
         // pull this warp's rows of x for the tile into L2 while the MMAs run
@@ -417,32 +261,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         const int ncols = min(128, p.N - ncol0);
         if (m < p.M && ncols > 0) dev::prefetch_l2(p.x + static_cast<int64_t>(m) * p.N + ncol0, ncols * 4);
       }
-      // every lane polls; a vote keeps the warp on one path
-      if (!__all_sync(0xffffffffu, dev::mbar_wait_cluster(&bars[kAccFull + buf], (tile_i >> 1) & 1, abort, p.wait_limit_ns))) {
-        give_up(p, abort, 15);
-        break;
-      }
-      dev::tc_fence_after();
+      if (!gemm_pair::acc_wait<L>(c, hk, tile_i)) break;
       const int nch = row_base < p.M ? max(0, (min(128, p.N - ncol0) + kXChunk - 1) / kXChunk) : 0;
-      if (lane == 0)
-        for (int i = 0; i < kPairXBufs && i < nch; ++i) {
-          dev::mbar_arrive_expect_tx(&xbar[i], kXChunkBytes);
-          dev::tma_load_2d(xb + i * kXChunkBytes, &map_x, &xbar[i], ncol0 + i * kXChunk, row_base);
-        }
+      if (lane == 0 && nch > 0) {
+        dev::mbar_arrive_expect_tx(xbar, kXChunkBytes);
+        dev::tma_load_2d(xb, &map_x, xbar, ncol0, row_base);
+      }
       bool ok = true;
       #pragma unroll 1
       for (int cc = 0; cc < nch; ++cc) {
-        const int bi = cc % kPairXBufs;
         uint32_t acc[32];
         dev::tmem_ld32(t_lane + static_cast<uint32_t>(buf * 256 + ch * 128 + cc * kXChunk), acc);
-        const bool xg = __all_sync(0xffffffffu, dev::mbar_wait(&xbar[bi], xwaits[bi] & 1, abort, p.wait_limit_ns));
-        ++xwaits[bi];
+        const bool xg = __all_sync(0xffffffffu, dev::mbar_wait(xbar, xwaits & 1, c.abort, p.wait_limit_ns));
+        ++xwaits;
         if (!xg) {
-          give_up(p, abort, 16);
+          gemm_pair::give_up(hk, c.abort, 16);
           ok = false;
           break;
         }
-        float4* row = reinterpret_cast<float4*>(xb + bi * kXChunkBytes + lane * 128);
+        float4* row = reinterpret_cast<float4*>(xb + lane * 128);
         const int n = ncol0 + cc * kXChunk;
         #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -459,41 +296,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         dev::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          dev::tma_store_2d(&map_x, xb + bi * kXChunkBytes, n, row_base);
+          dev::tma_store_2d(&map_x, xb, n, row_base);
           dev::bulk_commit();
-          if (cc + kPairXBufs < nch) {
+          if (cc + 1 < nch) {
+            // the buffer is reloaded once its store has read it
             dev::bulk_wait_read_all();
-            dev::mbar_arrive_expect_tx(&xbar[bi], kXChunkBytes);
-            dev::tma_load_2d(xb + bi * kXChunkBytes, &map_x, &xbar[bi], n + kPairXBufs * kXChunk, row_base);
+            dev::mbar_arrive_expect_tx(xbar, kXChunkBytes);
+            dev::tma_load_2d(xb, &map_x, xbar, n + kXChunk, row_base);
           }
         }
       }
       // this warp has read its part of the accumulator: release the buffer
-      dev::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (leader) dev::mbar_arrive(&bars[kAccEmpty + buf]);
-        else dev::mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(buf * 8));
-        dev::bulk_wait_read_all();  // the staging buffers are reloaded by the next tile
-      }
+      gemm_pair::acc_release<L>(c, tile_i);
+      if (lane == 0) dev::bulk_wait_read_all();  // the staging buffer is reloaded by the next tile
       __syncwarp();
       if (!ok) break;
     }
     if (lane == 0) dev::bulk_wait_all();
     __syncwarp();
   }
-
-  // neither CTA leaves (or frees TMEM) while its peer may still use its
-  // shared memory or run pair MMAs
-  dev::tc_fence_before();
-  __syncthreads();
-  dev::cluster_sync();
-  if (warp == 1) {
-    dev::tc_fence_after();
-    dev::tmem_dealloc_pair(tmem, 512);
-  }
-  __syncthreads();
-  dev::cluster_sync();
+  gemm_pair::teardown(c);
 }
 
 template <int BN>
@@ -552,17 +374,20 @@ int validate_out_proj(const void* o, const void* w, const float* bias, const flo
 int launch_pair(const void* o, const void* w, const float* bias, float* x, int64_t M, int K, int N, float dt,
                 int sms, cudaStream_t stream) {
   static bool attr_done[64] = {false};
+  static int max_clusters[64] = {0};
   int dev_id = 0;
   SAVGB_CUDA(cudaGetDevice(&dev_id));
   if (!attr_done[dev_id & 63]) {
     SAVGB_CUDA(cudaFuncSetAttribute(wo_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    pair::kDynSmem));
+                                    pair::L::kDynSmem));
+    int rc = gemm_pair::max_clusters(wo_pair_kernel, sms, pair::L::kDynSmem, &max_clusters[dev_id & 63]);
+    if (rc) return rc;
     attr_done[dev_id & 63] = true;
   }
   CUtensorMap ma, mb, mx;
   const uint64_t da[2] = {(uint64_t)K, (uint64_t)M};
   const uint64_t sa[1] = {(uint64_t)K * 2};
-  const uint32_t box128[2] = {pair::kBK, 128};
+  const uint32_t box128[2] = {gemm_pair::kBK, 128};
   int rc = encode_tiled(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o, da, sa, box128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
   const uint64_t db[2] = {(uint64_t)K, (uint64_t)N};
@@ -583,26 +408,9 @@ int launch_pair(const void* o, const void* w, const float* bias, float* x, int64
   const int n_tiles_n = N / 256;
   const int n_tiles = (int)((M + 255) / 256) * n_tiles_n;
   // one wave of pairs: as many clusters as can be resident at once
-  static int max_clusters[64] = {0};
-  if (max_clusters[dev_id & 63] == 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(2 * (sms / 2)));
-    cfg.blockDim = dim3(pair::kThreads);
-    cfg.dynamicSmemBytes = pair::kDynSmem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    SAVGB_CUDA(cudaOccupancyMaxActiveClusters(&n, wo_pair_kernel, &cfg));
-    max_clusters[dev_id & 63] = n > 0 ? n : 1;
-  }
   const int clusters = std::min(n_tiles, max_clusters[dev_id & 63]);
-  SAVGB_CUDA(launch_dependent(wo_pair_kernel, dim3((unsigned)(2 * clusters)), dim3(pair::kThreads), pair::kDynSmem,
-                              stream, ma, mb, mx, p, n_tiles_n, n_tiles));
+  SAVGB_CUDA(launch_dependent(wo_pair_kernel, dim3((unsigned)(2 * clusters)), dim3(gemm_pair::kThreads),
+                              pair::L::kDynSmem, stream, ma, mb, mx, p, n_tiles_n, n_tiles));
   SAVGB_CUDA(cudaGetLastError());
   return SAVGB_OK;
 }

@@ -795,8 +795,10 @@ def test_attention_qrope_parity(S, D, B, gt, gh, gw, t0, segs):
 # ------------------------------------------------------- DiT attention block
 
 @pytest.mark.parametrize("B,H,D,gt,gh,gw,t0", [
-    (1, 2, 64, 2, 4, 4, 0),     # tiny: 32 rows, 3*hid = 384 (128-column tiles)
-    (2, 2, 128, 3, 5, 7, 1),    # ragged: 210 rows over two batches, t0 = 1
+    (1, 2, 64, 2, 4, 4, 0),     # tiny: 32 rows, 3*hid = 384 (single-CTA kernel, 128-column tiles)
+    (2, 2, 128, 3, 5, 7, 1),    # ragged: 210 rows over two batches, t0 = 1 (CTA-pair kernel, one tile per cluster)
+    (2, 8, 128, 3, 10, 30, 0),  # CTA pair: 96 tiles of 256 x 256 over 76 clusters, both accumulator buffers
+    (1, 8, 64, 2, 7, 9, -1),    # CTA pair at D = 64: 126 rows (one partial row block), t0 = -1
 ])
 def test_qkv_rope_project_parity(S, B, H, D, gt, gh, gw, t0):
     N, hid = gt * gh * gw, H * D
