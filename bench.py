@@ -13,9 +13,10 @@ in HBM before timing.  Each rank runs an independent replica (sessions are
 independent; no collective on the data path), so scaling is weak.
 
 The default run measures the SR-shaped chunk (the largest configuration that
-fits one GPU) as the headline line, and the base-DiT chunk, the long
-session (4 sessions x 64 chunks), the interpolation-chunk step and the DiT
-attention-block step under the keys "base", "long", "ibase" and "block".
+fits one GPU) as the headline line, and the base-DiT chunk, the 1-step SR
+chunk, the long session (4 sessions x 64 chunks), the interpolation-chunk step
+and the DiT attention-block step under the keys "base", "sr1", "long",
+"ibase" and "block".
 Printed: one JSON line on rank 0.  value = dense attention TFLOP per step /
 device time per step (whole job); e2e = the same through the C-ABI call that
 takes host buffers: every step, the host -> device copy of the step's q, k, v
@@ -63,7 +64,8 @@ def attn_traffic(workload: str):
     for f in ("attention.cu", "ptx.cuh", "common.h"):
         with open(os.path.join(ROOT, "streaming_avatar_video_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    return ATTN_TRAFFIC.get(h.hexdigest(), {}).get(workload)
+    # the 1-step SR chunk launches the same attention as the SR chunk
+    return ATTN_TRAFFIC.get(h.hexdigest(), {}).get("sr" if workload == "sr1" else workload)
 
 
 NOMINAL_BF16_TFLOPS = 2250.0
@@ -1033,6 +1035,10 @@ def main():
     if args.config == "default":
         res["base"] = nested(run_ours(args, I.WORKLOADS["base"], world, rank, local))
         if not args.no_extra_workloads:
+            # the 1-step SR chunk: every step ends a chunk and rolls the boundary
+            sub_args = argparse.Namespace(**vars(args))
+            sub_args.no_e2e, sub_args.no_exp_forms = True, True
+            res["sr1"] = nested(run_ours(sub_args, I.WORKLOADS["sr1"], world, rank, local))
             # the other configurations, each with its own timed region and clocks
             sub = ("value", "unit", "ms_per_step", "steps", "latent_frames_per_s", "sustained_latent_frames_per_s",
                    "chunk_latency_ms", "memory", "block_tflops", "kernels_ms", "kernel_rates", "gpu_launches",
