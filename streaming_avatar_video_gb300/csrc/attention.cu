@@ -62,7 +62,9 @@ constexpr int kRegsHigh = 208;  // softmax warpgroups after setmaxnreg.inc
 constexpr int kRegPoolNeeded = 128 * kRegsLow + 256 * kRegsHigh;
 constexpr int kBlockQ = 256;  // two 128-row tiles
 constexpr int kTileKV = 128;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// a tile whose probabilities against the running max sum to more than this
+// (2^8) moves the max; below it no probability exceeds 2^8
+constexpr float kTileSumLimit = 256.0f;
 // K / V ring depths: 128-row tiles of 32 KiB (D=128) or 16 KiB (D=64)
 #ifndef SAVGB_ATTN_KS128
 #define SAVGB_ATTN_KS128 3
@@ -216,6 +218,62 @@ __device__ __forceinline__ void rope_q_row(uint8_t* sQ, int tile_bytes, const fl
       SAVGB_QROT(w0, 0) SAVGB_QROT(w1, 1) SAVGB_QROT(w2, 2) SAVGB_QROT(w3, 3)
       #undef SAVGB_QROT
       *cell = make_uint4(w0, w1, w2, w3);
+    }
+  }
+}
+
+// One thread's row of a 128-column score tile from tensor memory; columns
+// at or past `valid` (a segment's ragged tail) read as -inf.
+__device__ __forceinline__ void load_scores(uint32_t tS, uint32_t (&sr)[128], int valid) {
+  uint32_t (&lo)[64] = *reinterpret_cast<uint32_t(*)[64]>(&sr[0]);
+  uint32_t (&hi)[64] = *reinterpret_cast<uint32_t(*)[64]>(&sr[64]);
+  dev::tmem_ld64(tS, lo);
+  dev::tmem_ld64(tS + 64, hi);
+  if (valid < kTileKV) {
+    #pragma unroll
+    for (int c = 0; c < kTileKV; ++c)
+      if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
+  }
+}
+
+// Row max: a shallow tree of 3-input maxes (128 -> 43 -> 15 -> 5 -> 2 -> 1).
+__device__ __forceinline__ float row_max(const float* s) {
+  float t1[43];
+  #pragma unroll
+  for (int i = 0; i < 42; ++i) t1[i] = dev::fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+  t1[42] = fmaxf(s[126], s[127]);
+  float t2[15];
+  #pragma unroll
+  for (int i = 0; i < 14; ++i) t2[i] = dev::fmax3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
+  t2[14] = t1[42];
+  float t3[5];
+  #pragma unroll
+  for (int i = 0; i < 5; ++i) t3[i] = dev::fmax3(t2[3 * i], t2[3 * i + 1], t2[3 * i + 2]);
+  return fmaxf(dev::fmax3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4]));
+}
+
+// The tile's probabilities p = 2^(s * sl2 - m) as 64 bf16x2 words (the PV
+// operand), nm = -m, and their sum in (l0, l1).
+// EXACT_L: fp32 exponentials (one MUFU operation per score) summed exactly,
+// as the log-sum-exp output needs; otherwise one packed bf16x2 exponential
+// per two scores on the exponents rounded to bf16, whose result is already
+// the operand, and the sum adds exactly those bf16 values in fp32 (~0.3 %
+// low on average against fp32 exponentials, which cancels in O).
+template <bool EXACT_L>
+__device__ __forceinline__ void tile_exp(const float* s, float sl2, float nm, uint32_t (&pk)[64], float& l0,
+                                         float& l1) {
+  #pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    float y0, y1;
+    dev::ffma2(y0, y1, s[2 * i], s[2 * i + 1], sl2, nm);
+    if constexpr (EXACT_L) {
+      const float p0 = dev::ex2_approx(y0);
+      const float p1 = dev::ex2_approx(y1);
+      dev::fadd2(l0, l1, p0, p1);
+      pk[i] = dev::pack_bf16x2(p0, p1);
+    } else {
+      pk[i] = dev::ex2_bf16x2(dev::pack_bf16x2(y0, y1));
+      dev::add_bf16x2_to_f32(l0, l1, pk[i]);
     }
   }
 }
@@ -496,37 +554,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       dev::tc_fence_after();
-      uint32_t sr[128];
+      // Exponentials against the running max m, no row max: if the tile's
+      // probabilities sum to at most 2^8, none exceeds 2^8 (the bound the lazy
+      // rescale keeps).  Otherwise (always on the first tile, rarely later)
+      // the row takes the exact max of the tile, O and l are rescaled, and the
+      // tile is recomputed; S is still intact in tensor memory until P is
+      // written over it.
+      uint32_t pk[64];
+      float l0 = 0.f, l1 = 0.f;
       {
-        uint32_t (&lo)[64] = *reinterpret_cast<uint32_t(*)[64]>(&sr[0]);
-        uint32_t (&hi)[64] = *reinterpret_cast<uint32_t(*)[64]>(&sr[64]);
-        dev::tmem_ld64(tS, lo);
-        dev::tmem_ld64(tS + 64, hi);
+        uint32_t sr[128];
+        load_scores(tS, sr, valid);
+        tile_exp<EXACT_L>(reinterpret_cast<const float*>(sr), sl2, -m, pk, l0, l1);
       }
-      float* s = reinterpret_cast<float*>(sr);
-      if (valid < kTileKV) {
-        #pragma unroll
-        for (int c = 0; c < kTileKV; ++c)
-          if (c >= valid) s[c] = -INFINITY;
-      }
-      // row max: a shallow tree of 3-input maxes (128 -> 43 -> 15 -> 5 -> 2 -> 1)
-      float t1[43];
-      #pragma unroll
-      for (int i = 0; i < 42; ++i) t1[i] = dev::fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
-      t1[42] = fmaxf(s[126], s[127]);
-      float t2[15];
-      #pragma unroll
-      for (int i = 0; i < 14; ++i) t2[i] = dev::fmax3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
-      t2[14] = t1[42];
-      float t3[5];
-      #pragma unroll
-      for (int i = 0; i < 5; ++i) t3[i] = dev::fmax3(t2[3 * i], t2[3 * i + 1], t2[3 * i + 2]);
-      const float mx0 = dev::fmax3(t3[0], t3[1], t3[2]);
-      const float mx1 = fmaxf(t3[3], t3[4]);
-      const float mx = fmaxf(mx0, mx1) * sl2;
-      const float m_new = fmaxf(m, mx);
-      const bool need = m_new > m + kRescaleThreshold;
+      const bool need = !(l0 + l1 <= kTileSumLimit);  // also true for inf / NaN (first tile: m = -inf)
       if (__any_sync(0xffffffffu, need)) {
+        uint32_t sr[128];
+        load_scores(tS, sr, valid);
+        const float* s = reinterpret_cast<const float*>(sr);
+        const float mx = row_max(s) * sl2;
+        const float m_new = fmaxf(m, mx);
         const float alpha = need ? dev::ex2_approx(m - m_new) : 1.f;
         if (need) {
           m = m_new;
@@ -542,30 +589,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             dev::tmem_st32(tO + c, o);
           }
         }
+        l0 = 0.f;
+        l1 = 0.f;
+        tile_exp<EXACT_L>(s, sl2, -m, pk, l0, l1);
       }
-      const float nm = -m;
-      float l0 = 0.f, l1 = 0.f;
-      #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-        #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float y0, y1;
-          dev::ffma2(y0, y1, s[half * 64 + 2 * i], s[half * 64 + 2 * i + 1], sl2, nm);
-          if constexpr (EXACT_L) {
-            const float p0 = dev::ex2_approx(y0);
-            const float p1 = dev::ex2_approx(y1);
-            dev::fadd2(l0, l1, p0, p1);
-            pk[i] = dev::pack_bf16x2(p0, p1);
-          } else {
-            // p = 2^(s*scale - m) for two scores in one MUFU operation on the
-            // exponents rounded to bf16; the result is already P's MMA
-            // operand, and the row sum adds exactly those bf16 values in fp32
-            pk[i] = dev::ex2_bf16x2(dev::pack_bf16x2(y0, y1));
-            dev::add_bf16x2_to_f32(l0, l1, pk[i]);
-          }
-        }
-        dev::tmem_st32(tS + half * 32, pk);
+      {
+        uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
+        uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
+        dev::tmem_st32(tS, p0);
+        dev::tmem_st32(tS + 32, p1);
       }
       // publish the tile's probabilities: the PV product may start
       dev::tc_fence_before();
