@@ -53,8 +53,8 @@ METRIC = "chunk-attention TFLOP/s (% of bf16 tensor peak); latent frames/s per d
 # change of them reports null.
 ATTN_TRAFFIC = {
     # profiles/chunk_attention_base.md and profiles/chunk_attention_sr.md: the fused-RoPE kernel the stream
-    # runs; base 290.340 MB read + 60.136 MB written, SR 1.48 GB read + 295.68 MB written
-    "b276d2b26209180403689079af1542a65cc7a049031bd103eff0ff2a633eac54": {"base": 350476288, "sr": 1775680000},
+    # runs; base 290.046 MB read + 61.018 MB written, SR 1580.464 MB read + 296.106 MB written
+    "7f8e8219ad2d90b40116e1d7d80ea029c9e623efa9546b17baaccf0bc555c84d": {"base": 351064832, "sr": 1876570368},
 }
 
 
