@@ -257,23 +257,34 @@ __device__ __forceinline__ float row_max(const float* s) {
 // EXACT_L: fp32 exponentials (one MUFU operation per score) summed exactly,
 // as the log-sum-exp output needs; otherwise one packed bf16x2 exponential
 // per two scores on the exponents rounded to bf16, whose result is already
-// the operand, and the sum adds exactly those bf16 values in fp32 (~0.3 %
-// low on average against fp32 exponentials, which cancels in O).
+// the operand; the sum adds those bf16 values two words at a time in bf16x2
+// and then in fp32 (~0.3 % low on average against fp32 exponentials, which
+// cancels in O).
 template <bool EXACT_L>
 __device__ __forceinline__ void tile_exp(const float* s, float sl2, float nm, uint32_t (&pk)[64], float& l0,
                                          float& l1) {
-  #pragma unroll
-  for (int i = 0; i < 64; ++i) {
-    float y0, y1;
-    dev::ffma2(y0, y1, s[2 * i], s[2 * i + 1], sl2, nm);
-    if constexpr (EXACT_L) {
+  if constexpr (EXACT_L) {
+    #pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      float y0, y1;
+      dev::ffma2(y0, y1, s[2 * i], s[2 * i + 1], sl2, nm);
       const float p0 = dev::ex2_approx(y0);
       const float p1 = dev::ex2_approx(y1);
       dev::fadd2(l0, l1, p0, p1);
       pk[i] = dev::pack_bf16x2(p0, p1);
-    } else {
+    }
+  } else {
+    #pragma unroll
+    for (int i = 0; i < 64; i += 2) {
+      float y0, y1, y2, y3;
+      dev::ffma2(y0, y1, s[2 * i], s[2 * i + 1], sl2, nm);
+      dev::ffma2(y2, y3, s[2 * i + 2], s[2 * i + 3], sl2, nm);
       pk[i] = dev::ex2_bf16x2(dev::pack_bf16x2(y0, y1));
-      dev::add_bf16x2_to_f32(l0, l1, pk[i]);
+      pk[i + 1] = dev::ex2_bf16x2(dev::pack_bf16x2(y2, y3));
+      // two words' probabilities added pairwise in bf16x2, then widened
+      // exactly into the fp32 sums: half the fp32 additions, one more bf16
+      // rounding per pair of probabilities in the denominator only
+      dev::add_bf16x2_to_f32(l0, l1, dev::add_bf16x2(pk[i], pk[i + 1]));
     }
   }
 }

@@ -443,6 +443,13 @@ __device__ __forceinline__ void add_bf16x2_to_f32(float& a0, float& a1, uint32_t
       : "r"(h));
 }
 
+// (a + b) of two bf16x2 words, per half, rounded to nearest even.
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Packed fp32 pairs (sm_100+): one instruction for two lanes of work.
 // (y0, y1) = (x0 * a + c0, x1 * a + c1)
 __device__ __forceinline__ void ffma2(float& y0, float& y1, float x0, float x1, float a, float c) {
