@@ -65,7 +65,9 @@ def test_attention_sweep(S, c):
     S.savgb_device_check()
     sc = c["scale"] if c["scale"] > 0 else 1.0 / math.sqrt(D)
     osegs = [(f64(k), f64(v)) for k, v in segs]
-    assert_close(f64(o), O.attention(f64(q), osegs, sc), what=f"attention {c}")
+    mx, mn = assert_close(f64(o), O.attention(f64(q), osegs, sc), what=f"attention {c}")
+    print(f"attention sweep {c['B']}x{c['H']}x{c['D']} q{c['n_q']} kv{c['segs']} scale {c['scale']}: "
+          f"max-abs {mx:.2e} mean-abs {mn:.2e}")
     if lse is not None:
         kk = np.concatenate([k for k, _ in osegs], axis=1)
         s = np.einsum("bnhd,bmhd->bhnm", f64(q), kk) * sc
