@@ -148,6 +148,13 @@ typedef savgb_kv_segment kv_segment_t;
  * bf16 values in fp32.  With lse non-NULL the kernel instead takes fp32
  * exponentials and exact fp32 row sums (the packed form's sums run ~0.3 %
  * low, which cancels in O but not in lse); that form is a few percent slower.
+ * It also serves every scale above 1.25 x 1/sqrt(D): the packed form rounds
+ * each exponent to bf16, whose error grows with the spread of the logits.
+ * Against an fp64 reference, on unit-variance q and k at the default scale
+ * both forms stay near 2.5e-3 max-abs; for logits 2x to 6x sharper the fp32
+ * form stays below 1.7e-2 while the packed one can pass 2e-2.  Callers whose
+ * logits are sharper than that through their data rather than the scale can
+ * ask for the fp32 form with exact_softmax in a chunk stream's config.
  * ------------------------------------------------------------------------ */
 int chunk_attention(const void* q, int B, int64_t n_q, int H, int D, const savgb_kv_segment* segs,
                     int n_segs, float scale, void* o, float* lse, void* stream);
@@ -284,6 +291,7 @@ typedef struct {
   int interp_chunks;   /* nonzero: keep the anchors of interpolation chunks (needs F >= 3) */
   int qkv_block;       /* nonzero: reserve room for chunk_stream_block_step */
   int host_io;         /* nonzero: reserve two device input slots for chunk_stream_step_host */
+  int exact_softmax;   /* nonzero: the steps' attention takes fp32 exponentials (see chunk_attention) */
 } chunk_stream_config;
 /* The same config under the name the problem statement's interface uses. */
 typedef chunk_stream_config chunk_stream_config_t;

@@ -65,6 +65,8 @@ constexpr int kTileKV = 128;
 // a tile whose probabilities against the running max sum to more than this
 // (2^8) moves the max; below it no probability exceeds 2^8
 constexpr float kTileSumLimit = 256.0f;
+// softmax scales above this multiple of 1/sqrt(D) take fp32 exponentials
+constexpr float kExactScaleRatio = 1.25f;
 // K / V ring depths: 128-row tiles of 32 KiB (D=128) or 16 KiB (D=64)
 #ifndef SAVGB_ATTN_KS128
 #define SAVGB_ATTN_KS128 3
@@ -698,12 +700,17 @@ int prepare_kernel(Kernel kernel, bool* done) {
 
 template <int D, int KS, int VS, bool ROPE_Q>
 int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, int n_segs,
-                float scale, void* o, float* lse, const QRope* rope, cudaStream_t stream) {
+                float scale, void* o, float* lse, const QRope* rope, cudaStream_t stream, bool exact_req) {
   using L = Layout<D, KS, VS>;
-  // the log-sum-exp output takes the instantiation with exact row sums
+  const float default_scale = 1.0f / std::sqrt((float)D);
+  if (!(scale > 0.f)) scale = default_scale;
+  // fp32 exponentials and exact row sums for the log-sum-exp output, on
+  // request, and for logits sharper than the default scale's, where the
+  // packed form's bf16-rounded exponents cost the most precision
+  const bool exact = lse != nullptr || exact_req || scale > kExactScaleRatio * default_scale;
   static bool ready[2][64] = {};
-  auto kernel = lse ? attn_fwd_kernel<D, KS, VS, ROPE_Q, true> : attn_fwd_kernel<D, KS, VS, ROPE_Q, false>;
-  int rc = prepare_kernel(kernel, ready[lse ? 1 : 0]);
+  auto kernel = exact ? attn_fwd_kernel<D, KS, VS, ROPE_Q, true> : attn_fwd_kernel<D, KS, VS, ROPE_Q, false>;
+  int rc = prepare_kernel(kernel, ready[exact ? 1 : 0]);
   if (rc) return rc;
   AttnMaps maps;
   if ((rc = make_token_map(&maps.q, q, B, n_q, H, D))) return rc;
@@ -725,7 +732,6 @@ int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, i
       maps.v[s] = maps.q;
     }
   }
-  if (!(scale > 0.f)) scale = 1.0f / std::sqrt((float)D);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.lse = lse;
   int dyn_smem = L::kDynSmem;
@@ -783,13 +789,14 @@ int validate_attention(const void* q, int B, int64_t n_q, int H, int D, const At
 }
 
 int launch_attention(const void* q, int B, int64_t n_q, int H, int D, const AttnSeg* segs,
-                     int n_segs, float scale, void* o, float* lse, cudaStream_t stream) {
+                     int n_segs, float scale, void* o, float* lse, cudaStream_t stream, bool exact_softmax) {
   int rc = check_device(nullptr);
   if (rc) return rc;
   if (D == 64)
-    return launch_impl<64, kStagesK64, kStagesV64, false>(q, B, n_q, H, segs, n_segs, scale, o, lse, nullptr, stream);
+    return launch_impl<64, kStagesK64, kStagesV64, false>(q, B, n_q, H, segs, n_segs, scale, o, lse, nullptr, stream,
+                                                          exact_softmax);
   return launch_impl<128, kStagesK128, kStagesV128, false>(q, B, n_q, H, segs, n_segs, scale, o, lse, nullptr,
-                                                          stream);
+                                                          stream, exact_softmax);
 }
 
 int validate_qrope(const QRope& r, int64_t n_q, int D) {
@@ -855,7 +862,7 @@ int rope_q_table_build(void* tab, int D, int t_lo, int n_t, int grid_h, int grid
 
 int launch_attention_qrope(const void* q, int B, int64_t n_q, int H, int D, const AttnSeg* segs,
                            int n_segs, float scale, const QRope& rope, void* o, float* lse,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, bool exact_softmax) {
   int rc = check_device(nullptr);
   if (rc) return rc;
   if (!qrope_fits(D, rope.tab ? rope.tab_t_n : rope.grid_t, rope.grid_h, rope.grid_w))
@@ -873,9 +880,11 @@ int launch_attention_qrope(const void* q, int B, int64_t n_q, int H, int D, cons
   }
   if (!rc) {
     if (D == 64)
-      rc = launch_impl<64, kStagesK64, kStagesV64, true>(q, B, n_q, H, segs, n_segs, scale, o, lse, &r, stream);
+      rc = launch_impl<64, kStagesK64, kStagesV64, true>(q, B, n_q, H, segs, n_segs, scale, o, lse, &r, stream,
+                                                         exact_softmax);
     else  // two K stages leave room for the tables (and run as fast as three)
-      rc = launch_impl<128, 2, kStagesV128, true>(q, B, n_q, H, segs, n_segs, scale, o, lse, &r, stream);
+      rc = launch_impl<128, 2, kStagesV128, true>(q, B, n_q, H, segs, n_segs, scale, o, lse, &r, stream,
+                                                  exact_softmax);
   }
   if (tmp) {
     const cudaError_t e = cudaFreeAsync(tmp, stream);

@@ -300,10 +300,10 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
     r.tab_t_lo = 0;
     r.tab_t_n = c.F;
     rc = launch_attention_qrope(q, c.B, s->n_tok, c.H, c.D, segs, 3, c.softmax_scale, r, s->o, nullptr,
-                                s->stream);
+                                s->stream, c.exact_softmax != 0);
   } else {
     rc = launch_attention(s->q_rot, c.B, s->n_tok, c.H, c.D, segs, 3, c.softmax_scale, s->o, nullptr,
-                          s->stream);
+                          s->stream, c.exact_softmax != 0);
   }
   if (rc) return rc;
   if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[2], s->stream));
@@ -441,9 +441,11 @@ int chunk_stream_istep(chunk_stream_t* s, const void* q, const void* k, const vo
     r.tab = s->qrope_tab;
     r.tab_t_lo = 0;
     r.tab_t_n = c.F;
-    rc = launch_attention_qrope(q, c.B, n_int, c.H, c.D, segs, 3, c.softmax_scale, r, s->o, nullptr, s->stream);
+    rc = launch_attention_qrope(q, c.B, n_int, c.H, c.D, segs, 3, c.softmax_scale, r, s->o, nullptr, s->stream,
+                                c.exact_softmax != 0);
   } else {
-    rc = launch_attention(s->q_rot, c.B, n_int, c.H, c.D, segs, 3, c.softmax_scale, s->o, nullptr, s->stream);
+    rc = launch_attention(s->q_rot, c.B, n_int, c.H, c.D, segs, 3, c.softmax_scale, s->o, nullptr, s->stream,
+                          c.exact_softmax != 0);
   }
   if (rc) return rc;
   if ((rc = wait_readback(s))) return rc;
@@ -515,7 +517,7 @@ int chunk_stream_block_step(chunk_stream_t* s, const void* w_qkv, const void* w_
       {s->k_rot, s->v_buf, s->n_tok},
   };
   if ((rc = launch_attention(s->q_rot, c.B, s->n_tok, c.H, c.D, segs, 3, c.softmax_scale, s->o, nullptr,
-                             s->stream)))
+                             s->stream, c.exact_softmax != 0)))
     return rc;
   if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[2], s->stream));
   if ((rc = launch_out_proj_euler(s->o, w_o, bias, x, M, (int)s->hid, (int)s->hid, dt, nullptr, s->stream)))

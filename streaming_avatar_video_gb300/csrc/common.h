@@ -110,8 +110,11 @@ struct AttnSeg {
 };
 int validate_attention(const void* q, int B, int64_t n_q, int H, int D, const AttnSeg* segs,
                        int n_segs, const void* o);
+// exact_softmax selects the instantiation with fp32 exponentials and exact row
+// sums; so do a log-sum-exp output and a softmax scale above 1.25 x 1/sqrt(D).
 int launch_attention(const void* q, int B, int64_t n_q, int H, int D, const AttnSeg* segs,
-                     int n_segs, float scale, void* o, float* lse, cudaStream_t stream);
+                     int n_segs, float scale, void* o, float* lse, cudaStream_t stream,
+                     bool exact_softmax = false);
 // Grid of the (unrotated) queries for attention with RoPE of Q fused in.
 struct QRope {
   int grid_t, grid_h, grid_w, t0;
@@ -131,7 +134,7 @@ int rope_q_table_build(void* tab, int D, int t_lo, int n_t, int grid_h, int grid
 bool qrope_fits(int D, int grid_t, int grid_h, int grid_w);
 int launch_attention_qrope(const void* q, int B, int64_t n_q, int H, int D, const AttnSeg* segs,
                            int n_segs, float scale, const QRope& rope, void* o, float* lse,
-                           cudaStream_t stream);
+                           cudaStream_t stream, bool exact_softmax = false);
 
 // QKV projection with the RoPE of q and k in the GEMM epilogue.
 struct QkvArgs {

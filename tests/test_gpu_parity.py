@@ -136,6 +136,22 @@ def test_attention_lazy_rescale_path(S):
     attn_case(S, 1, 2, 128, 256, [512, 0, 768], 13, q_scale=8.0)
 
 
+def test_attention_sharp_scale_takes_fp32_exponentials(S):
+    """A softmax scale above 1.25 x 1/sqrt(D) selects the kernel with fp32
+    exponentials (the one the log-sum-exp output selects): bit-identical
+    outputs with and without lse there, different ones at the default scale
+    (where the packed bf16x2 exponentials run)."""
+    B, H, D, n_q = 2, 3, 128, 300
+    q = bf16((B, n_q, H, D), 71, I.KIND_Q).cuda()
+    segs = [(bf16((B, n, H, D), 71, I.KIND_K, chunk=j).cuda(), bf16((B, n, H, D), 71, I.KIND_V, chunk=j).cuda())
+            for j, n in enumerate([100, 0, 300])]
+    lse = torch.empty((B, H, n_q), dtype=torch.float32, device="cuda")
+    sharp = 2.0 / math.sqrt(D)
+    assert torch.equal(S.chunk_attention(q, segs, scale=sharp), S.chunk_attention(q, segs, scale=sharp, lse=lse))
+    assert not torch.equal(S.chunk_attention(q, segs), S.chunk_attention(q, segs, lse=lse))
+    S.savgb_device_check()
+
+
 @pytest.mark.parametrize("name", ["base", "sr"])
 def test_attention_full_size_sampled_rows(S, name):
     w = I.WORKLOADS[name]
@@ -359,6 +375,37 @@ def test_stream_host_io_matches_device_steps(S):
         plain.step_host(st.q, st.k, st.v, wo, x, 0.1, False)
     assert e.value.status == -7
     plain.close()
+
+
+def test_stream_exact_softmax(S):
+    """A stream created with exact_softmax runs its attention with fp32
+    exponentials: its steps match the oracle, and differ (slightly) from the
+    packed form's."""
+    w = I.WORKLOADS["small"]
+    seed = 19
+    rk, rv = I.reference_kv(w, seed)
+    wo = I.out_proj_weight(w, seed).cuda()
+    dts = S.flow_time_grid(w.steps, w.shift)
+    xs = {}
+    for exact in (False, True):
+        cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                           w.rope_base, exact_softmax=exact)
+        cs.set_reference(rk.cuda(), rv.cuda())
+        x = I.state_x(w, seed).cuda()
+        for s_, dt in enumerate(dts):
+            st = I.step_inputs(w, seed, 0, s_)
+            cs.step(st.q.cuda(), st.k.cuda(), st.v.cuda(), wo, x, dt, s_ == len(dts) - 1)
+        cs.sync()
+        xs[exact] = x.cpu()
+        cs.close()
+    f = lambda t: t.double().numpy()  # noqa: E731
+    want, _ = O.run_stream(w, f(rk), f(rv), f(wo.cpu()), lambda c: f(I.state_x(w, seed)),
+                           lambda c, s_: tuple(f(t) for t in (I.step_inputs(w, seed, c, s_).q,
+                                                              I.step_inputs(w, seed, c, s_).k,
+                                                              I.step_inputs(w, seed, c, s_).v)),
+                           O.time_grid(w.steps, w.shift), chunks=1)
+    assert_close(f64(xs[True]), want[0], what="exact-softmax stream chunk 0 x")
+    assert not torch.equal(xs[True], xs[False])
 
 
 def test_stream_export_import_resume(S):
