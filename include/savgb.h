@@ -290,7 +290,7 @@ typedef struct {
   float softmax_scale; /* <= 0 selects 1/sqrt(D) */
   int interp_chunks;   /* nonzero: keep the anchors of interpolation chunks (needs F >= 3) */
   int qkv_block;       /* nonzero: reserve room for chunk_stream_block_step */
-  int host_io;         /* nonzero: reserve two device input slots for chunk_stream_step_host */
+  int host_io;         /* 0, or the device input slots of chunk_stream_step_host: 2 to 4 (1 means 2) */
   int exact_softmax;   /* nonzero: the steps' attention takes fp32 exponentials (see chunk_attention) */
 } chunk_stream_config;
 /* The same config under the name the problem statement's interface uses. */
@@ -322,7 +322,9 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
  * the updated state read back to host memory: the whole step through one
  * call, host to host, as a serving loop that receives each step's q, k, v
  * from the host and hands the state back would run it.  Needs host_io in the
- * config (the arena then holds two device input slots, 2 x 3 x B*N*H*D bf16).
+ * config: the arena then holds host_io (at least 2, at most 4) device input
+ * slots of 3 x B*N*H*D bf16; more slots let the uploads run further ahead of
+ * the compute and ride out a slow spell of the host link.
  *   q_host, k_host, v_host  bf16 [B][N][H][D] in host memory; page-locked
  *       (cudaHostAlloc / cudaHostRegister) for the upload to overlap compute,
  *       pageable memory also works but its copy blocks the calling thread.
@@ -330,8 +332,8 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
  *   x_host  optional fp32 [B*N][H*D] host buffer (page-locked to overlap):
  *       receives x after this step.
  * The call enqueues and returns.  The upload goes into input slot (call
- * count mod 2) on an internal copy stream once the step that last used that
- * slot has finished with it; the step runs on the handle's stream once its
+ * count mod slots) on an internal copy stream once the step that last used
+ * that slot has finished with it; the step runs on the handle's stream once its
  * upload has landed; the read-back of x runs on a second internal copy stream
  * after the step, straight from x (no staging copy): the W_o update of the
  * next step of this stream waits for it.  So consecutive calls overlap the

@@ -33,6 +33,9 @@
 
 using namespace savgb;
 
+// input slots of chunk_stream_step_host: host_io in the config (1 means 2)
+constexpr int kMaxInSlots = 4;
+
 struct chunk_stream {
   chunk_stream_config cfg;
   cudaStream_t stream;
@@ -67,12 +70,13 @@ struct chunk_stream {
   int64_t chunk_index;
   cudaEvent_t step_events[4];  // recorded by the next step, then cleared
   bool have_events;
-  // host_io: two device input slots [q | k | v] filled from host memory on
-  // copy_in, the state read back on copy_out (chunk_stream_step_host)
-  __nv_bfloat16_raw* in_slot[2][3];
+  // host_io: n_slots device input slots [q | k | v] filled from host memory
+  // on copy_in, the state read back on copy_out (chunk_stream_step_host)
+  int n_slots;
+  __nv_bfloat16_raw* in_slot[kMaxInSlots][3];
   cudaStream_t copy_in, copy_out;
-  cudaEvent_t ev_loaded[2], ev_freed[2], ev_step_done, ev_out_done;
-  bool slot_used[2];
+  cudaEvent_t ev_loaded[kMaxInSlots], ev_freed[kMaxInSlots], ev_step_done, ev_out_done;
+  bool slot_used[kMaxInSlots];
   int next_slot;
   bool out_pending;  // a read-back of x is in flight: the next W_o update waits for it
   bool host_used;    // copies were enqueued since the last join / sync
@@ -108,6 +112,9 @@ int validate_config(const chunk_stream_config* c) {
   if (hid % 16) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: H*D must be a multiple of 16");
   if (c->interp_chunks && c->F < 3)
     return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: interpolation chunks need F >= 3");
+  if (c->host_io < 0 || c->host_io > kMaxInSlots)
+    return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream: host_io must be 0 (off) or 1 to %d input slots (1 means 2)",
+                kMaxInSlots);
   return SAVGB_OK;
 }
 
@@ -115,7 +122,7 @@ int validate_config(const chunk_stream_config* c) {
 int host_io_init(chunk_stream* s) {
   SAVGB_CUDA(cudaStreamCreateWithFlags(&s->copy_in, cudaStreamNonBlocking));
   SAVGB_CUDA(cudaStreamCreateWithFlags(&s->copy_out, cudaStreamNonBlocking));
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < s->n_slots; ++i) {
     SAVGB_CUDA(cudaEventCreateWithFlags(&s->ev_loaded[i], cudaEventDisableTiming));
     SAVGB_CUDA(cudaEventCreateWithFlags(&s->ev_freed[i], cudaEventDisableTiming));
     s->slot_used[i] = false;
@@ -131,7 +138,7 @@ int host_io_init(chunk_stream* s) {
 void host_io_release(chunk_stream* s) {
   if (s->copy_in) cudaStreamSynchronize(s->copy_in);
   if (s->copy_out) cudaStreamSynchronize(s->copy_out);
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < kMaxInSlots; ++i) {
     if (s->ev_loaded[i]) cudaEventDestroy(s->ev_loaded[i]);
     if (s->ev_freed[i]) cudaEventDestroy(s->ev_freed[i]);
   }
@@ -192,7 +199,8 @@ int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stre
   const int64_t vbuf_b = c.qkv_block ? tok_b : 0;
   s->qrope = qrope_fits(c.D, c.F, c.grid_h, c.grid_w);
   const int64_t tab_b = s->qrope ? round_up(rope_q_table_bytes(c.D, c.F, c.grid_h, c.grid_w), 256) : 0;
-  const int64_t in_b = c.host_io ? 6 * tok_b : 0;
+  s->n_slots = c.host_io ? (c.host_io < 2 ? 2 : c.host_io) : 0;
+  const int64_t in_b = 3 * s->n_slots * tok_b;
   s->arena_bytes = 2 * ref_b + 4 * bnd_b + 3 * tok_b + 4 * anc_b + vbuf_b + tab_b + in_b;
   const char* cap = getenv("SAVGB_ARENA_LIMIT_BYTES");
   if (cap && *cap) {
@@ -222,8 +230,8 @@ int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stre
   }
   s->v_buf = vbuf_b ? take(vbuf_b) : nullptr;
   s->qrope_tab = tab_b ? static_cast<void*>(take(tab_b)) : nullptr;
-  for (int i = 0; i < 2; ++i)
-    for (int t = 0; t < 3; ++t) s->in_slot[i][t] = in_b ? take(tok_b) : nullptr;
+  for (int i = 0; i < s->n_slots; ++i)
+    for (int t = 0; t < 3; ++t) s->in_slot[i][t] = take(tok_b);
   if (s->qrope &&
       (rc = rope_q_table_build(s->qrope_tab, c.D, 0, c.F, c.grid_h, c.grid_w, c.rope_base, s->stream))) {
     cudaFree(s->arena);
@@ -377,7 +385,7 @@ int chunk_stream_step_host(chunk_stream_t* s, const void* q_host, const void* k_
   if (rc) return rc;
   SAVGB_CUDA(cudaEventRecord(s->ev_freed[slot], s->stream));
   s->slot_used[slot] = true;
-  s->next_slot = slot ^ 1;
+  s->next_slot = (slot + 1) % s->n_slots;
   if (x_host) {
     // read x back straight from the state; the next W_o update waits for it
     SAVGB_CUDA(cudaEventRecord(s->ev_step_done, s->stream));

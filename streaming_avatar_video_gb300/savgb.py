@@ -397,10 +397,10 @@ class ChunkStream:
     def __init__(self, B: int, H: int, D: int, F: int, grid_h: int, grid_w: int, ref_frames: int = 1,
                  boundary_frames: int = 0, ref_t: int = -1, rope_base: float = 10000.0,
                  softmax_scale: float = 0.0, stream=None, interp_chunks: bool = False, qkv_block: bool = False,
-                 host_io: bool = False, exact_softmax: bool = False):
+                 host_io: int = 0, exact_softmax: bool = False):
         self.cfg = ChunkStreamConfig(B, H, D, F, grid_h, grid_w, ref_frames, boundary_frames, ref_t,
                                      float(rope_base), float(softmax_scale), int(bool(interp_chunks)),
-                                     int(bool(qkv_block)), int(bool(host_io)), int(bool(exact_softmax)))
+                                     int(bool(qkv_block)), int(host_io), int(bool(exact_softmax)))
         self.stream = _stream(stream)
         h = ctypes.c_void_p()
         _check(lib().chunk_stream_create(ctypes.byref(self.cfg), self.stream, ctypes.byref(h)))

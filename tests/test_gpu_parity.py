@@ -306,7 +306,8 @@ def test_stream_two_sessions_ragged_blocks(S):
         assert torch.equal(xs[c], xs2[c]), f"chunk {c}: rerun differs"
 
 
-def test_stream_host_io_matches_device_steps(S):
+@pytest.mark.parametrize("slots", [1, 3], ids=["two-slots", "three-slots"])
+def test_stream_host_io_matches_device_steps(S, slots):
     """chunk_stream_step_host (q, k, v from host memory, x read back every
     step) against chunk_stream_step on the same inputs: every step's read-back
     bit-identical to the device path's x after that step, the final state
@@ -325,7 +326,7 @@ def test_stream_host_io_matches_device_steps(S):
 
     def make(host_io):
         cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
-                           w.rope_base, host_io=host_io)
+                           w.rope_base, host_io=int(host_io))
         cs.set_reference(rk.cuda(), rv.cuda())
         return cs
 
@@ -341,7 +342,7 @@ def test_stream_host_io_matches_device_steps(S):
     ref.sync()
     ref.close()
 
-    hs = make(True)
+    hs = make(slots)
     x = I.state_x(w, seed).cuda()
     back = {cs_: torch.empty((w.B * w.n_q, w.hid), dtype=torch.float32).pin_memory() for cs_ in plan}
     # every host input stays alive until the sync below: the uploads read them asynchronously
