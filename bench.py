@@ -53,8 +53,8 @@ METRIC = "chunk-attention TFLOP/s (% of bf16 tensor peak); latent frames/s per d
 # change of them reports null.
 ATTN_TRAFFIC = {
     # profiles/chunk_attention_base.md and profiles/chunk_attention_sr.md: the fused-RoPE kernel the stream
-    # runs; base 290.046 MB read + 61.018 MB written, SR 1580.464 MB read + 296.106 MB written
-    "7f8e8219ad2d90b40116e1d7d80ea029c9e623efa9546b17baaccf0bc555c84d": {"base": 351064832, "sr": 1876570368},
+    # runs; base 291.162 MB read + 60.773 MB written, SR 1579.716 MB read + 295.467 MB written
+    "64028471a636424dcfff760e87c6e33f35c6d0dc782a1338dab91e7a1d3112dd": {"base": 351934976, "sr": 1875183104},
 }
 
 
