@@ -862,15 +862,70 @@ def test_qkv_rope_project_parity(S, B, H, D, gt, gh, gw, t0):
     assert_close(f64(v), ov, what="v")
 
 
-def _block_workload():
-    return I.Workload("blk", B=1, H=4, D=64, F=3, grid_h=8, grid_w=8, ref_frames=1, boundary_frames=1, steps=2,
-                      shift=1.0)
+def test_stream_host_io_two_sessions_four_slots(S):
+    """chunk_stream_step_host with the deepest input ring (4 device slots) on
+    two sessions of 1100 queries (W_o tiles straddle the sessions, ragged last
+    attention blocks), three chunks: every step's read-back bit-identical to
+    chunk_stream_step's x after that step, each chunk's final x against the
+    oracle.  Each chunk's x is a new device tensor; all of them stay alive
+    until the sync, since the read-backs run after the call returns."""
+    w = I.Workload("straddle", B=2, H=4, D=128, F=5, grid_h=10, grid_w=22, ref_frames=1,
+                   boundary_frames=1, steps=3, shift=1.0)
+    seed, chunks = 4, 3
+    dts = S.flow_time_grid(w.steps, w.shift)
+    rk, rv = I.reference_kv(w, seed)
+    wo = I.out_proj_weight(w, seed).cuda()
+    plan = [(c, s_) for c in range(chunks) for s_ in range(w.steps)]
+    ins = {p: I.step_inputs(w, seed, *p) for p in plan}
+    x0 = [torch.from_numpy(I.normal_f32((w.B * w.n_q, w.hid), 1.0, seed, I.KIND_X, c)) for c in range(chunks)]
+
+    def run(host_io):
+        cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                           w.rope_base, host_io=host_io)
+        cs.set_reference(rk.cuda(), rv.cuda())
+        host_in = {p: tuple(t.pin_memory() for t in (ins[p].q, ins[p].k, ins[p].v)) for p in plan}
+        out = {p: torch.empty((w.B * w.n_q, w.hid), dtype=torch.float32).pin_memory() for p in plan}
+        xs = []
+        for c in range(chunks):
+            xs.append(x0[c].cuda())
+            for s_ in range(w.steps):
+                p, last = (c, s_), s_ == w.steps - 1
+                if host_io:
+                    cs.step_host(*host_in[p], wo, xs[c], dts[s_], last, x_host=out[p])
+                else:
+                    cs.step(*(t.cuda() for t in host_in[p]), wo, xs[c], dts[s_], last)
+                    out[p].copy_(xs[c])
+                if last:
+                    cs.end_chunk()
+        cs.sync()
+        torch.cuda.synchronize()
+        cs.close()
+        return out, [x.cpu() for x in xs]
+
+    want, _ = run(0)
+    got, finals = run(4)
+    for p in plan:
+        assert torch.equal(got[p], want[p]), f"read-back after chunk {p[0]} step {p[1]}"
+    oracle_x, _ = run_stream_oracle(w, seed, chunks)
+    for c in range(chunks):
+        assert torch.equal(finals[c], want[(c, w.steps - 1)])
+        assert_close(f64(finals[c]), oracle_x[c], what=f"host-io two-session chunk {c} x")
 
 
-def test_stream_block_steps(S):
+_BLOCK_WORKLOADS = {
+    "d64": I.Workload("blk", B=1, H=4, D=64, F=3, grid_h=8, grid_w=8, ref_frames=1, boundary_frames=1, steps=2,
+                      shift=1.0),
+    # two sessions of 189 tokens: projection and W_o tiles straddle the sessions, ragged attention blocks
+    "d128-two-sessions": I.Workload("blk2", B=2, H=4, D=128, F=3, grid_h=7, grid_w=9, ref_frames=1,
+                                    boundary_frames=1, steps=2, shift=1.0),
+}
+
+
+@pytest.mark.parametrize("wname", list(_BLOCK_WORKLOADS))
+def test_stream_block_steps(S, wname):
     """Two chunks x two steps through one DiT attention block (q, k, v
     projected from x): every chunk's x against the oracle."""
-    w = _block_workload()
+    w = _BLOCK_WORKLOADS[wname]
     seed = 12
     rk, rv = I.reference_kv(w, seed)
     wqkv, wo = I.qkv_weight(w, seed), I.out_proj_weight(w, seed)
