@@ -167,3 +167,25 @@ def test_qrope_table_calls_validate(S):
                                               None, None) == -1
     assert L.chunk_attention_qrope_with_table(c_vp(16), 1, 33, 2, 128, 2, 4, 4, 0, c_vp(64), segs, 1, 0.0,
                                               c_vp(16), None, None) == -1  # n_q != grid
+
+
+def test_c_abi_from_plain_c(S, tmp_path):
+    """The header compiles as C99 and as C++17 with every warning an error, and
+    a plain C program linked against libsavgb.so runs the host-only calls as
+    the header states (tests/abi_c_check.c)."""
+    import shutil
+    import subprocess
+    cc, cxx = shutil.which("gcc") or shutil.which("cc"), shutil.which("g++") or shutil.which("c++")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lib_dir = os.path.dirname(S.LIB_PATH)
+    exe = str(tmp_path / "abi_c_check")
+    flags = ["-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include")]
+    subprocess.run([cc, "-std=c99", "-pedantic", *flags, os.path.join(ROOT, "tests", "abi_c_check.c"),
+                    "-L", lib_dir, "-lsavgb", f"-Wl,-rpath,{lib_dir}", "-lm", "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr
+    if cxx is not None:
+        src = tmp_path / "header.cpp"
+        src.write_text('#include "savgb.h"\nint main() { return savgb_version() > 0 ? 0 : 1; }\n')
+        subprocess.run([cxx, "-std=c++17", *flags, "-fsyntax-only", str(src)], check=True)
