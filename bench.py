@@ -53,8 +53,8 @@ METRIC = "chunk-attention TFLOP/s (% of bf16 tensor peak); latent frames/s per d
 # change of them reports null.
 ATTN_TRAFFIC = {
     # profiles/chunk_attention_base.md and profiles/chunk_attention_sr.md: the fused-RoPE kernel the stream
-    # runs; base 291.162 MB read + 60.773 MB written, SR 1579.716 MB read + 295.467 MB written
-    "64028471a636424dcfff760e87c6e33f35c6d0dc782a1338dab91e7a1d3112dd": {"base": 351934976, "sr": 1875183104},
+    # runs; base 292.767 MB read + 61.134 MB written, SR 1738.437 MB read + 295.282 MB written
+    "a6b132ae6f7e95df8e19bbec15f02d80a3175144f42917a46612aa6af81fefb5": {"base": 353901056, "sr": 2033718784},
 }
 
 
@@ -283,9 +283,10 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
     cs.step(q, k, v, wo, x, dts[0], True)
     cs.end_chunk()
 
-    state = {"i": 0, "launches": 0}
+    state = {"i": 0}
 
     def one_step(events=None):
+        # 3 launches (RoPE of k, attention, W_o + Euler), and the boundary's RoPE after a chunk's last step
         i = state["i"]
         s = i % w.steps
         q, k, v = dsets[i & 1]
@@ -293,7 +294,6 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
         if events is not None:
             cs.set_step_events(events)
         cs.step(q, k, v, wo, x, dts[s], last)
-        state["launches"] += 3 + (1 if last and w.boundary_frames > 0 else 0)
         if last:
             cs.end_chunk()
         state["i"] = i + 1
@@ -307,7 +307,7 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     with ClockSampler(local) as clk:
-        state["launches"] = 0
+        l0 = S.savgb_kernel_launches()
         barrier(world)
         torch.cuda.synchronize()
         start.record(stream)
@@ -316,7 +316,7 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
         end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-    launches = state["launches"]
+    launches = S.savgb_kernel_launches() - l0  # the library's own count of the kernels it enqueued
     clocks = clk.summary()
 
     # end-to-end through the public API with host buffers, right after the
@@ -650,14 +650,10 @@ def run_long(args, w: I.Workload, world: int, rank: int, local: int):
     cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
                        w.rope_base)
     cs.set_reference(rk.to(dev), rv.to(dev))
-    launches = [0]
-
     def chunk(i0):
         for s in range(w.steps):
             q, k, v = sets[(i0 + s) & 1]
             cs.step(q, k, v, wo, x, dts[s], s == w.steps - 1)
-            launches[0] += 3
-        launches[0] += 1 if w.boundary_frames else 0
         cs.end_chunk()
 
     for c in range(max(1, args.warmup // w.steps + 1)):  # warm-up chunks
@@ -666,7 +662,7 @@ def run_long(args, w: I.Workload, world: int, rank: int, local: int):
     n = args.chunks
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
     free = []
-    launches[0] = 0
+    l0 = S.savgb_kernel_launches()
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
@@ -677,6 +673,7 @@ def run_long(args, w: I.Workload, world: int, rank: int, local: int):
             if c % 8 == 7:
                 free.append(torch.cuda.mem_get_info(dev)[0])  # synchronising query, outside the events
         torch.cuda.synchronize()
+    launches = S.savgb_kernel_launches() - l0
     barrier(world)
     cs.sync()
     per_chunk = sorted(ev[c].elapsed_time(ev[c + 1]) for c in range(n))
@@ -702,7 +699,7 @@ def run_long(args, w: I.Workload, world: int, rank: int, local: int):
                              "min": round(per_chunk[0], 3), "max": round(per_chunk[-1], 3)},
         "memory": {"arena_bytes": info["arena_bytes"], "free_bytes_samples": len(free),
                    "free_bytes_constant": len(set(free)) <= 1},
-        "gpu_launches": launches[0],
+        "gpu_launches": launches,
         "clocks": clk.summary(),
         "e2e": None, "cpu_baseline": None, "roofline": None,
     }
@@ -745,11 +742,13 @@ def run_interp(args, w: I.Workload, world: int, rank: int, local: int):
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        l0 = S.savgb_kernel_launches()
         a.record(stream)
         for i in range(args.steps):
             cs.istep(*isets[i & 1], wo, xi, dts[i % w.steps])
         b.record(stream)
         torch.cuda.synchronize()
+        launches = S.savgb_kernel_launches() - l0
     barrier(world)
     cs.sync()
     cs.close()
@@ -768,7 +767,7 @@ def run_interp(args, w: I.Workload, world: int, rank: int, local: int):
                    "parallelism": f"replicas x{world}", "global_batch": world * w.B,
                    "l2": "two alternating input sets larger than L2"},
         "latent_frames_per_s": round(whole_job_rate(world, w.B * (w.F - 2), ms), 1),
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": launches,
         "clocks": clk.summary(),
         "e2e": None, "cpu_baseline": None, "roofline": None,
     }
@@ -797,7 +796,7 @@ def run_block(args, w: I.Workload, world: int, rank: int, local: int):
     cs.set_reference(rk.to(dev), rv.to(dev))
     cs.block_step(wqkv, wo, x, dts[0], True)
     cs.end_chunk()
-    state = {"i": 0, "launches": 0}
+    state = {"i": 0}
 
     def one(events=None):
         i = state["i"]
@@ -806,7 +805,6 @@ def run_block(args, w: I.Workload, world: int, rank: int, local: int):
         if events is not None:
             cs.set_step_events(events)
         cs.block_step(wqkv, wo, x, dts[s_], last)
-        state["launches"] += 4 + (1 if last and w.boundary_frames else 0)
         if last:
             cs.end_chunk()
         state["i"] = i + 1
@@ -819,7 +817,7 @@ def run_block(args, w: I.Workload, world: int, rank: int, local: int):
     ai, bi = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         # the steps alone, then a second region with per-stage events
-        state["launches"] = 0
+        l0 = S.savgb_kernel_launches()
         barrier(world)
         torch.cuda.synchronize()
         a.record(stream)
@@ -828,7 +826,7 @@ def run_block(args, w: I.Workload, world: int, rank: int, local: int):
         b.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        launches = state["launches"]
+        launches = S.savgb_kernel_launches() - l0
         barrier(world)
         torch.cuda.synchronize()
         ai.record(stream)

@@ -59,6 +59,11 @@ const char* savgb_status_string(int status);
 const char* savgb_last_error(void);
 /* Library version, major*10000 + minor*100 + patch. */
 int savgb_version(void);
+/* Kernels this process has enqueued through the library since it was loaded:
+ * every launch the CUDA runtime accepted, on any device or stream, counted on
+ * the host.  No device work; the difference of two readings counts the
+ * launches of the calls between them. */
+uint64_t savgb_kernel_launches(void);
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns SAVGB_ERR_TIMEOUT (with the kernel and wait that gave up in

@@ -763,6 +763,7 @@ int launch_impl(const void* q, int B, int64_t n_q, int H, const AttnSeg* segs, i
   dim3 grid((unsigned)((n_q + kBlockQ - 1) / kBlockQ), (unsigned)H, (unsigned)B);
   SAVGB_CUDA(launch_dependent(kernel, grid, dim3(kThreads), dyn_smem, stream, maps, p));
   SAVGB_CUDA(cudaGetLastError());
+  note_launch();
   return SAVGB_OK;
 }
 
@@ -857,6 +858,7 @@ int rope_q_table_build(void* tab, int D, int t_lo, int n_t, int grid_h, int grid
     rope_q_table_kernel<128><<<blocks, threads, 0, stream>>>(static_cast<float2*>(tab), t_lo, n_t, grid_h, grid_w,
                                                               log2_base);
   SAVGB_CUDA(cudaGetLastError());
+  note_launch();
   return SAVGB_OK;
 }
 

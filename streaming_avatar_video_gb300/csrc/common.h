@@ -14,6 +14,9 @@ namespace savgb {
 int fail(int code, const char* fmt, ...);
 // Clears the thread-local message (called at the start of every entry point).
 void clear_error();
+// Counts one kernel the library enqueued (after the runtime accepted the launch);
+// read through savgb_kernel_launches().
+void note_launch();
 
 // A named NVTX range around one C-ABI call, for profilers (ncu --nvtx
 // filters kernels by it); with no tool attached it costs a few nanoseconds.

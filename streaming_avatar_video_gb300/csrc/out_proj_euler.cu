@@ -351,6 +351,7 @@ int launch_bn(const void* o, const void* w, const float* bias, float* x, int64_t
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + gemm::kBM - 1) / gemm::kBM));
   SAVGB_CUDA(launch_dependent(wo_euler_kernel<BN>, grid, dim3(gemm::kThreads), L::kDynSmem, stream, ma, mb, mx, p));
   SAVGB_CUDA(cudaGetLastError());
+  note_launch();
   return SAVGB_OK;
 }
 
@@ -412,6 +413,7 @@ int launch_pair(const void* o, const void* w, const float* bias, float* x, int64
   SAVGB_CUDA(launch_dependent(wo_pair_kernel, dim3((unsigned)(2 * clusters)), dim3(gemm_pair::kThreads),
                               pair::L::kDynSmem, stream, ma, mb, mx, p, n_tiles_n, n_tiles));
   SAVGB_CUDA(cudaGetLastError());
+  note_launch();
   return SAVGB_OK;
 }
 

@@ -306,6 +306,7 @@ int launch_qkv_bn(const QkvArgs& a, cudaStream_t stream) {
   dim3 grid((unsigned)((p.N3 + BN - 1) / BN), (unsigned)((p.M + gemm::kBM - 1) / gemm::kBM));
   qkv_rope_kernel<BN><<<grid, gemm::kThreads, (int)(L::kDynSmem + tab), stream>>>(ma, mb, p);
   SAVGB_CUDA(cudaGetLastError());
+  note_launch();
   return SAVGB_OK;
 }
 
@@ -336,6 +337,7 @@ int launch_qkv_pair(const QkvArgs& a, int sms, cudaStream_t stream) {
   SAVGB_CUDA(launch_dependent(qkv_pair_kernel, dim3((unsigned)(2 * clusters)), dim3(gemm_pair::kThreads), smem,
                               stream, ma, mb, p, n_tiles_n, n_tiles));
   SAVGB_CUDA(cudaGetLastError());
+  note_launch();
   return SAVGB_OK;
 }
 
@@ -384,6 +386,7 @@ int launch_to_bf16(const float* x, void* y, int64_t n, cudaStream_t stream) {
   to_bf16_kernel<<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, stream>>>(reinterpret_cast<const float4*>(x),
                                                                            static_cast<uint4*>(y), n8);
   SAVGB_CUDA(cudaGetLastError());
+  note_launch();
   return SAVGB_OK;
 }
 

@@ -268,6 +268,7 @@ static int launch_rope_multi(const RopeArgs* args, int n, cudaStream_t stream) {
   dim3 grid((unsigned)(groups < per ? groups : per), (unsigned)a.B, (unsigned)n);
   SAVGB_CUDA(launch_dependent(kern, grid, dim3(kRopeThreads), smem, stream, k));
   SAVGB_CUDA(cudaGetLastError());
+  note_launch();
   return SAVGB_OK;
 }
 

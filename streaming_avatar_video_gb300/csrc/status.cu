@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <cmath>
+#include <atomic>
 #include <mutex>
 
 #include "common.h"
@@ -24,9 +25,12 @@ constexpr int kMaxDevices = 64;
 DeviceErrorWord* g_err_ptr[kMaxDevices] = {nullptr};
 int g_sm_count[kMaxDevices] = {0};
 std::mutex g_mu;
+std::atomic<uint64_t> g_launches{0};
 }  // namespace
 
 void clear_error() { g_msg[0] = 0; }
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
 std::mutex g_fault_mu;
@@ -147,6 +151,8 @@ using namespace savgb;
 
 extern "C" {
 
+uint64_t savgb_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
 const char* savgb_status_string(int status) {
   switch (status) {
     case SAVGB_OK: return "SAVGB_OK";
@@ -195,6 +201,7 @@ int savgb_watchdog_selftest(uint64_t limit_ns, void* stream) {
   if ((rc = error_word(&err))) return rc;
   watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, limit_ns);
   SAVGB_CUDA(cudaGetLastError());
+  note_launch();
   return SAVGB_OK;
 }
 

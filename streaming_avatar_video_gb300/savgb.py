@@ -26,7 +26,7 @@ STATUS = {
 
 # every entry point of include/savgb.h
 EXPORTS = (
-    "savgb_status_string", "savgb_last_error", "savgb_version", "savgb_device_check",
+    "savgb_status_string", "savgb_last_error", "savgb_version", "savgb_kernel_launches", "savgb_device_check",
     "savgb_watchdog_selftest", "savgb_arm_wait_fault", "rope3d_apply", "chunk_attention", "out_proj_euler_step",
     "flow_time_grid", "chunk_stream_create", "chunk_stream_set_reference", "chunk_stream_step",
     "chunk_stream_end_chunk", "chunk_stream_set_step_events", "chunk_stream_sync", "chunk_stream_info", "chunk_stream_export_state",
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
         "savgb_status_string": (ctypes.c_char_p, [c_int]),
         "savgb_last_error": (ctypes.c_char_p, []),
         "savgb_version": (c_int, []),
+        "savgb_kernel_launches": (ctypes.c_uint64, []),
         "savgb_device_check": (c_int, [c_vp]),
         "savgb_watchdog_selftest": (c_int, [ctypes.c_uint64, c_vp]),
         "savgb_arm_wait_fault": (c_int, [c_int, c_int, ctypes.c_uint64]),
@@ -167,6 +168,12 @@ def _need_host(t: torch.Tensor, name: str, dtype: torch.dtype, numel: int) -> No
 
 def savgb_version() -> int:
     return lib().savgb_version()
+
+
+def savgb_kernel_launches() -> int:
+    """Kernels this process has enqueued through the library so far (a host
+    counter); the difference of two readings counts the calls' launches."""
+    return int(lib().savgb_kernel_launches())
 
 
 def savgb_device_check(stream=None) -> None:

@@ -487,6 +487,54 @@ def test_stream_arena_limit(S, monkeypatch):
     assert e.value.status == -4
 
 
+def test_kernel_launch_counter(S):
+    """savgb_kernel_launches counts the kernels each call enqueues: one per
+    stand-alone kernel call; three per stream step (RoPE of k, attention with
+    the RoPE of q inside, W_o + Euler), and one more, the boundary's RoPE, at a
+    chunk's end; none for a call refused on the host.  The bench reports the
+    same counter over its timed regions."""
+    w = I.WORKLOADS["small"]
+    seed = 14
+    n = S.savgb_kernel_launches
+
+    def delta(fn):
+        before = n()
+        fn()
+        torch.cuda.synchronize()
+        return n() - before
+
+    q = bf16((1, 300, 2, 128), seed, I.KIND_Q).cuda()
+    kv = (bf16((1, 200, 2, 128), seed, I.KIND_K).cuda(), bf16((1, 200, 2, 128), seed, I.KIND_V).cuda())
+    assert delta(lambda: S.chunk_attention(q, [kv])) == 1
+    assert delta(lambda: S.rope3d_apply(q, torch.empty_like(q), 3, 10, 10)) == 1
+    o = bf16((300, 256), seed, I.KIND_Q).cuda()
+    wt = bf16((256, 256), seed, I.KIND_WO, std=1 / 16).cuda()
+    x = torch.zeros((300, 256), dtype=torch.float32, device="cuda")
+    assert delta(lambda: S.out_proj_euler_step(o, wt, x, 0.1)) == 1
+    before = n()
+    with pytest.raises(S.SavgbError):
+        S._check(S.lib().rope3d_apply(None, None, 1, 16, 2, 64, 1, 4, 4, 0, 1e4, None))
+    assert n() == before
+
+    rk, rv = I.reference_kv(w, seed)
+    wo = I.out_proj_weight(w, seed).cuda()
+    cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
+                       w.rope_base)
+    cs.set_reference(rk.cuda(), rv.cuda())
+    assert cs.fused_q_rope
+    xs = torch.from_numpy(I.normal_f32((w.B * w.n_q, w.hid), 1.0, seed, I.KIND_X, 0)).cuda()
+    dts = S.flow_time_grid(w.steps, w.shift)
+    ins = [tuple(t.cuda() for t in (st.q, st.k, st.v)) for st in (I.step_inputs(w, seed, 0, s_) for s_ in range(2))]
+    assert delta(lambda: cs.step(*ins[0], wo, xs, dts[0], False)) == 3
+
+    def last_step():
+        cs.step(*ins[1], wo, xs, dts[1], True)
+        cs.end_chunk()
+    assert delta(last_step) == 4
+    cs.sync()
+    cs.close()
+
+
 # ------------------------------------------------------------- watchdog
 
 def test_watchdog_timeout_is_reported(S):
