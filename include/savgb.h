@@ -328,8 +328,9 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
  * call, host to host, as a serving loop that receives each step's q, k, v
  * from the host and hands the state back would run it.  Needs host_io in the
  * config: the arena then holds host_io (at least 2, at most 4) device input
- * slots of 3 x B*N*H*D bf16; more slots let the uploads run further ahead of
- * the compute and ride out a slow spell of the host link.
+ * slots of 3 x B*N*H*D bf16 and two staging copies of the state, B*N*H*D fp32
+ * each; more slots let the uploads run further ahead of the compute and ride
+ * out a slow spell of the host link.
  *   q_host, k_host, v_host  bf16 [B][N][H][D] in host memory; page-locked
  *       (cudaHostAlloc / cudaHostRegister) for the upload to overlap compute,
  *       pageable memory also works but its copy blocks the calling thread.
@@ -339,14 +340,16 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
  * The call enqueues and returns.  The upload goes into input slot (call
  * count mod slots) on an internal copy stream once the step that last used
  * that slot has finished with it; the step runs on the handle's stream once its
- * upload has landed; the read-back of x runs on a second internal copy stream
- * after the step, straight from x (no staging copy): the W_o update of the
- * next step of this stream waits for it.  So consecutive calls overlap the
- * upload of step i+1 and the read-back of step i with the compute of step i+1.
+ * upload has landed.  With x_host, the step's W_o update also writes the new x
+ * into one of the two staging copies (alternately), and the read-back reads
+ * that copy on a second internal copy stream after the step; only the W_o
+ * update that writes the same copy again, two such calls later, waits for it.
+ * So consecutive calls overlap the upload of step i+1 and the read-back of
+ * step i with the compute of step i+1, and a read-back has two steps' time to
+ * land before it holds anything up.
  * Host buffers passed to a call must stay valid and unchanged (inputs) or
  * unread (x_host) until chunk_stream_sync() returns, or until the handle's
  * stream has passed a chunk_stream_join_copies() enqueued after the call.
- * Until then x may be written only by later steps of this stream.
  * SAVGB_ERR_STATE without host_io.  Otherwise as chunk_stream_step. */
 int chunk_stream_step_host(chunk_stream_t* s, const void* q_host, const void* k_host, const void* v_host,
                            const void* w_o, const float* bias, float* x, float dt, int is_last_step,

@@ -71,14 +71,19 @@ struct chunk_stream {
   cudaEvent_t step_events[4];  // recorded by the next step, then cleared
   bool have_events;
   // host_io: n_slots device input slots [q | k | v] filled from host memory
-  // on copy_in, the state read back on copy_out (chunk_stream_step_host)
+  // on copy_in; the state read back on copy_out from one of two staging
+  // copies that the W_o update writes beside x (chunk_stream_step_host)
   int n_slots;
   __nv_bfloat16_raw* in_slot[kMaxInSlots][3];
+  float* x_stage[2];
   cudaStream_t copy_in, copy_out;
   cudaEvent_t ev_loaded[kMaxInSlots], ev_freed[kMaxInSlots], ev_step_done, ev_out_done;
+  cudaEvent_t ev_stage_read[2];  // the read-back from that staging copy has landed
   bool slot_used[kMaxInSlots];
   int next_slot;
-  bool out_pending;  // a read-back of x is in flight: the next W_o update waits for it
+  bool stage_pending[2];  // a read-back from that staging copy is in flight
+  int next_stage;
+  bool out_pending;  // some read-back is in flight (ev_out_done: the latest)
   bool host_used;    // copies were enqueued since the last join / sync
 };
 
@@ -129,7 +134,12 @@ int host_io_init(chunk_stream* s) {
   }
   SAVGB_CUDA(cudaEventCreateWithFlags(&s->ev_step_done, cudaEventDisableTiming));
   SAVGB_CUDA(cudaEventCreateWithFlags(&s->ev_out_done, cudaEventDisableTiming));
+  for (int i = 0; i < 2; ++i) {
+    SAVGB_CUDA(cudaEventCreateWithFlags(&s->ev_stage_read[i], cudaEventDisableTiming));
+    s->stage_pending[i] = false;
+  }
   s->next_slot = 0;
+  s->next_stage = 0;
   s->out_pending = false;
   s->host_used = false;
   return SAVGB_OK;
@@ -144,15 +154,20 @@ void host_io_release(chunk_stream* s) {
   }
   if (s->ev_step_done) cudaEventDestroy(s->ev_step_done);
   if (s->ev_out_done) cudaEventDestroy(s->ev_out_done);
+  for (int i = 0; i < 2; ++i)
+    if (s->ev_stage_read[i]) cudaEventDestroy(s->ev_stage_read[i]);
   if (s->copy_in) cudaStreamDestroy(s->copy_in);
   if (s->copy_out) cudaStreamDestroy(s->copy_out);
 }
 
-// Before a launch that writes x: a read-back of x still in flight must end first.
-int wait_readback(chunk_stream* s) {
-  if (!s->out_pending) return SAVGB_OK;
-  SAVGB_CUDA(cudaStreamWaitEvent(s->stream, s->ev_out_done, 0));
-  s->out_pending = false;
+// The staging copy of x that a host step's W_o update writes: the read-back
+// from it two host steps back must have landed first.  nullptr for stage < 0.
+int take_stage(chunk_stream* s, int stage, float** x_copy) {
+  *x_copy = nullptr;
+  if (stage < 0) return SAVGB_OK;
+  if (s->stage_pending[stage]) SAVGB_CUDA(cudaStreamWaitEvent(s->stream, s->ev_stage_read[stage], 0));
+  s->stage_pending[stage] = false;
+  *x_copy = s->x_stage[stage];
   return SAVGB_OK;
 }
 
@@ -201,7 +216,8 @@ int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stre
   const int64_t tab_b = s->qrope ? round_up(rope_q_table_bytes(c.D, c.F, c.grid_h, c.grid_w), 256) : 0;
   s->n_slots = c.host_io ? (c.host_io < 2 ? 2 : c.host_io) : 0;
   const int64_t in_b = 3 * s->n_slots * tok_b;
-  s->arena_bytes = 2 * ref_b + 4 * bnd_b + 3 * tok_b + 4 * anc_b + vbuf_b + tab_b + in_b;
+  const int64_t stage_b = c.host_io ? round_up(s->n_tok * s->hid * 4 * c.B, 256) : 0;  // fp32 copies of x
+  s->arena_bytes = 2 * ref_b + 4 * bnd_b + 3 * tok_b + 4 * anc_b + vbuf_b + tab_b + in_b + 2 * stage_b;
   const char* cap = getenv("SAVGB_ARENA_LIMIT_BYTES");
   if (cap && *cap) {
     const long long lim = atoll(cap);
@@ -232,6 +248,7 @@ int chunk_stream_create(const chunk_stream_config* cfg, void* stream, chunk_stre
   s->qrope_tab = tab_b ? static_cast<void*>(take(tab_b)) : nullptr;
   for (int i = 0; i < s->n_slots; ++i)
     for (int t = 0; t < 3; ++t) s->in_slot[i][t] = take(tok_b);
+  for (int i = 0; i < 2; ++i) s->x_stage[i] = stage_b ? reinterpret_cast<float*>(take(stage_b)) : nullptr;
   if (s->qrope &&
       (rc = rope_q_table_build(s->qrope_tab, c.D, 0, c.F, c.grid_h, c.grid_w, c.rope_base, s->stream))) {
     cudaFree(s->arena);
@@ -274,10 +291,9 @@ int chunk_stream_set_reference(chunk_stream_t* s, const void* k_ref, const void*
   return SAVGB_OK;
 }
 
-int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const void* v,
-                      const void* w_o, const float* bias, float* x, float dt, int is_last_step) {
-  savgb::ApiRange api_range_("savgb:chunk_stream_step");
-  clear_error();
+// The step; with stage >= 0 the W_o update also writes x into that staging copy.
+static int step_impl(chunk_stream_t* s, const void* q, const void* k, const void* v, const void* w_o,
+                     const float* bias, float* x, float dt, int is_last_step, int stage) {
   if (!s) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_step: null handle");
   if (!s->ref_set) return fail(SAVGB_ERR_STATE, "chunk_stream_step: set_reference has not been called");
   if (!q || !k || !v || !w_o || !x) return fail(SAVGB_ERR_INVALID_ARG, "chunk_stream_step: null argument");
@@ -315,9 +331,10 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
   }
   if (rc) return rc;
   if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[2], s->stream));
-  if ((rc = wait_readback(s))) return rc;
+  float* x_copy = nullptr;
+  if ((rc = take_stage(s, stage, &x_copy))) return rc;
   rc = launch_out_proj_euler(s->o, w_o, bias, x, c.B * s->n_tok, (int)s->hid, (int)s->hid, dt,
-                             nullptr, s->stream);
+                             nullptr, s->stream, x_copy);
   if (rc) return rc;
   if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[3], s->stream));
   if (is_last_step && s->n_bnd > 0) {
@@ -359,6 +376,13 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
   return SAVGB_OK;
 }
 
+int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const void* v,
+                      const void* w_o, const float* bias, float* x, float dt, int is_last_step) {
+  savgb::ApiRange api_range_("savgb:chunk_stream_step");
+  clear_error();
+  return step_impl(s, q, k, v, w_o, bias, x, dt, is_last_step, -1);
+}
+
 int chunk_stream_step_host(chunk_stream_t* s, const void* q_host, const void* k_host, const void* v_host,
                            const void* w_o, const float* bias, float* x, float dt, int is_last_step,
                            float* x_host) {
@@ -380,19 +404,25 @@ int chunk_stream_step_host(chunk_stream_t* s, const void* q_host, const void* k_
   SAVGB_CUDA(cudaEventRecord(s->ev_loaded[slot], s->copy_in));
   SAVGB_CUDA(cudaStreamWaitEvent(s->stream, s->ev_loaded[slot], 0));
   s->host_used = true;
-  int rc = chunk_stream_step(s, s->in_slot[slot][0], s->in_slot[slot][1], s->in_slot[slot][2], w_o, bias, x, dt,
-                             is_last_step);
+  const int stage = x_host ? s->next_stage : -1;
+  int rc = step_impl(s, s->in_slot[slot][0], s->in_slot[slot][1], s->in_slot[slot][2], w_o, bias, x, dt,
+                     is_last_step, stage);
   if (rc) return rc;
   SAVGB_CUDA(cudaEventRecord(s->ev_freed[slot], s->stream));
   s->slot_used[slot] = true;
   s->next_slot = (slot + 1) % s->n_slots;
   if (x_host) {
-    // read x back straight from the state; the next W_o update waits for it
+    // read back the staging copy of x that this step's W_o update wrote; the
+    // W_o update that next writes this copy, two host steps later, waits for
+    // it, and nothing else does (x itself is not read)
     SAVGB_CUDA(cudaEventRecord(s->ev_step_done, s->stream));
     SAVGB_CUDA(cudaStreamWaitEvent(s->copy_out, s->ev_step_done, 0));
-    SAVGB_CUDA(cudaMemcpyAsync(x_host, x, (size_t)(s->cfg.B * s->n_tok * s->hid * 4), cudaMemcpyDeviceToHost,
-                               s->copy_out));
+    SAVGB_CUDA(cudaMemcpyAsync(x_host, s->x_stage[stage], (size_t)(s->cfg.B * s->n_tok * s->hid * 4),
+                               cudaMemcpyDeviceToHost, s->copy_out));
+    SAVGB_CUDA(cudaEventRecord(s->ev_stage_read[stage], s->copy_out));
     SAVGB_CUDA(cudaEventRecord(s->ev_out_done, s->copy_out));
+    s->stage_pending[stage] = true;
+    s->next_stage = stage ^ 1;
     s->out_pending = true;
   }
   return SAVGB_OK;
@@ -406,6 +436,7 @@ int chunk_stream_join_copies(chunk_stream_t* s) {
   // read-back (ev_out_done follows every earlier one on copy_out) is not
   if (s->out_pending) SAVGB_CUDA(cudaStreamWaitEvent(s->stream, s->ev_out_done, 0));
   s->out_pending = false;
+  s->stage_pending[0] = s->stage_pending[1] = false;
   return SAVGB_OK;
 }
 
@@ -456,7 +487,6 @@ int chunk_stream_istep(chunk_stream_t* s, const void* q, const void* k, const vo
                           c.exact_softmax != 0);
   }
   if (rc) return rc;
-  if ((rc = wait_readback(s))) return rc;
   return launch_out_proj_euler(s->o, w_o, bias, x, c.B * n_int, (int)s->hid, (int)s->hid, dt, nullptr,
                                s->stream);
 }
@@ -495,9 +525,7 @@ int chunk_stream_block_step(chunk_stream_t* s, const void* w_qkv, const void* w_
   if (ev) SAVGB_CUDA(cudaEventRecord(s->step_events[0], s->stream));
   const int64_t M = (int64_t)c.B * s->n_tok;
   void* xb = s->o;  // the bf16 copy of x is consumed by the projection before attention writes o
-  int rc = wait_readback(s);
-  if (rc) return rc;
-  rc = launch_to_bf16(x, xb, M * s->hid, s->stream);
+  int rc = launch_to_bf16(x, xb, M * s->hid, s->stream);
   if (rc) return rc;
   const int nxt = s->cur ^ 1;
   const bool capture = is_last_step && s->n_bnd > 0;
@@ -572,6 +600,7 @@ int chunk_stream_sync(chunk_stream_t* s) {
     SAVGB_CUDA(cudaStreamSynchronize(s->copy_in));
     SAVGB_CUDA(cudaStreamSynchronize(s->copy_out));
     s->out_pending = false;
+    s->stage_pending[0] = s->stage_pending[1] = false;
     s->host_used = false;
   }
   return savgb_device_check(s->stream);

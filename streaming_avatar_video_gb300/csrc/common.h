@@ -160,7 +160,9 @@ int launch_to_bf16(const float* x, void* y, int64_t n, cudaStream_t stream);
 
 int validate_out_proj(const void* o, const void* w, const float* bias, const float* x, int64_t M,
                       int hid_in, int hid_out, const float* v_out);
+// x_copy (optional, fp32 like x, not with v_out): also receives the updated x.
 int launch_out_proj_euler(const void* o, const void* w, const float* bias, float* x, int64_t M,
-                          int hid_in, int hid_out, float dt, float* v_out, cudaStream_t stream);
+                          int hid_in, int hid_out, float dt, float* v_out, cudaStream_t stream,
+                          float* x_copy = nullptr);
 
 }  // namespace savgb

@@ -46,6 +46,9 @@ struct WoParams {
   // and the limit of every wait of that kernel
   int fault_iter;
   uint64_t wait_limit_ns;
+  // optional fp32 [M][N]: receives a copy of the updated x (the same tensor-map
+  // stores, a second destination); x-only epilogues, not with v_out
+  float* x_copy;
 };
 
 constexpr int kXChunk = 32;                   // columns of x per staged chunk
@@ -56,7 +59,8 @@ template <int BN>
 __global__ void __launch_bounds__(gemm::kThreads, 1)
     wo_euler_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b,
-                    const __grid_constant__ CUtensorMap map_x, const WoParams p) {
+                    const __grid_constant__ CUtensorMap map_x,
+                    const __grid_constant__ CUtensorMap map_xc, const WoParams p) {
   using L = gemm::Layout<BN>;
   static_assert(8 * kXBufs * kXChunkBytes <= L::kBar, "x staging must fit in the operand ring");
   static_assert(8 * kXBufs * 8 <= 1024, "x barriers must fit in the epilogue's shared memory");
@@ -137,6 +141,7 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
           __syncwarp();
           if (lane == 0) {
             dev::tma_store_2d(&map_x, xb + bi * kXChunkBytes, ncol0, row_base);
+            if (p.x_copy) dev::tma_store_2d(&map_xc, xb + bi * kXChunkBytes, ncol0, row_base);
             dev::bulk_commit();
             if (cc + kXBufs < nch) {
               // the buffer is reloaded once its store has read it
@@ -223,7 +228,8 @@ static_assert(L::kDynSmem <= 227 * 1024, "shared memory budget");
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_pair::kThreads, 1)
     wo_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                   const __grid_constant__ CUtensorMap map_x, const WoParams p, int n_tiles_n, int n_tiles) {
+                   const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_xc,
+                   const WoParams p, int n_tiles_n, int n_tiles) {
   using L = pair::L;
   extern __shared__ uint8_t smem_raw[];
   const gemm_pair::Ctx c = gemm_pair::setup<L>(smem_raw, &map_a, &map_b, &map_x);
@@ -297,6 +303,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_pair::kThreads,
         __syncwarp();
         if (lane == 0) {
           dev::tma_store_2d(&map_x, xb, n, row_base);
+          if (p.x_copy) dev::tma_store_2d(&map_xc, xb, n, row_base);
           dev::bulk_commit();
           if (cc + 1 < nch) {
             // the buffer is reloaded once its store has read it
@@ -320,7 +327,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_pair::kThreads,
 
 template <int BN>
 int launch_bn(const void* o, const void* w, const float* bias, float* x, int64_t M, int K, int N,
-              float dt, float* v_out, cudaStream_t stream) {
+              float dt, float* v_out, float* x_copy, cudaStream_t stream) {
   using L = gemm::Layout<BN>;
   static bool attr_done[64] = {false};
   int dev_id = 0;
@@ -340,16 +347,20 @@ int launch_bn(const void* o, const void* w, const float* bias, float* x, int64_t
   const uint32_t bb[2] = {gemm::kBK, BN};
   rc = encode_tiled(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, db, sa, bb, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
-  CUtensorMap mx;
+  CUtensorMap mx, mxc;
   const uint64_t dx[2] = {(uint64_t)N, (uint64_t)M};
   const uint64_t sx[1] = {(uint64_t)N * 4};
   const uint32_t bx[2] = {kXChunk, 32};
   rc = encode_tiled(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, x, dx, sx, bx, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
-  WoParams p{(int)M, N, K, dt, bias, x, v_out, nullptr, -1, dev::kWaitLimitNs};
+  rc = encode_tiled(&mxc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, x_copy ? x_copy : x, dx, sx, bx,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  WoParams p{(int)M, N, K, dt, bias, x, v_out, nullptr, -1, dev::kWaitLimitNs, x_copy};
   if ((rc = error_word(&p.err))) return rc;
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + gemm::kBM - 1) / gemm::kBM));
-  SAVGB_CUDA(launch_dependent(wo_euler_kernel<BN>, grid, dim3(gemm::kThreads), L::kDynSmem, stream, ma, mb, mx, p));
+  SAVGB_CUDA(launch_dependent(wo_euler_kernel<BN>, grid, dim3(gemm::kThreads), L::kDynSmem, stream, ma, mb, mx,
+                              mxc, p));
   SAVGB_CUDA(cudaGetLastError());
   note_launch();
   return SAVGB_OK;
@@ -373,7 +384,7 @@ int validate_out_proj(const void* o, const void* w, const float* bias, const flo
 // The persistent CTA-pair kernel: x updated alone (no velocity output), the
 // output width a multiple of 256.
 int launch_pair(const void* o, const void* w, const float* bias, float* x, int64_t M, int K, int N, float dt,
-                int sms, cudaStream_t stream) {
+                float* x_copy, int sms, cudaStream_t stream) {
   static bool attr_done[64] = {false};
   static int max_clusters[64] = {0};
   int dev_id = 0;
@@ -385,7 +396,7 @@ int launch_pair(const void* o, const void* w, const float* bias, float* x, int64
     if (rc) return rc;
     attr_done[dev_id & 63] = true;
   }
-  CUtensorMap ma, mb, mx;
+  CUtensorMap ma, mb, mx, mxc;
   const uint64_t da[2] = {(uint64_t)K, (uint64_t)M};
   const uint64_t sa[1] = {(uint64_t)K * 2};
   const uint32_t box128[2] = {gemm_pair::kBK, 128};
@@ -399,7 +410,10 @@ int launch_pair(const void* o, const void* w, const float* bias, float* x, int64
   const uint32_t bx[2] = {kXChunk, 32};
   rc = encode_tiled(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, x, dx, sx, bx, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
-  WoParams p{(int)M, N, K, dt, bias, x, nullptr, nullptr, -1, dev::kWaitLimitNs};
+  rc = encode_tiled(&mxc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, x_copy ? x_copy : x, dx, sx, bx,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  WoParams p{(int)M, N, K, dt, bias, x, nullptr, nullptr, -1, dev::kWaitLimitNs, x_copy};
   if ((rc = error_word(&p.err))) return rc;
   ArmedFault fault;
   if (take_fault(SAVGB_FAULT_WO_PAIR_RELAY, &fault)) {
@@ -411,22 +425,24 @@ int launch_pair(const void* o, const void* w, const float* bias, float* x, int64
   // one wave of pairs: as many clusters as can be resident at once
   const int clusters = std::min(n_tiles, max_clusters[dev_id & 63]);
   SAVGB_CUDA(launch_dependent(wo_pair_kernel, dim3((unsigned)(2 * clusters)), dim3(gemm_pair::kThreads),
-                              pair::L::kDynSmem, stream, ma, mb, mx, p, n_tiles_n, n_tiles));
+                              pair::L::kDynSmem, stream, ma, mb, mx, mxc, p, n_tiles_n, n_tiles));
   SAVGB_CUDA(cudaGetLastError());
   note_launch();
   return SAVGB_OK;
 }
 
 int launch_out_proj_euler(const void* o, const void* w, const float* bias, float* x, int64_t M,
-                          int hid_in, int hid_out, float dt, float* v_out, cudaStream_t stream) {
+                          int hid_in, int hid_out, float dt, float* v_out, cudaStream_t stream, float* x_copy) {
   int sms = 0;
   int rc = check_device(&sms);
   if (rc) return rc;
+  if (x_copy && (v_out || !aligned16(x_copy)))
+    return fail(SAVGB_ERR_INVALID_ARG, "out_proj_euler: a copy of x needs no v_out and a 16-byte aligned buffer");
   if (v_out == nullptr && hid_out % 256 == 0)
-    return launch_pair(o, w, bias, x, M, hid_in, hid_out, dt, sms, stream);
+    return launch_pair(o, w, bias, x, M, hid_in, hid_out, dt, x_copy, sms, stream);
   if (hid_out % 256 == 0)
-    return launch_bn<256>(o, w, bias, x, M, hid_in, hid_out, dt, v_out, stream);
-  return launch_bn<128>(o, w, bias, x, M, hid_in, hid_out, dt, v_out, stream);
+    return launch_bn<256>(o, w, bias, x, M, hid_in, hid_out, dt, v_out, x_copy, stream);
+  return launch_bn<128>(o, w, bias, x, M, hid_in, hid_out, dt, v_out, x_copy, stream);
 }
 
 }  // namespace savgb

@@ -312,8 +312,8 @@ def test_stream_host_io_matches_device_steps(S, slots):
     step) against chunk_stream_step on the same inputs: every step's read-back
     bit-identical to the device path's x after that step, the final state
     against the oracle.  One step in the middle runs through the device call:
-    its W_o update must wait for the previous read-back, whose buffer must
-    still hold the earlier state.  Pageable input memory works too."""
+    it updates x while the previous step's read-back, from its staging copy,
+    may still be in flight.  Pageable input memory works too."""
     w = I.WORKLOADS["small"]
     seed = 9
     rk, rv = I.reference_kv(w, seed)
@@ -910,15 +910,25 @@ def test_qkv_rope_project_parity(S, B, H, D, gt, gh, gw, t0):
     assert_close(f64(v), ov, what="v")
 
 
-def test_stream_host_io_two_sessions_four_slots(S):
-    """chunk_stream_step_host with the deepest input ring (4 device slots) on
-    two sessions of 1100 queries (W_o tiles straddle the sessions, ragged last
-    attention blocks), three chunks: every step's read-back bit-identical to
-    chunk_stream_step's x after that step, each chunk's final x against the
-    oracle.  Each chunk's x is a new device tensor; all of them stay alive
-    until the sync, since the read-backs run after the call returns."""
-    w = I.Workload("straddle", B=2, H=4, D=128, F=5, grid_h=10, grid_w=22, ref_frames=1,
-                   boundary_frames=1, steps=3, shift=1.0)
+_HOST_IO_WORKLOADS = {
+    # two sessions of 1100 queries: W_o tiles straddle the sessions, ragged last attention blocks
+    "two-sessions": I.Workload("straddle", B=2, H=4, D=128, F=5, grid_h=10, grid_w=22, ref_frames=1,
+                               boundary_frames=1, steps=3, shift=1.0),
+    # hid = 192: the single-CTA W_o kernel writes the staging copy
+    "narrow": I.Workload("narrow", B=1, H=3, D=64, F=3, grid_h=6, grid_w=10, ref_frames=1,
+                         boundary_frames=1, steps=3, shift=1.0),
+}
+
+
+@pytest.mark.parametrize("wname", list(_HOST_IO_WORKLOADS))
+def test_stream_host_io_four_slots(S, wname):
+    """chunk_stream_step_host with the deepest input ring (4 device slots),
+    three chunks: every step's read-back (from the staging copy the W_o update
+    writes) bit-identical to chunk_stream_step's x after that step, each
+    chunk's final x against the oracle.  Each chunk's x is a new device
+    tensor; all of them stay alive until the sync, since the read-backs run
+    after the call returns."""
+    w = _HOST_IO_WORKLOADS[wname]
     seed, chunks = 4, 3
     dts = S.flow_time_grid(w.steps, w.shift)
     rk, rv = I.reference_kv(w, seed)
@@ -957,7 +967,7 @@ def test_stream_host_io_two_sessions_four_slots(S):
     oracle_x, _ = run_stream_oracle(w, seed, chunks)
     for c in range(chunks):
         assert torch.equal(finals[c], want[(c, w.steps - 1)])
-        assert_close(f64(finals[c]), oracle_x[c], what=f"host-io two-session chunk {c} x")
+        assert_close(f64(finals[c]), oracle_x[c], what=f"host-io {wname} chunk {c} x")
 
 
 _BLOCK_WORKLOADS = {
