@@ -53,8 +53,8 @@ METRIC = "chunk-attention TFLOP/s (% of bf16 tensor peak); latent frames/s per d
 # change of them reports null.
 ATTN_TRAFFIC = {
     # profiles/chunk_attention_base.md and profiles/chunk_attention_sr.md: the fused-RoPE kernel the stream
-    # runs; base 292.767 MB read + 61.134 MB written, SR 1738.437 MB read + 295.282 MB written
-    "a6b132ae6f7e95df8e19bbec15f02d80a3175144f42917a46612aa6af81fefb5": {"base": 353901056, "sr": 2033718784},
+    # runs; base 291.848 MB read + 61.056 MB written, SR 1720.399 MB read + 295.447 MB written
+    "e8953a85b0dbd3b45a18a45a833dfcf75489c2be595551076a0736069d9ff2e2": {"base": 352904192, "sr": 2015845632},
 }
 
 
