@@ -579,14 +579,20 @@ def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world, i0=0):
     cs.sync()
     i_next += n
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    stage = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
     evs[0].record(stream)
     for j, i in enumerate(range(i_next, i_next + n)):
+        cs.set_step_events(stage[j])
         step(i, ev=evs[j + 1])
     cs.join_copies()
     torch.cuda.synchronize()
     cs.sync()
     i_next += n
     periods = [round(evs[j].elapsed_time(evs[j + 1]), 3) for j in range(n)]
+    # a step starts once its upload has landed: the gap after the previous step is the upload's wait; W_o's span
+    # includes its wait for the read-back that last used its staging copy
+    upload_wait = [round((evs[j] if j == 0 else stage[j - 1][3]).elapsed_time(stage[j][0]), 3) for j in range(n)]
+    wo_span = [round(stage[j][2].elapsed_time(stage[j][3]), 3) for j in range(n)]
     h2d = sum(t.numel() * t.element_size() for t in sets[0])
     d2h = x.numel() * x.element_size()
     return {"value": round(whole_job_rate(world, w.attn_flops(True), ms) / 1e12, 2), "unit": "TFLOP/s",
@@ -594,8 +600,12 @@ def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world, i0=0):
             "clocks": clk.summary(), "copies_alone": copies,
             "diagnostics": {"uploads_only_ms_per_step": round(a2.elapsed_time(b2) / n, 4),
                             "step_periods_ms": periods,
-                            "what": "after the timed region: the same loop without read-backs, and the period of "
-                                    "each step of one more pass (events on the compute stream)"},
+                            "upload_wait_ms": upload_wait,
+                            "wo_incl_readback_wait_ms": wo_span,
+                            "what": "after the timed region: the same loop without read-backs, and for each step "
+                                    "of one more pass its period, the compute stream's wait for its upload and "
+                                    "the span of its W_o update with any wait for an earlier read-back (events "
+                                    "on the compute stream)"},
             "api": "C ABI chunk_stream_step_host: pinned host q/k/v in, x read back to pinned host memory every "
                    "step; the library overlaps the uploads and read-backs with the steps on two copy streams; "
                    "measured right after the headline region"}, i0 + i_next
