@@ -42,6 +42,12 @@
 extern "C" {
 #endif
 
+/* The library is built with hidden symbol visibility: these declarations are
+ * its only exports. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
 typedef enum {
   SAVGB_OK = 0,
   SAVGB_ERR_INVALID_ARG = -1, /* a size, count or pointer is out of range */
@@ -474,6 +480,10 @@ int chunk_step_noalloc(const void* q, const void* k, const void* v, const savgb_
                        int n_context, const void* w_o, const float* bias, float* x, float dt, int B,
                        int H, int D, int F, int grid_h, int grid_w, double rope_base,
                        float softmax_scale, void* stream);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
 
 #ifdef __cplusplus
 }

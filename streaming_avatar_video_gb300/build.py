@@ -33,7 +33,7 @@ def nvcc_path() -> str:
 
 
 def _flags(ptxas_verbose: bool):
-    f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
+    f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
                 "-I", INCLUDE, "-I", CSRC]
     if ptxas_verbose:
         f += ["-Xptxas", "-v"]
