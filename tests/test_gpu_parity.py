@@ -5,6 +5,7 @@ Sizes the oracle finishes in seconds span several tiles and a ragged tail;
 the full base-DiT and SR chunk shapes are checked on sampled query rows,
 computed by the oracle one by one against the full key/value set."""
 import math
+import os
 
 import numpy as np
 import pytest
@@ -269,6 +270,65 @@ def test_stream_wide_grid_unfused(S):
     q = torch.zeros(1, w.n_q, w.H, w.D, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(S.SavgbError):
         S.chunk_attention_qrope(q, (w.F, w.grid_h, w.grid_w), [(q, q)])
+
+
+def _cuda_dirs():
+    """The CUDA toolkit's include and runtime-library directories."""
+    import glob
+    import shutil
+    home = os.environ.get("CUDA_HOME") or os.path.dirname(os.path.dirname(shutil.which("nvcc") or
+                                                                          "/usr/local/cuda/bin/nvcc"))
+    incs = [os.path.join(home, "include")] + glob.glob(os.path.join(home, "targets", "*", "include"))
+    libs = [os.path.join(home, "lib64")] + glob.glob(os.path.join(home, "targets", "*", "lib"))
+    inc = next((d for d in incs if os.path.exists(os.path.join(d, "cuda_runtime_api.h"))), None)
+    lib = next((d for d in libs if glob.glob(os.path.join(d, "libcudart.so*"))), None)
+    return inc, lib
+
+
+def test_c_program_runs_a_stream(S, tmp_path):
+    """A plain C program (tests/abi_c_stream.c) runs a two-session stream of 3
+    chunks x 3 shifted steps through the C ABI alone, with device buffers from
+    its own CUDA runtime calls: each chunk's x equals, bit for bit, the same
+    stream run through the Python binding, and matches the oracle."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    inc, cudalib = _cuda_dirs()
+    if cc is None or inc is None or cudalib is None:
+        pytest.skip("no C compiler or CUDA runtime headers")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.dirname(S.LIB_PATH)
+    exe = str(tmp_path / "abi_c_stream")
+    subprocess.run([cc, "-std=c11", "-O2", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(root, "include"),
+                    "-I", inc, os.path.join(root, "tests", "abi_c_stream.c"), "-L", libdir, "-lsavgb",
+                    "-L", cudalib, "-lcudart", f"-Wl,-rpath,{libdir}:{cudalib}", "-o", exe], check=True)
+    w = I.Workload("cprog", B=2, H=2, D=64, F=3, grid_h=4, grid_w=6, ref_frames=1, boundary_frames=1, steps=3,
+                   shift=3.0)
+    seed, chunks = 15, 3
+    raw = lambda t: t.contiguous().view(torch.int16).numpy().tobytes() if t.dtype == torch.bfloat16 \
+        else t.contiguous().numpy().tobytes()  # noqa: E731
+    rk, rv = I.reference_kv(w, seed)
+    (tmp_path / "ref_k.bin").write_bytes(raw(rk))
+    (tmp_path / "ref_v.bin").write_bytes(raw(rv))
+    (tmp_path / "w_o.bin").write_bytes(raw(I.out_proj_weight(w, seed)))
+    for c in range(chunks):
+        (tmp_path / f"x_{c}.bin").write_bytes(I.normal_f32((w.B * w.n_q, w.hid), 1.0, seed, I.KIND_X, c).tobytes())
+        for s_ in range(w.steps):
+            st = I.step_inputs(w, seed, c, s_)
+            for name, t in (("q", st.q), ("k", st.k), ("v", st.v)):
+                (tmp_path / f"{name}_{c}_{s_}.bin").write_bytes(raw(t))
+    r = subprocess.run([exe, str(tmp_path), *map(str, (w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames,
+                                                          w.boundary_frames, w.ref_t, chunks, w.steps, w.shift))],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr
+    got = [np.frombuffer((tmp_path / f"out_{c}.bin").read_bytes(), dtype=np.float32).reshape(w.B * w.n_q, w.hid)
+           for c in range(chunks)]
+    cs, xs, _ = run_stream_gpu(S, w, seed, chunks)
+    cs.close()
+    want, _ = run_stream_oracle(w, seed, chunks)
+    for c in range(chunks):
+        assert np.array_equal(got[c], xs[c].numpy()), f"chunk {c}: the C program and the binding differ"
+        assert_close(got[c].astype(np.float64), want[c], what=f"C program chunk {c} x")
 
 
 def test_stream_small_pair(S):
