@@ -949,12 +949,33 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    """The host CPU's model, from lscpu, else /proc/cpuinfo, else the machine type."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.machine() or "unknown"
+
+
 def cpu_baseline(w: I.Workload, budget_s: float):
     smp = OracleSample(w)
     rows, frames = smp.calibrated(budget_s)
     secs, per_step, desc = smp.run(rows, frames)
     return {"value": round(w.attn_flops(True) / per_step / 1e12, 6), "unit": "TFLOP/s",
-            "cores": cpu_cores(), "kind": "oracle", "sample": desc,
+            "cores": cpu_cores(), "cpu_model": cpu_model(), "kind": "oracle", "sample": desc,
             "sample_seconds": round(secs, 2), "extrapolated": True,
             "extrapolated_s_per_step": round(per_step, 2),
             "threads": "numpy BLAS default (all affinity cores)"}
@@ -992,8 +1013,8 @@ def run_reference(args, w: I.Workload, world: int, rank: int):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) q/k/v/ref, W_o ~ N(0,1/hid), x ~ N(0,1))",
         "config": config_of(w, world),
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": desc, "extrapolated": True},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "cpu_model": cpu_model(),
+                         "kind": "oracle", "sample": desc, "extrapolated": True},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
