@@ -991,7 +991,7 @@ def run_reference(args, w: I.Workload, world: int, rank: int):
     if rank != 0:
         return None
     smp = OracleSample(w)
-    budget = min(20.0, max(0.05, 100.0 / (args.steps + args.warmup)))
+    budget = min(20.0, args.cpu_seconds, max(0.05, 100.0 / (args.steps + args.warmup)))
     rows, frames = smp.calibrated(budget)
     per, walls = [], []
     desc = ""
@@ -1049,11 +1049,15 @@ def main():
         ap.error("--warmup must be >= 3")
     head = "sr" if args.config == "default" else args.config
     w = I.WORKLOADS["base" if head in ("ibase", "block") else head]
-    world, rank, local = dist_setup()
+    # the reference arm runs on the host cores alone: its ranks need no GPU
+    world, rank, local = dist_setup("gloo" if args.impl == "reference" else "nccl")
     if args.impl == "reference":
         res = run_reference(args, w, world, rank)
         if rank == 0 and res is not None:
             print(json.dumps(res), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
     if head in ("long", "ibase", "block"):
         fn = {"long": run_long, "ibase": run_interp, "block": run_block}[head]

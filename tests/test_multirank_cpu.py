@@ -55,3 +55,25 @@ def test_single_rank_needs_no_process_group(monkeypatch):
     assert bench.dist_setup("gloo") == (1, 0, 0)
     assert bench.max_over_ranks(1, 3.5) == 3.5
     assert bench.whole_job_rate(1, 8.0, 2.0) == pytest.approx(4000.0)
+
+
+def test_reference_arm_under_torchrun():
+    """`bench.py --impl reference` launched as the driver launches it for N > 1
+    (torchrun, two ranks, 127.0.0.1), on the tiny workload: rank 0 times the
+    oracle and prints one JSON line; the other rank exits 0 without work.  The
+    reference arm needs no GPU, so its ranks form a gloo group."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
+           "--config", "tiny", "--gpus", "2", "--steps", "1", "--warmup", "3", "--cpu-seconds", "0.1"]
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=600,
+                       env={**os.environ, "OMP_NUM_THREADS": "1"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["extrapolated"] is True
+    assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
