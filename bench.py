@@ -991,7 +991,7 @@ def run_reference(args, w: I.Workload, world: int, rank: int):
     if rank != 0:
         return None
     smp = OracleSample(w)
-    budget = min(20.0, args.cpu_seconds, max(0.05, 100.0 / (args.steps + args.warmup)))
+    budget = min(20.0, getattr(args, "cpu_seconds", 20.0), max(0.05, 100.0 / (args.steps + args.warmup)))
     rows, frames = smp.calibrated(budget)
     per, walls = [], []
     desc = ""
