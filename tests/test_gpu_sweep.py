@@ -1,8 +1,8 @@
 """Seeded random-shape sweeps of every kernel entry point against the fp64
 oracle, every output element compared (bars of tests/_util.py).
 
-The shapes are drawn from a fixed seed so that each run checks the same
-cases: degenerate sizes (a single query, a single key, empty segments, one
+The shapes are drawn from fixed seeds (two batches per kernel) so that each
+run checks the same cases: degenerate sizes (a single query, a single key, empty segments, one
 row of W_o), sizes one either side of the 128-row tiles and of the 256-row
 query blocks, odd head counts, both head sizes, both W_o kernels, and RoPE
 grids with negative start times."""
@@ -40,7 +40,7 @@ _NQ = [1, 2, 127, 128, 129, 255, 256, 257, 383, 700]
 _NKV = [0, 1, 2, 63, 127, 128, 129, 300, 511]
 
 
-def _attention_cases(n=16, seed=2024):
+def _attention_cases(n=16, seed=2024, degenerate=True, seed0=100):
     rng = np.random.default_rng(seed)
     cases = []
     for i in range(n):
@@ -50,15 +50,18 @@ def _attention_cases(n=16, seed=2024):
             segs[-1] = int(rng.choice(_NKV[1:]))
         cases.append(dict(B=int(rng.integers(1, 4)), H=int(rng.integers(1, 5)), D=int(rng.choice([64, 128])),
                           n_q=int(rng.choice(_NQ)), segs=segs, scale=float(rng.choice([0.0, 0.05, 0.3])),
-                          lse=bool(i % 2), seed=100 + i))
-    # degenerate ones, always: one query over one key, one query over many, keys only in the last segment
+                          lse=bool(i % 2), seed=seed0 + i))
+    if not degenerate:
+        return cases
+    # degenerate ones: one query over one key, one query over many, keys only in the last segment
     cases += [dict(B=1, H=1, D=128, n_q=1, segs=[1], scale=0.0, lse=True, seed=150),
               dict(B=2, H=3, D=64, n_q=1, segs=[511, 1, 0], scale=0.0, lse=True, seed=151),
               dict(B=1, H=2, D=128, n_q=2, segs=[0, 0, 1], scale=0.0, lse=False, seed=152)]
     return cases
 
 
-@pytest.mark.parametrize("c", _attention_cases(), ids=lambda c: f"B{c['B']}H{c['H']}D{c['D']}q{c['n_q']}kv{c['segs']}")
+@pytest.mark.parametrize("c", _attention_cases() + _attention_cases(16, 31337, False, 500),
+                         ids=lambda c: f"B{c['B']}H{c['H']}D{c['D']}q{c['n_q']}kv{c['segs']}s{c['scale']}")
 def test_attention_sweep(S, c):
     B, H, D, n_q, seed = c["B"], c["H"], c["D"], c["n_q"], c["seed"]
     q = bf16((B, n_q, H, D), seed, I.KIND_Q)
@@ -80,17 +83,18 @@ def test_attention_sweep(S, c):
                      what=f"lse {c}")
 
 
-def _qrope_cases(n=8, seed=7):
+def _qrope_cases(n=8, seed=7, seed0=200):
     rng = np.random.default_rng(seed)
     out = []
     for i in range(n):
         out.append(dict(B=int(rng.integers(1, 3)), H=int(rng.integers(1, 4)), D=int(rng.choice([64, 128])),
                         grid=(int(rng.integers(1, 5)), int(rng.integers(1, 21)), int(rng.integers(1, 41))),
-                        t0=int(rng.integers(-5, 6)), ctx=int(rng.choice([0, 1, 90, 257])), seed=200 + i))
+                        t0=int(rng.integers(-5, 6)), ctx=int(rng.choice([0, 1, 90, 257])), seed=seed0 + i))
     return out
 
 
-@pytest.mark.parametrize("c", _qrope_cases(), ids=lambda c: f"B{c['B']}H{c['H']}D{c['D']}g{c['grid']}t{c['t0']}")
+@pytest.mark.parametrize("c", _qrope_cases() + _qrope_cases(8, 4242, 600),
+                         ids=lambda c: f"B{c['B']}H{c['H']}D{c['D']}g{c['grid']}t{c['t0']}c{c['ctx']}")
 def test_attention_qrope_sweep(S, c):
     B, H, D, (gt, gh, gw), t0, seed = c["B"], c["H"], c["D"], c["grid"], c["t0"], c["seed"]
     n_q = gt * gh * gw
@@ -109,7 +113,7 @@ def test_attention_qrope_sweep(S, c):
     assert_close(f64(o), O.attention(O.rope3d(f64(q), gt, gh, gw, t0), osegs), what=f"qrope attention {c}")
 
 
-def _wo_cases(n=12, seed=99):
+def _wo_cases(n=12, seed=99, seed0=300):
     rng = np.random.default_rng(seed)
     out = []
     for i in range(n):
@@ -117,11 +121,12 @@ def _wo_cases(n=12, seed=99):
         out.append(dict(M=int(rng.choice([1, 7, 128, 255, 256, 257, 700, 1500])),
                         hid_in=int(rng.choice([8, 24, 64, 200, 512, 1000])), hid_out=hid_out,
                         bias=bool(rng.integers(0, 2)), with_v=bool(rng.integers(0, 2)),
-                        dt=float(rng.choice([0.01, 0.125, -0.3])), seed=300 + i))
+                        dt=float(rng.choice([0.01, 0.125, -0.3])), seed=seed0 + i))
     return out
 
 
-@pytest.mark.parametrize("c", _wo_cases(), ids=lambda c: f"M{c['M']}k{c['hid_in']}n{c['hid_out']}")
+@pytest.mark.parametrize("c", _wo_cases() + _wo_cases(12, 2718, 700),
+                         ids=lambda c: f"M{c['M']}k{c['hid_in']}n{c['hid_out']}b{int(c['bias'])}v{int(c['with_v'])}")
 def test_out_proj_euler_sweep(S, c):
     M, K, N, seed = c["M"], c["hid_in"], c["hid_out"], c["seed"]
     o = bf16((M, K), seed, I.KIND_Q)
