@@ -162,6 +162,55 @@ def test_attention_full_size_sampled_rows(S, name):
     attn_case(S, w.B, w.H, w.D, w.n_q, [w.n_ref, w.n_b, w.n_q], 21, rows=rows, margin=True)
 
 
+def test_attention_sr_every_element_by_invariants(S):
+    """The SR-shaped attention on every output element, through properties
+    that hold at any size (the oracle checks sampled rows above):
+    - two sessions whose second is a copy of the first give two identical
+      outputs, bit for bit (batch indexing);
+    - reversing the heads of q, k and v reverses the output's heads, bit for
+      bit (head indexing);
+    - the same keys split as [reference | boundary | chunk] and as
+      [reference + boundary | chunk] (other tile boundaries and tails) agree
+      within twice the oracle bar, since each is within the bar of the exact
+      result;
+    - the fused-RoPE call on unrotated queries agrees with the plain call on
+      queries rotated by rope3d_apply within the same bound."""
+    w = I.WORKLOADS["sr"]
+    seed = 22
+    q = bf16((1, w.n_q, w.H, w.D), seed, I.KIND_Q).cuda()
+    segs = [(bf16((1, n, w.H, w.D), seed, I.KIND_K, chunk=i).cuda(), bf16((1, n, w.H, w.D), seed, I.KIND_V,
+                                                                          chunk=i).cuda())
+            for i, n in enumerate([w.n_ref, w.n_b, w.n_q])]
+    o = S.chunk_attention(q, segs)
+    # batch: the session duplicated
+    o2 = S.chunk_attention(torch.cat([q, q]), [(torch.cat([k, k]), torch.cat([v, v])) for k, v in segs])
+    assert torch.equal(o2[0], o[0]) and torch.equal(o2[1], o[0])
+    del o2
+    # heads reversed
+    flip = lambda t: t.flip(2).contiguous()  # noqa: E731
+    of = S.chunk_attention(flip(q), [(flip(k), flip(v)) for k, v in segs])
+    assert torch.equal(of.flip(2), o)
+    del of
+    # the keys re-split: reference and boundary in one segment
+    joined = [(torch.cat([segs[0][0], segs[1][0]], 1), torch.cat([segs[0][1], segs[1][1]], 1)), segs[2]]
+    oj = S.chunk_attention(q, joined)
+    d = (oj.float() - o.float()).abs()
+    resplit = (d.max().item(), d.mean().item())
+    assert resplit[0] <= 4e-2 and resplit[1] <= 4e-3, resplit
+    del oj
+    # fused RoPE of q against rope3d_apply + the plain call
+    qr = torch.empty_like(q)
+    S.rope3d_apply(q, qr, w.F, w.grid_h, w.grid_w, 0)
+    o_plain = S.chunk_attention(qr, segs)
+    o_fused = S.chunk_attention_qrope(q, (w.F, w.grid_h, w.grid_w), segs, t0=0)
+    S.savgb_device_check()
+    d = (o_fused.float() - o_plain.float()).abs()
+    fused = (d.max().item(), d.mean().item())
+    assert fused[0] <= 4e-2 and fused[1] <= 4e-3, fused
+    print(f"SR attention, every element: re-split max-abs {resplit[0]:.2e} mean-abs {resplit[1]:.2e}; "
+          f"fused RoPE of q max-abs {fused[0]:.2e} mean-abs {fused[1]:.2e}")
+
+
 # ------------------------------------------------------- W_o + Euler update
 
 @pytest.mark.parametrize("with_v", [True, False])  # the velocity-out epilogue, and the staged one of the stream
