@@ -276,7 +276,7 @@ def run_ours(args, w: I.Workload, world: int, rank: int, local: int):
     x = I.state_x(w, seed).to(dev)
 
     cs = S.ChunkStream(w.B, w.H, w.D, w.F, w.grid_h, w.grid_w, w.ref_frames, w.boundary_frames, w.ref_t,
-                       w.rope_base, host_io=0 if args.no_e2e else 4)
+                       w.rope_base, host_io=0 if args.no_e2e else 8)
     cs.set_reference(rk.to(dev), rv.to(dev))
     # prime: one chunk end so that every timed step attends over the boundary too
     q, k, v = dsets[0]
@@ -533,8 +533,8 @@ def run_e2e(args, w, cs, sets, wo, x, dts, dev, stream, world, i0=0):
     """Same metric through the C-ABI call with HOST buffers:
     chunk_stream_step_host takes the step's q, k, v from pinned host memory
     and reads the updated state x back into pinned host memory every step.
-    The library uploads each step's inputs into one of four device slots on
-    a copy stream, up to three steps ahead of the compute, and reads x back
+    The library uploads each step's inputs into one of eight device slots on
+    a copy stream, up to seven steps ahead of the compute, and reads x back
     from a staging copy (written by the W_o update beside x, two alternating)
     on a second copy stream while the next steps compute.  The timed region ends
     once the last read-back has landed (join_copies, then an event)."""

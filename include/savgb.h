@@ -301,7 +301,7 @@ typedef struct {
   float softmax_scale; /* <= 0 selects 1/sqrt(D) */
   int interp_chunks;   /* nonzero: keep the anchors of interpolation chunks (needs F >= 3) */
   int qkv_block;       /* nonzero: reserve room for chunk_stream_block_step */
-  int host_io;         /* 0, or the device input slots of chunk_stream_step_host: 2 to 4 (1 means 2) */
+  int host_io;         /* 0, or the device input slots of chunk_stream_step_host: 2 to 8 (1 means 2) */
   int exact_softmax;   /* nonzero: the steps' attention takes fp32 exponentials (see chunk_attention) */
 } chunk_stream_config;
 /* The same config under the name the problem statement's interface uses. */
@@ -333,7 +333,7 @@ int chunk_stream_step(chunk_stream_t* s, const void* q, const void* k, const voi
  * the updated state read back to host memory: the whole step through one
  * call, host to host, as a serving loop that receives each step's q, k, v
  * from the host and hands the state back would run it.  Needs host_io in the
- * config: the arena then holds host_io (at least 2, at most 4) device input
+ * config: the arena then holds host_io (at least 2, at most 8) device input
  * slots of 3 x B*N*H*D bf16 and two staging copies of the state, B*N*H*D fp32
  * each; more slots let the uploads run further ahead of the compute and ride
  * out a slow spell of the host link.

@@ -34,7 +34,7 @@
 using namespace savgb;
 
 // input slots of chunk_stream_step_host: host_io in the config (1 means 2)
-constexpr int kMaxInSlots = 4;
+constexpr int kMaxInSlots = 8;
 
 struct chunk_stream {
   chunk_stream_config cfg;

@@ -1020,24 +1020,25 @@ def test_qkv_rope_project_parity(S, B, H, D, gt, gh, gw, t0):
 
 
 _HOST_IO_WORKLOADS = {
-    # two sessions of 1100 queries: W_o tiles straddle the sessions, ragged last attention blocks
-    "two-sessions": I.Workload("straddle", B=2, H=4, D=128, F=5, grid_h=10, grid_w=22, ref_frames=1,
-                               boundary_frames=1, steps=3, shift=1.0),
+    # two sessions of 1100 queries: W_o tiles straddle the sessions, ragged last attention blocks; the deepest
+    # ring (8 slots: more than the 9 steps of the run can fill ahead of the compute)
+    "two-sessions": (I.Workload("straddle", B=2, H=4, D=128, F=5, grid_h=10, grid_w=22, ref_frames=1,
+                                boundary_frames=1, steps=3, shift=1.0), 8),
     # hid = 192: the single-CTA W_o kernel writes the staging copy
-    "narrow": I.Workload("narrow", B=1, H=3, D=64, F=3, grid_h=6, grid_w=10, ref_frames=1,
-                         boundary_frames=1, steps=3, shift=1.0),
+    "narrow": (I.Workload("narrow", B=1, H=3, D=64, F=3, grid_h=6, grid_w=10, ref_frames=1,
+                          boundary_frames=1, steps=3, shift=1.0), 4),
 }
 
 
 @pytest.mark.parametrize("wname", list(_HOST_IO_WORKLOADS))
-def test_stream_host_io_four_slots(S, wname):
-    """chunk_stream_step_host with the deepest input ring (4 device slots),
+def test_stream_host_io_deep_rings(S, wname):
+    """chunk_stream_step_host with deep input rings (4 and 8 device slots),
     three chunks: every step's read-back (from the staging copy the W_o update
     writes) bit-identical to chunk_stream_step's x after that step, each
     chunk's final x against the oracle.  Each chunk's x is a new device
     tensor; all of them stay alive until the sync, since the read-backs run
     after the call returns."""
-    w = _HOST_IO_WORKLOADS[wname]
+    w, slots = _HOST_IO_WORKLOADS[wname]
     seed, chunks = 4, 3
     dts = S.flow_time_grid(w.steps, w.shift)
     rk, rv = I.reference_kv(w, seed)
@@ -1070,7 +1071,7 @@ def test_stream_host_io_four_slots(S, wname):
         return out, [x.cpu() for x in xs]
 
     want, _ = run(0)
-    got, finals = run(4)
+    got, finals = run(slots)
     for p in plan:
         assert torch.equal(got[p], want[p]), f"read-back after chunk {p[0]} step {p[1]}"
     oracle_x, _ = run_stream_oracle(w, seed, chunks)

@@ -89,6 +89,9 @@ def test_entry_points_validate_before_launch(S):
     assert L.chunk_stream_create(ctypes.byref(cfg), None, ctypes.byref(h)) == -2
     cfg = S.ChunkStreamConfig(1, 2, 64, 2, 4, 4, 1, 3, -1, 1e4, 0.0)  # boundary_frames > F
     assert L.chunk_stream_create(ctypes.byref(cfg), None, ctypes.byref(h)) == -1
+    for bad in (-1, 9):  # host_io: 0 (off), else 1 to 8 input slots
+        cfg = S.ChunkStreamConfig(1, 2, 64, 2, 4, 4, 1, 1, -1, 1e4, 0.0, 0, 0, bad)
+        assert L.chunk_stream_create(ctypes.byref(cfg), None, ctypes.byref(h)) == -1
     assert L.chunk_stream_end_chunk(None) == -1
     assert L.chunk_stream_destroy(None) == 0
 
