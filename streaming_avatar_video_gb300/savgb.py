@@ -587,6 +587,12 @@ class ChunkStream:
             _check(lib().chunk_stream_destroy(self.handle))
             self.handle = None
 
+    def __enter__(self) -> "ChunkStream":
+        return self
+
+    def __exit__(self, *exc) -> None:
+        self.close()
+
     def __del__(self):
         try:
             self.close()
